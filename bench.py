@@ -1,0 +1,401 @@
+"""Benchmark of the DSA decode step (Lightning Indexer + Top-K + Sparse Flash Attention).
+
+Default workload: BF16 decode, batch 32, context 32768, 64-token pages randomly placed,
+indexer 64 heads x d128, top-K 2048, SFA 128 heads x 576 (bf16).  One step = one
+dsa_fused_decode call: one new token for each of the 32 sequences.
+
+Prints one JSON line:
+  value   decode tokens/s over the timed steps (device clock, inputs resident in HBM)
+  e2e     the same through host buffers (pinned H2D of the step's queries, weights and
+          page metadata + D2H of indices and attention output inside the timed region)
+  roofline  the dominant kernel's algorithmic bytes per launch over its event-timed
+          average duration, against the measured HBM copy bandwidth
+  cpu_baseline  the float64 oracle on the host cores over a bounded sample
+Use --impl reference to time the float64 oracle itself (the reference arm).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import dsa_workloads as W  # noqa: E402
+
+METRIC = "decode tokens/s and µs/step (indexer+SFA) at 1 GB300; % HBM / tensor roofline"
+UNIT = "tokens/s"
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), "measured"
+    return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, 1700.0, "fallback"
+
+
+# ---------------------------------------------------------------------------------------
+# Algorithmic work per launch (bytes that must move at least once; flops of the math)
+# ---------------------------------------------------------------------------------------
+def _visible(wl):
+    lens = wl.seq_lens.astype(np.int64)
+    return np.minimum(wl.q_pos.astype(np.int64) + 1, lens[wl.q_seq]).clip(min=0)
+
+
+def algorithmic(wl):
+    s = wl.spec
+    vis = _visible(wl)
+    T = wl.n_tokens
+    k_elem = 2 if s.idx_dtype == "bf16" else 1
+    k_row = s.idx_dim * k_elem + (4 if s.idx_scale == "per_token" else (s.idx_dim // 32 if s.idx_scale == "mx" else 0))
+    if s.mode == "decode":
+        key_tokens = int(vis.sum())            # every visible key row read once
+    else:
+        key_tokens = int(wl.seq_lens[0])       # the prefix is read once (shared by all rows)
+    q_bytes = T * s.idx_heads * s.idx_dim * k_elem + T * s.idx_heads * 4
+    if s.idx_scale == "per_token":
+        q_bytes += T * 4
+    elif s.idx_scale == "mx":
+        q_bytes += T * s.idx_heads * s.idx_dim // 32
+    sel = np.minimum(vis, s.topk)
+    idx_bytes = T * s.topk * 4
+    score_flops = 2.0 * s.idx_heads * s.idx_dim * float(vis.sum())
+    gather_rows = int(sel.sum())
+    sfa_bytes = gather_rows * 1152 + T * s.sfa_heads * 576 * 2 + T * s.sfa_heads * 512 * 2 + idx_bytes
+    sfa_flops = 2.0 * s.sfa_heads * (576 + 512) * float(sel.sum())
+    meta = wl.block_table.nbytes + wl.seq_lens.nbytes
+    return {
+        "indexer_score": {"bytes": key_tokens * k_row + q_bytes + meta, "flops": score_flops},
+        "indexer_topk": {"bytes": idx_bytes, "flops": 0.0},
+        "sfa": {"bytes": sfa_bytes, "flops": sfa_flops},
+        "sfa_combine": {"bytes": T * s.sfa_heads * 512 * 2, "flops": 0.0},
+        "step": {"bytes": key_tokens * k_row + q_bytes + meta + sfa_bytes, "flops": score_flops + sfa_flops},
+    }
+
+
+# ---------------------------------------------------------------------------------------
+# Clock sampling during the timed region
+# ---------------------------------------------------------------------------------------
+class ClockSampler:
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"dsa_clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------------------
+# Traffic measured by ncu (profiles/traffic.json), used only while the kernel source is
+# unchanged since the capture.
+# ---------------------------------------------------------------------------------------
+KERNEL_SOURCES = {"indexer_score": "indexer_score.cu", "indexer_topk": "topk.cu", "sfa": "sfa.cu",
+                  "sfa_combine": "sfa.cu"}
+
+
+def _src_sha(kernel):
+    path = os.path.join(ROOT, "sparse_attention_decode_dsa_gb300", "csrc", KERNEL_SOURCES[kernel])
+    return hashlib.sha256(open(path, "rb").read()).hexdigest()[:16]
+
+
+def _traffic(kernel, workload, units):
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p)).get(kernel)
+    if not d or d.get("src_sha") != _src_sha(kernel):
+        return None
+    # bytes per unit (key token or gathered row) from the capture, scaled to this launch
+    return d["bytes_per_unit"] * units
+
+
+def _cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def _oracle_sample(wl, budget_s):
+    """Time the float64 oracle over whole query tokens until the budget is spent."""
+    from oracle import dsa_oracle as O
+    n, t0 = 0, time.perf_counter()
+    order = np.random.default_rng(0).permutation(wl.n_tokens)
+    while n < len(order):
+        O.step(wl, int(order[n]))
+        n += 1
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    return n, time.perf_counter() - t0
+
+
+# ---------------------------------------------------------------------------------------
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="bf16_decode", choices=sorted(W.ALL))
+    ap.add_argument("--batch", type=int, default=0, help="override the batch (smaller capture cases)")
+    ap.add_argument("--e2e-steps", type=int, default=0)
+    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    spec = W.ALL[args.workload]
+    if args.batch:
+        assert spec.mode == "decode"
+        lens = spec.seq_lens[:args.batch] if spec.seq_lens else ()
+        spec = W.replace(spec, batch=args.batch, seq_lens=lens, pool_pages=0 if spec.seq_lens else spec.pool_pages)
+    config = {"workload": spec.name, "batch": spec.batch,
+              "context": int(max(spec.seq_lens)) if spec.seq_lens else f"log-uniform{list(spec.len_loguniform)}",
+              "top_k": spec.topk, "index_heads": spec.idx_heads, "index_dim": spec.idx_dim,
+              "index_dtype": spec.idx_dtype + ("" if spec.idx_scale == "none" else "+" + spec.idx_scale),
+              "sfa_heads": spec.sfa_heads, "kv_dim": 576, "page_size": 64, "seed": spec.seed}
+
+    if args.impl == "reference":
+        return run_reference(args, spec, config, world, rank)
+
+    import torch
+    import sparse_attention_decode_dsa_gb300 as dsa
+    from dsa_workloads.device import to_device
+
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+
+    wl = W.make(spec)
+    d = to_device(wl, dev)
+    plan = dsa.Plan(d)
+    T, K, H = wl.n_tokens, spec.topk, spec.sfa_heads
+    out_idx = torch.empty((T, K), dtype=torch.int32, device=dev)
+    out = torch.empty((T, H, 512), dtype=torch.bfloat16, device=dev)
+    ws = dsa.alloc_workspace(plan.ws_fused(), dev)
+    stream = torch.cuda.current_stream(dev)
+    work = algorithmic(wl)
+    l2_bytes = torch.cuda.get_device_properties(dev).L2_cache_size
+    input_bytes = sum(int(t.numel() * t.element_size()) for t in
+                      [d.idx_k, d.kv, d.idx_q, d.sfa_q, d.head_w, d.block_table] if t is not None)
+
+    def step(trace=None):
+        dsa.fused_decode(plan, out_idx, out, ws, stream=stream, trace=trace)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    assert dsa.read_device_error(ws) == 0
+
+    # per-launch events over the timed region
+    traces = []
+    for _ in range(args.steps):
+        tr = dsa.Trace()
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(2 * dsa.DSA_TRACE_MAX)]
+        for i in range(dsa.DSA_TRACE_MAX):
+            tr.begin[i] = evs[2 * i].cuda_event
+            tr.end[i] = evs[2 * i + 1].cuda_event
+        traces.append((tr, evs))
+    for _, evs in traces:   # torch creates CUDA events lazily, on their first record
+        for e in evs:
+            e.record(stream)
+    torch.cuda.synchronize()
+
+    clocks = ClockSampler(torch.cuda.current_device() if world == 1 else local_rank)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    t_begin = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_begin.record(stream)
+    for tr, _ in traces:
+        step(tr)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    clk = clocks.stop()
+    total_ms = t_begin.elapsed_time(t_end)
+    if dist:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    assert dsa.read_device_error(ws) == 0
+
+    per_kernel = {}
+    launches = 0
+    for tr, evs in traces:
+        for i in range(tr.n_recorded):
+            name = tr.name[i].decode()
+            per_kernel.setdefault(name, []).append(evs[2 * i].elapsed_time(evs[2 * i + 1]))
+            launches += 1
+    kstats = {k: {"launches": len(v), "avg_us": 1e3 * sum(v) / len(v), "total_ms": sum(v)}
+              for k, v in per_kernel.items()}
+    ktotal = sum(s["total_ms"] for s in kstats.values())
+    for s in kstats.values():
+        s["share"] = s["total_ms"] / ktotal if ktotal else None
+    dom = max(kstats, key=lambda k: kstats[k]["total_ms"])
+    hbm_gbs, bf16_tf, bf16_tf_sust, peak_src = _peaks()
+    dom_work = work.get(dom, {"bytes": 0, "flops": 0})
+    avg_s = kstats[dom]["avg_us"] * 1e-6
+    units = int(_visible(wl).sum()) if dom == "indexer_score" else int(np.minimum(_visible(wl), K).sum())
+    traffic = _traffic(dom, spec.name, units)
+    roofline = {"kernel": dom, "bound": "hbm", "achieved": dom_work["bytes"] / avg_s / 1e9, "peak": hbm_gbs,
+                "unit": "GB/s", "frac": dom_work["bytes"] / avg_s / 1e9 / hbm_gbs,
+                "traffic": traffic, "algorithmic_bytes": dom_work["bytes"],
+                "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs, burst copy)" if peak_src == "measured" else "fallback 6.8 TB/s",
+                "frac_of_8TBps_nominal": dom_work["bytes"] / avg_s / 1e9 / 8000.0}
+
+    ms_per_step = total_ms / args.steps
+    value = world * T * args.steps / (total_ms * 1e-3)
+
+    # ---- end to end through host buffers ----------------------------------------------
+    e2e_steps = args.e2e_steps or max(10, args.steps // 4)
+    pin = lambda t: t.cpu().pin_memory()  # noqa: E731
+    h_in = [pin(d.idx_q), pin(d.head_w), pin(d.sfa_q), pin(d.block_table), pin(d.seq_lens)]
+    dv_in = [d.idx_q, d.head_w, d.sfa_q, d.block_table, d.seq_lens]
+    if d.idx_q_scale is not None:
+        h_in.append(pin(d.idx_q_scale))
+        dv_in.append(d.idx_q_scale)
+    h_out = [torch.empty(out_idx.shape, dtype=out_idx.dtype).pin_memory(),
+             torch.empty(out.shape, dtype=out.dtype).pin_memory()]
+    h2d = sum(t.numel() * t.element_size() for t in h_in)
+    d2h = sum(t.numel() * t.element_size() for t in h_out)
+    torch.cuda.synchronize()
+    e_b = torch.cuda.Event(enable_timing=True)
+    e_e = torch.cuda.Event(enable_timing=True)
+    e_b.record(stream)
+    for _ in range(e2e_steps):
+        for h, dv in zip(h_in, dv_in):
+            dv.copy_(h, non_blocking=True)
+        step()
+        h_out[0].copy_(out_idx, non_blocking=True)
+        h_out[1].copy_(out, non_blocking=True)
+    e_e.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e_b.elapsed_time(e_e)
+    e2e_val = world * T * e2e_steps / (e2e_ms * 1e-3)
+    assert dsa.read_device_error(ws) == 0
+
+    # ---- oracle on the host cores --------------------------------------------------------
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        n, secs = _oracle_sample(wl, args.cpu_budget)
+        cpu = {"value": n / secs, "unit": UNIT, "cores": _cores(), "kind": "oracle",
+               "sample": f"{n} of {T} query tokens of {spec.name} (whole indexer + top-K + attention "
+                         f"per token), float64 NumPy, {secs:.1f} s"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "us_per_step": 1e3 * ms_per_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded; integer-valued indexer inputs, N(0,1) bf16 latent KV)",
+            "config": {**config, "l2": f"no flush: per-step inputs {input_bytes / 1e6:.0f} MB > L2 {l2_bytes / 1e6:.0f} MB",
+                       "parallelism": "replicas" if world > 1 else "single GPU"},
+            "roofline": roofline,
+            "kernels": kstats,
+            "gpu_launches": launches,
+            "step_algorithmic_bytes": work["step"]["bytes"],
+            "step_frac_hbm": work["step"]["bytes"] / (ms_per_step * 1e-3) / 1e9 / hbm_gbs,
+            "e2e": {"value": e2e_val, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "steps": e2e_steps, "ms_per_step": e2e_ms / e2e_steps},
+            "cpu_baseline": cpu,
+            "clocks": clk,
+        }
+        print(json.dumps(line))
+    if dist:
+        dist.destroy_process_group()
+
+
+def run_reference(args, spec, config, world, rank):
+    """The reference arm: the float64 oracle on the host cores, a bounded sample per step."""
+    if rank != 0:
+        return
+    wl = W.make(spec)
+    from oracle import dsa_oracle as O
+    order = np.random.default_rng(0).permutation(wl.n_tokens)
+    per_step = max(1, min(wl.n_tokens, int(os.environ.get("DSA_REF_TOKENS_PER_STEP", "1"))))
+    times = []
+    k = 0
+    for i in range(args.warmup + args.steps):
+        t0 = time.perf_counter()
+        for _ in range(per_step):
+            O.step(wl, int(order[k % len(order)]))
+            k += 1
+        if i >= args.warmup:
+            times.append(time.perf_counter() - t0)
+    total = sum(times)
+    value = per_step * len(times) / total
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / len(times),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded)", "config": config,
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": _cores(), "kind": "oracle",
+                             "sample": f"{per_step} query token(s) of {spec.name} per step (whole indexer + "
+                                       f"top-K + attention), float64 NumPy"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+
+
+if __name__ == "__main__":
+    main()

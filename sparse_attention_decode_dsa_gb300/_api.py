@@ -1,0 +1,142 @@
+"""Marshalling from torch tensors to the C structs of include/dsa.h and back."""
+from __future__ import annotations
+
+import ctypes as C
+from dataclasses import dataclass
+from typing import Optional
+
+import torch
+
+from . import (lib, _check, PageTable, Tokens, IndexCache, IndexerArgs, LatentCache, SfaArgs, Trace,
+               DSA_BF16, DSA_E4M3, DSA_SCALE_NONE, DSA_SCALE_PER_TOKEN_F32, DSA_SCALE_MX_E8M0_G32,
+               DSA_ACT_IDENTITY)
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    if t is None:
+        return None
+    return C.c_void_p(t.data_ptr())
+
+
+def _i32_host_ptr(t: Optional[torch.Tensor]):
+    if t is None:
+        return None
+    assert t.device.type == "cpu" and t.dtype == torch.int32 and t.is_contiguous()
+    return C.cast(C.c_void_p(t.data_ptr()), C.POINTER(C.c_int32))
+
+
+def _stream_ptr(stream: Optional[torch.cuda.Stream]):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return C.c_void_p(s.cuda_stream)
+
+
+@dataclass
+class DeviceInputs:
+    """Device-resident inputs of one DSA step (caller-owned torch tensors).
+
+    Storage dtypes: bf16 tensors may be torch.bfloat16 or raw uint16/int16 bits; e4m3
+    tensors are torch.float8_e4m3fn or uint8 bytes; E8M0 scales are uint8.
+    """
+    block_table: torch.Tensor            # int32 [B, max_pages] (device)
+    seq_lens: torch.Tensor               # int32 [B] (device)
+    seq_lens_host: torch.Tensor          # int32 [B] (host)
+    num_pages: int
+    idx_q: torch.Tensor                  # [T, H_I, d]
+    head_w: torch.Tensor                 # f32 [T, H_I]
+    idx_k: torch.Tensor                  # [num_pages, 64, d]
+    top_k: int
+    idx_q_scale: Optional[torch.Tensor] = None
+    idx_k_scale: Optional[torch.Tensor] = None
+    kv: Optional[torch.Tensor] = None    # bf16 [num_pages, 64, 576]
+    sfa_q: Optional[torch.Tensor] = None  # bf16 [T, H, 576]
+    softmax_scale: float = 576 ** -0.5
+    token_seq: Optional[torch.Tensor] = None
+    token_pos: Optional[torch.Tensor] = None
+    token_seq_host: Optional[torch.Tensor] = None
+    token_pos_host: Optional[torch.Tensor] = None
+    act: int = DSA_ACT_IDENTITY
+
+    @property
+    def n_tokens(self) -> int:
+        return int(self.idx_q.shape[0]) if self.idx_q is not None else int(self.sfa_q.shape[0])
+
+
+class Plan:
+    """C structs for one set of device inputs, kept alive together with the tensors."""
+
+    def __init__(self, d: DeviceInputs):
+        self.d = d
+        B, maxp = d.block_table.shape
+        self.pages = PageTable(_ptr(d.block_table), _ptr(d.seq_lens), _i32_host_ptr(d.seq_lens_host),
+                               B, maxp, 64, d.num_pages)
+        self.tokens = Tokens(d.n_tokens, _ptr(d.token_seq), _ptr(d.token_pos),
+                             _i32_host_ptr(d.token_seq_host), _i32_host_ptr(d.token_pos_host))
+        dt = DSA_BF16 if d.idx_k.element_size() == 2 else DSA_E4M3
+        if d.idx_k_scale is None:
+            sk = DSA_SCALE_NONE
+        elif d.idx_k_scale.dtype == torch.float32:
+            sk = DSA_SCALE_PER_TOKEN_F32
+        else:
+            sk = DSA_SCALE_MX_E8M0_G32
+        self.icache = IndexCache(_ptr(d.idx_k), _ptr(d.idx_k_scale), dt, sk, int(d.idx_k.shape[-1]))
+        self.iargs = IndexerArgs(_ptr(d.idx_q), _ptr(d.idx_q_scale), dt, sk, _ptr(d.head_w),
+                                 int(d.idx_q.shape[1]), int(d.top_k), int(d.act))
+        self.lcache = LatentCache(_ptr(d.kv), 576, 512) if d.kv is not None else None
+        self.sargs = (SfaArgs(_ptr(d.sfa_q), int(d.sfa_q.shape[1]), float(d.softmax_scale))
+                      if d.sfa_q is not None else None)
+
+    def ws_indexer(self) -> int:
+        return lib.dsa_indexer_workspace_size(C.byref(self.iargs), C.byref(self.icache),
+                                              C.byref(self.pages), C.byref(self.tokens))
+
+    def ws_sfa(self) -> int:
+        return lib.dsa_sparse_attn_workspace_size(C.byref(self.sargs), C.byref(self.pages),
+                                                  C.byref(self.tokens), int(self.d.top_k))
+
+    def ws_fused(self) -> int:
+        return lib.dsa_fused_workspace_size(C.byref(self.iargs), C.byref(self.icache), C.byref(self.sargs),
+                                            C.byref(self.pages), C.byref(self.tokens))
+
+
+def workspace_size(plan: Plan, which: str = "fused") -> int:
+    return {"fused": plan.ws_fused, "indexer": plan.ws_indexer, "sfa": plan.ws_sfa}[which]()
+
+
+def alloc_workspace(nbytes: int, device="cuda") -> torch.Tensor:
+    """A zeroed, 256-byte aligned workspace (torch allocations are 512-byte aligned)."""
+    return torch.zeros(max(nbytes, 256), dtype=torch.uint8, device=device)
+
+
+def indexer_topk(plan: Plan, out_idx: torch.Tensor, ws: torch.Tensor, out_score: Optional[torch.Tensor] = None,
+                 stream=None, trace: Optional[Trace] = None):
+    _check(lib.dsa_indexer_topk(C.byref(plan.iargs), C.byref(plan.icache), C.byref(plan.pages),
+                                C.byref(plan.tokens), _ptr(out_idx), _ptr(out_score), _ptr(ws),
+                                ws.numel() * ws.element_size(), _stream_ptr(stream),
+                                C.byref(trace) if trace is not None else None), "dsa_indexer_topk")
+
+
+def sparse_attn(plan: Plan, idx: torch.Tensor, out: torch.Tensor, ws: torch.Tensor, stream=None,
+                trace: Optional[Trace] = None):
+    _check(lib.dsa_sparse_attn(C.byref(plan.sargs), C.byref(plan.lcache), C.byref(plan.pages),
+                               C.byref(plan.tokens), _ptr(idx), int(idx.shape[-1]), _ptr(out), _ptr(ws),
+                               ws.numel() * ws.element_size(), _stream_ptr(stream),
+                               C.byref(trace) if trace is not None else None), "dsa_sparse_attn")
+
+
+def fused_decode(plan: Plan, out_idx: torch.Tensor, out: torch.Tensor, ws: torch.Tensor, stream=None,
+                 trace: Optional[Trace] = None):
+    _check(lib.dsa_fused_decode(C.byref(plan.iargs), C.byref(plan.icache), C.byref(plan.sargs),
+                                C.byref(plan.lcache), C.byref(plan.pages), C.byref(plan.tokens),
+                                _ptr(out_idx), _ptr(out), _ptr(ws), ws.numel() * ws.element_size(),
+                                _stream_ptr(stream), C.byref(trace) if trace is not None else None),
+           "dsa_fused_decode")
+
+
+def read_device_error(ws: torch.Tensor, stream=None) -> int:
+    v = C.c_uint32(0)
+    _check(lib.dsa_read_device_error(_ptr(ws), C.byref(v), _stream_ptr(stream)), "dsa_read_device_error")
+    return int(v.value)
+
+
+def clear_device_error(ws: torch.Tensor, stream=None):
+    _check(lib.dsa_clear_device_error(_ptr(ws), _stream_ptr(stream)), "dsa_clear_device_error")

@@ -1,0 +1,390 @@
+// Host side of the C ABI declared in include/dsa.h: argument checks, launch planning,
+// workspace carving and kernel launches.  No allocation, no host synchronisation
+// except in dsa_read_device_error().
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <string>
+
+#include "dsa_internal.h"
+
+namespace dsa {
+namespace {
+
+thread_local std::string g_last_error;
+
+dsa_status_t fail(dsa_status_t st, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return st;
+}
+
+dsa_status_t cuda_fail(cudaError_t e, const char* what) {
+  return fail(DSA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+constexpr size_t kAlign = 256;
+size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+int num_sms() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return 148;
+  return n;
+}
+
+// ---- shared checks -------------------------------------------------------------------
+dsa_status_t check_pages_tokens(const dsa_page_table_t* pg, const dsa_tokens_t* tk, int32_t* max_visible) {
+  if (!pg || !tk) return fail(DSA_ERR_INVALID_ARG, "page table or tokens is NULL");
+  if (pg->page_size != kPage) return fail(DSA_ERR_UNSUPPORTED, "page_size must be 64 (got %d)", pg->page_size);
+  if (pg->batch < 1 || pg->max_pages_per_seq < 1 || pg->num_pages < 1)
+    return fail(DSA_ERR_INVALID_ARG, "batch, max_pages_per_seq and num_pages must be >= 1");
+  if (!pg->block_table || !pg->seq_lens || !pg->seq_lens_host)
+    return fail(DSA_ERR_INVALID_ARG, "block_table, seq_lens and seq_lens_host are required");
+  if (tk->n_tokens < 1) return fail(DSA_ERR_INVALID_ARG, "n_tokens must be >= 1");
+  if (!tk->token_seq && tk->n_tokens != pg->batch)
+    return fail(DSA_ERR_INVALID_ARG, "token_seq NULL requires n_tokens == batch");
+  if (tk->token_seq && !tk->token_seq_host)
+    return fail(DSA_ERR_INVALID_ARG, "token_seq_host is required with token_seq");
+  if (tk->token_pos && !tk->token_pos_host)
+    return fail(DSA_ERR_INVALID_ARG, "token_pos_host is required with token_pos");
+  const int64_t cap = (int64_t)pg->max_pages_per_seq * kPage;
+  for (int b = 0; b < pg->batch; ++b) {
+    const int32_t L = pg->seq_lens_host[b];
+    if (L < 0 || L > cap)
+      return fail(DSA_ERR_INVALID_ARG, "seq_lens_host[%d] = %d outside [0, %lld]", b, L, (long long)cap);
+  }
+  int32_t mv = 0;
+  for (int i = 0; i < tk->n_tokens; ++i) {
+    const int b = tk->token_seq ? tk->token_seq_host[i] : i;
+    if (b < 0 || b >= pg->batch) return fail(DSA_ERR_INVALID_ARG, "token_seq_host[%d] = %d outside [0, batch)", i, b);
+    const int32_t L = pg->seq_lens_host[b];
+    const int32_t pos = tk->token_pos ? tk->token_pos_host[i] : L - 1;
+    if (pos < -1) return fail(DSA_ERR_INVALID_ARG, "token_pos_host[%d] = %d < -1", i, pos);
+    const int32_t n = pos + 1 < L ? pos + 1 : L;
+    if (n > mv) mv = n;
+  }
+  if (mv > kMaxVisible)
+    return fail(DSA_ERR_UNSUPPORTED, "a token sees %d positions; this build selects from at most %d", mv, kMaxVisible);
+  *max_visible = mv;
+  return DSA_OK;
+}
+
+TokenView token_view(const dsa_page_table_t* pg, const dsa_tokens_t* tk, int32_t max_visible) {
+  TokenView tv;
+  tv.max_visible = max_visible;
+  tv.token_seq = tk->token_seq;
+  tv.token_pos = tk->token_pos;
+  tv.seq_lens = pg->seq_lens;
+  tv.block_table = pg->block_table;
+  tv.batch = pg->batch;
+  tv.max_pages = pg->max_pages_per_seq;
+  tv.num_pages = pg->num_pages;
+  tv.n_tokens = tk->n_tokens;
+  return tv;
+}
+
+dsa_status_t check_indexer(const dsa_indexer_args_t* a, const dsa_index_cache_t* c) {
+  if (!a || !c) return fail(DSA_ERR_INVALID_ARG, "indexer args or cache is NULL");
+  if (!a->q || !a->head_w || !c->data) return fail(DSA_ERR_INVALID_ARG, "q, head_w and cache data are required");
+  if (a->n_heads < 1 || a->n_heads > kMaxIdxHeads)
+    return fail(DSA_ERR_UNSUPPORTED, "indexer n_heads must be in [1, %d] (got %d)", kMaxIdxHeads, a->n_heads);
+  if (c->dim != 64 && c->dim != 128) return fail(DSA_ERR_UNSUPPORTED, "index dim must be 64 or 128 (got %d)", c->dim);
+  if (a->top_k < 1 || a->top_k > kMaxTopK)
+    return fail(DSA_ERR_UNSUPPORTED, "top_k must be in [1, %d] (got %d)", kMaxTopK, a->top_k);
+  if (a->act != DSA_ACT_IDENTITY && a->act != DSA_ACT_RELU) return fail(DSA_ERR_INVALID_ARG, "unknown activation");
+  if (a->q_dtype != c->dtype || a->q_scale_kind != c->scale_kind)
+    return fail(DSA_ERR_UNSUPPORTED, "query and cache must share dtype and scale kind");
+  if (c->dtype == DSA_BF16) {
+    if (c->scale_kind != DSA_SCALE_NONE) return fail(DSA_ERR_UNSUPPORTED, "bf16 index cache takes no scales");
+  } else if (c->dtype == DSA_E4M3) {
+    if (c->scale_kind != DSA_SCALE_PER_TOKEN_F32 && c->scale_kind != DSA_SCALE_MX_E8M0_G32)
+      return fail(DSA_ERR_UNSUPPORTED, "e4m3 index cache needs per-token f32 or MX E8M0 scales");
+    if (!c->scale || !a->q_scale) return fail(DSA_ERR_INVALID_ARG, "e4m3 modes need q_scale and cache scale");
+  } else {
+    return fail(DSA_ERR_INVALID_ARG, "unknown index dtype");
+  }
+  return DSA_OK;
+}
+
+dsa_status_t check_sfa(const dsa_sfa_args_t* a, const dsa_latent_cache_t* c) {
+  if (!a) return fail(DSA_ERR_INVALID_ARG, "sfa args is NULL");
+  if (!a->q) return fail(DSA_ERR_INVALID_ARG, "sfa q is NULL");
+  if (a->n_heads < 1 || a->n_heads > kMaxSfaHeads)
+    return fail(DSA_ERR_UNSUPPORTED, "sfa n_heads must be in [1, %d] (got %d)", kMaxSfaHeads, a->n_heads);
+  if (!std::isfinite(a->softmax_scale)) return fail(DSA_ERR_INVALID_ARG, "softmax_scale must be finite");
+  if (c) {
+    if (!c->data) return fail(DSA_ERR_INVALID_ARG, "latent cache data is NULL");
+    if (c->dim != kLatentDim || c->v_dim != kValueDim)
+      return fail(DSA_ERR_UNSUPPORTED, "latent rows must be 576 wide with a 512-wide value (got %d/%d)", c->dim, c->v_dim);
+  }
+  return DSA_OK;
+}
+
+// ---- workspace plans ------------------------------------------------------------------
+struct IndexerPlan {
+  int32_t max_visible;
+  int64_t score_stride;
+  size_t score_bytes;
+};
+
+IndexerPlan plan_indexer(int32_t max_visible, int32_t n_tokens) {
+  IndexerPlan p;
+  p.max_visible = max_visible;
+  p.score_stride = ((int64_t)max_visible + 63) / 64 * 64;
+  if (p.score_stride == 0) p.score_stride = 64;
+  p.score_bytes = align_up((size_t)n_tokens * p.score_stride * sizeof(float));
+  return p;
+}
+
+struct SfaPlan {
+  int32_t n_splits, split_len;
+  size_t part_o_bytes, part_lse_bytes;
+};
+
+SfaPlan plan_sfa(int32_t n_tokens, int32_t n_heads, int32_t top_k) {
+  SfaPlan p;
+  const int tiles = (top_k + 63) / 64;
+  const int units = n_tokens * ((n_heads + 63) / 64);
+  int s = num_sms() / (units > 0 ? units : 1);
+  if (s < 1) s = 1;
+  if (s > tiles) s = tiles;
+  if (s > 16) s = 16;
+  p.n_splits = s;
+  p.split_len = (tiles + s - 1) / s * 64;
+  p.n_splits = (tiles * 64 + p.split_len - 1) / p.split_len;  // drop empty splits
+  if (p.n_splits > 1) {
+    p.part_o_bytes = align_up((size_t)n_tokens * p.n_splits * n_heads * kValueDim * sizeof(float));
+    p.part_lse_bytes = align_up((size_t)n_tokens * p.n_splits * n_heads * sizeof(float));
+  } else {
+    p.part_o_bytes = p.part_lse_bytes = 0;
+  }
+  return p;
+}
+
+dsa_status_t check_ws(void* ws, size_t ws_bytes, size_t need) {
+  if (!ws) return fail(DSA_ERR_WORKSPACE, "workspace is NULL");
+  if (((uintptr_t)ws) % kAlign) return fail(DSA_ERR_WORKSPACE, "workspace must be 256-byte aligned");
+  if (ws_bytes < need)
+    return fail(DSA_ERR_WORKSPACE, "workspace of %zu bytes is below the %zu needed", ws_bytes, need);
+  return DSA_OK;
+}
+
+// ---- tracing -----------------------------------------------------------------------
+struct Tracer {
+  dsa_trace_t* t;
+  cudaStream_t s;
+  int n = 0;
+  explicit Tracer(dsa_trace_t* tr, cudaStream_t st) : t(tr), s(st) {
+    if (t) t->n_recorded = 0;
+  }
+  void begin() {
+    if (t && n < DSA_TRACE_MAX && t->begin[n]) cudaEventRecord((cudaEvent_t)t->begin[n], s);
+  }
+  void end(const char* name) {
+    if (t && n < DSA_TRACE_MAX) {
+      if (t->end[n]) cudaEventRecord((cudaEvent_t)t->end[n], s);
+      t->name[n] = name;
+      t->n_recorded = ++n;
+    }
+  }
+};
+
+// ---- the three passes -----------------------------------------------------------------
+dsa_status_t run_indexer(const dsa_indexer_args_t* a, const dsa_index_cache_t* c,
+                         const dsa_page_table_t* pg, const dsa_tokens_t* tk, const IndexerPlan& ip,
+                         int32_t* out_idx, float* out_score, uint8_t* ws, cudaStream_t s, Tracer& tr) {
+  uint32_t* err = (uint32_t*)ws;
+  float* scores = (float*)(ws + kAlign);
+  ScoreParams sp;
+  sp.tv = token_view(pg, tk, ip.max_visible);
+  sp.q = a->q;
+  sp.q_scale = a->q_scale;
+  sp.head_w = a->head_w;
+  sp.k = c->data;
+  sp.k_scale = c->scale;
+  sp.scores = scores;
+  sp.score_stride = ip.score_stride;
+  sp.err = err;
+  sp.n_heads = a->n_heads;
+  sp.dim = c->dim;
+  sp.act = (int)a->act;
+  sp.max_page_blocks = (ip.max_visible + kPage - 1) / kPage;
+  if (sp.max_page_blocks > 0) {
+    tr.begin();
+    cudaError_t e = launch_score(sp, c->dtype, c->scale_kind, s);
+    tr.end("indexer_score");
+    if (e != cudaSuccess) return cuda_fail(e, "indexer score launch");
+  }
+  TopkParams tp;
+  tp.tv = sp.tv;
+  tp.scores = scores;
+  tp.score_stride = ip.score_stride;
+  tp.out_idx = out_idx;
+  tp.out_score = out_score;
+  tp.err = err;
+  tp.top_k = a->top_k;
+  tr.begin();
+  cudaError_t e = launch_topk(tp, ip.max_visible, s);
+  tr.end("indexer_topk");
+  if (e != cudaSuccess) return cuda_fail(e, "top-k launch");
+  return DSA_OK;
+}
+
+dsa_status_t run_sfa(const dsa_sfa_args_t* a, const dsa_latent_cache_t* c, const dsa_page_table_t* pg,
+                     const dsa_tokens_t* tk, int32_t max_visible, const int32_t* idx, int32_t top_k, void* out,
+                     uint8_t* ws, const SfaPlan& sp_, cudaStream_t s, Tracer& tr) {
+  SfaParams p;
+  p.tv = token_view(pg, tk, max_visible);
+  p.q = (const uint16_t*)a->q;
+  p.kv = (const uint16_t*)c->data;
+  p.idx = idx;
+  p.out = (uint16_t*)out;
+  p.part_o = sp_.n_splits > 1 ? (float*)(ws + kAlign) : nullptr;
+  p.part_lse = sp_.n_splits > 1 ? (float*)(ws + kAlign + sp_.part_o_bytes) : nullptr;
+  p.err = (uint32_t*)ws;
+  p.n_heads = a->n_heads;
+  p.top_k = top_k;
+  p.n_splits = sp_.n_splits;
+  p.split_len = sp_.split_len;
+  p.scale_log2 = a->softmax_scale * 1.4426950408889634f;
+  tr.begin();
+  cudaError_t e = launch_sfa(p, s);
+  tr.end("sfa");
+  if (e != cudaSuccess) return cuda_fail(e, "sparse attention launch");
+  if (p.n_splits > 1) {
+    tr.begin();
+    e = launch_sfa_combine(p, s);
+    tr.end("sfa_combine");
+    if (e != cudaSuccess) return cuda_fail(e, "split combine launch");
+  }
+  return DSA_OK;
+}
+
+}  // namespace
+}  // namespace dsa
+
+using namespace dsa;
+
+extern "C" {
+
+size_t dsa_indexer_workspace_size(const dsa_indexer_args_t* args, const dsa_index_cache_t* cache,
+                                  const dsa_page_table_t* pages, const dsa_tokens_t* tokens) {
+  int32_t mv = 0;
+  if (check_indexer(args, cache) != DSA_OK || check_pages_tokens(pages, tokens, &mv) != DSA_OK) return 0;
+  return kAlign + plan_indexer(mv, tokens->n_tokens).score_bytes;
+}
+
+dsa_status_t dsa_indexer_topk(const dsa_indexer_args_t* args, const dsa_index_cache_t* cache,
+                              const dsa_page_table_t* pages, const dsa_tokens_t* tokens, int32_t* out_idx,
+                              float* out_score, void* ws, size_t ws_bytes, dsa_stream_t stream,
+                              dsa_trace_t* trace) {
+  dsa_status_t st = check_indexer(args, cache);
+  if (st != DSA_OK) return st;
+  int32_t mv = 0;
+  if ((st = check_pages_tokens(pages, tokens, &mv)) != DSA_OK) return st;
+  if (!out_idx) return fail(DSA_ERR_INVALID_ARG, "out_idx is NULL");
+  IndexerPlan ip = plan_indexer(mv, tokens->n_tokens);
+  if ((st = check_ws(ws, ws_bytes, kAlign + ip.score_bytes)) != DSA_OK) return st;
+  Tracer tr(trace, (cudaStream_t)stream);
+  return run_indexer(args, cache, pages, tokens, ip, out_idx, out_score, (uint8_t*)ws, (cudaStream_t)stream, tr);
+}
+
+size_t dsa_sparse_attn_workspace_size(const dsa_sfa_args_t* args, const dsa_page_table_t* pages,
+                                      const dsa_tokens_t* tokens, int32_t top_k) {
+  int32_t mv = 0;
+  if (check_sfa(args, nullptr) != DSA_OK || check_pages_tokens(pages, tokens, &mv) != DSA_OK) return 0;
+  if (top_k < 1 || top_k > kMaxTopK) return 0;
+  SfaPlan sp = plan_sfa(tokens->n_tokens, args->n_heads, top_k);
+  return kAlign + sp.part_o_bytes + sp.part_lse_bytes;
+}
+
+dsa_status_t dsa_sparse_attn(const dsa_sfa_args_t* args, const dsa_latent_cache_t* cache,
+                             const dsa_page_table_t* pages, const dsa_tokens_t* tokens, const int32_t* idx,
+                             int32_t top_k, void* out, void* ws, size_t ws_bytes, dsa_stream_t stream,
+                             dsa_trace_t* trace) {
+  dsa_status_t st = check_sfa(args, cache);
+  if (st != DSA_OK) return st;
+  if (!cache) return fail(DSA_ERR_INVALID_ARG, "latent cache is NULL");
+  int32_t mv = 0;
+  if ((st = check_pages_tokens(pages, tokens, &mv)) != DSA_OK) return st;
+  if (!idx || !out) return fail(DSA_ERR_INVALID_ARG, "idx and out are required");
+  if (top_k < 1 || top_k > kMaxTopK) return fail(DSA_ERR_UNSUPPORTED, "top_k must be in [1, %d]", kMaxTopK);
+  SfaPlan sp = plan_sfa(tokens->n_tokens, args->n_heads, top_k);
+  if ((st = check_ws(ws, ws_bytes, kAlign + sp.part_o_bytes + sp.part_lse_bytes)) != DSA_OK) return st;
+  Tracer tr(trace, (cudaStream_t)stream);
+  return run_sfa(args, cache, pages, tokens, mv, idx, top_k, out, (uint8_t*)ws, sp, (cudaStream_t)stream, tr);
+}
+
+size_t dsa_fused_workspace_size(const dsa_indexer_args_t* iargs, const dsa_index_cache_t* icache,
+                                const dsa_sfa_args_t* sargs, const dsa_page_table_t* pages,
+                                const dsa_tokens_t* tokens) {
+  int32_t mv = 0;
+  if (check_indexer(iargs, icache) != DSA_OK || check_sfa(sargs, nullptr) != DSA_OK ||
+      check_pages_tokens(pages, tokens, &mv) != DSA_OK)
+    return 0;
+  IndexerPlan ip = plan_indexer(mv, tokens->n_tokens);
+  SfaPlan sp = plan_sfa(tokens->n_tokens, sargs->n_heads, iargs->top_k);
+  const size_t sfa_b = sp.part_o_bytes + sp.part_lse_bytes;
+  return kAlign + (ip.score_bytes > sfa_b ? ip.score_bytes : sfa_b);  // the passes reuse one region
+}
+
+dsa_status_t dsa_fused_decode(const dsa_indexer_args_t* iargs, const dsa_index_cache_t* icache,
+                              const dsa_sfa_args_t* sargs, const dsa_latent_cache_t* lcache,
+                              const dsa_page_table_t* pages, const dsa_tokens_t* tokens, int32_t* out_idx,
+                              void* out, void* ws, size_t ws_bytes, dsa_stream_t stream, dsa_trace_t* trace) {
+  dsa_status_t st = check_indexer(iargs, icache);
+  if (st != DSA_OK) return st;
+  if ((st = check_sfa(sargs, lcache)) != DSA_OK) return st;
+  if (!lcache) return fail(DSA_ERR_INVALID_ARG, "latent cache is NULL");
+  int32_t mv = 0;
+  if ((st = check_pages_tokens(pages, tokens, &mv)) != DSA_OK) return st;
+  if (!out_idx || !out) return fail(DSA_ERR_INVALID_ARG, "out_idx and out are required");
+  IndexerPlan ip = plan_indexer(mv, tokens->n_tokens);
+  SfaPlan sp = plan_sfa(tokens->n_tokens, sargs->n_heads, iargs->top_k);
+  const size_t sfa_b = sp.part_o_bytes + sp.part_lse_bytes;
+  if ((st = check_ws(ws, ws_bytes, kAlign + (ip.score_bytes > sfa_b ? ip.score_bytes : sfa_b))) != DSA_OK)
+    return st;
+  Tracer tr(trace, (cudaStream_t)stream);
+  if ((st = run_indexer(iargs, icache, pages, tokens, ip, out_idx, nullptr, (uint8_t*)ws, (cudaStream_t)stream,
+                        tr)) != DSA_OK)
+    return st;
+  return run_sfa(sargs, lcache, pages, tokens, mv, out_idx, iargs->top_k, out, (uint8_t*)ws, sp,
+                 (cudaStream_t)stream, tr);
+}
+
+dsa_status_t dsa_read_device_error(const void* ws, uint32_t* err, dsa_stream_t stream) {
+  if (!ws || !err) return fail(DSA_ERR_INVALID_ARG, "ws and err are required");
+  cudaError_t e = cudaMemcpyAsync(err, ws, sizeof(uint32_t), cudaMemcpyDeviceToHost, (cudaStream_t)stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize((cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "reading the device error word");
+  return DSA_OK;
+}
+
+dsa_status_t dsa_clear_device_error(void* ws, dsa_stream_t stream) {
+  if (!ws) return fail(DSA_ERR_INVALID_ARG, "ws is NULL");
+  cudaError_t e = cudaMemsetAsync(ws, 0, sizeof(uint32_t), (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "clearing the device error word");
+  return DSA_OK;
+}
+
+const char* dsa_status_string(dsa_status_t s) {
+  switch (s) {
+    case DSA_OK: return "DSA_OK";
+    case DSA_ERR_INVALID_ARG: return "DSA_ERR_INVALID_ARG";
+    case DSA_ERR_UNSUPPORTED: return "DSA_ERR_UNSUPPORTED";
+    case DSA_ERR_WORKSPACE: return "DSA_ERR_WORKSPACE";
+    case DSA_ERR_CUDA: return "DSA_ERR_CUDA";
+  }
+  return "DSA_ERR_UNKNOWN";
+}
+
+const char* dsa_last_error_message(void) { return g_last_error.c_str(); }
+
+int32_t dsa_abi_version(void) { return DSA_ABI_VERSION; }
+
+}  // extern "C"

@@ -1,0 +1,73 @@
+// Internal declarations shared by the host API and the kernel translation units.
+#pragma once
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/dsa.h"
+
+namespace dsa {
+
+constexpr int kPage = 64;
+constexpr int kMaxTopK = 2048;
+constexpr int kMaxIdxHeads = 64;
+constexpr int kMaxSfaHeads = 128;
+constexpr int kLatentDim = 576;
+constexpr int kValueDim = 512;
+constexpr int kTopkCluster = 8;              // CTAs cooperating on one row's Top-K
+constexpr int kMaxTopkChunk = 32768;         // scores one Top-K CTA holds in shared memory
+constexpr int kMaxVisible = kTopkCluster * kMaxTopkChunk;  // longest row the Top-K handles
+
+// Everything a kernel needs to locate a token's row, sequence and visible range.
+struct TokenView {
+  const int32_t* token_seq;  // may be null: token i is batch row i
+  const int32_t* token_pos;  // may be null: seq_len - 1
+  const int32_t* seq_lens;
+  const int32_t* block_table;
+  int32_t batch, max_pages, num_pages, n_tokens;
+  int32_t max_visible;       // host-planned bound on any token's visible count
+};
+
+// Score pass: one row per query token; scores[row * stride + t] for visible t.
+struct ScoreParams {
+  TokenView tv;
+  const void* q;           // [T, H, d]
+  const void* q_scale;     // null | f32 [T] | u8 [T, H, d/32]
+  const float* head_w;     // [T, H]
+  const void* k;           // [num_pages, 64, d]
+  const void* k_scale;     // null | f32 [num_pages, 64] | u8 [num_pages, 64, d/32]
+  float* scores;           // workspace
+  int64_t score_stride;
+  uint32_t* err;
+  int32_t n_heads, dim, act, max_page_blocks;
+};
+
+struct TopkParams {
+  TokenView tv;
+  const float* scores;
+  int64_t score_stride;
+  int32_t* out_idx;
+  float* out_score;  // may be null
+  uint32_t* err;
+  int32_t top_k;
+};
+
+struct SfaParams {
+  TokenView tv;
+  const uint16_t* q;       // bf16 [T, H, 576]
+  const uint16_t* kv;      // bf16 [num_pages, 64, 576]
+  const int32_t* idx;      // [T, K]
+  uint16_t* out;           // bf16 [T, H, 512]
+  float* part_o;           // [T, S, H, 512] (null when S == 1)
+  float* part_lse;         // [T, S, H]
+  uint32_t* err;
+  int32_t n_heads, top_k, n_splits, split_len;
+  float scale_log2;        // softmax_scale * log2(e)
+};
+
+// Launchers (each returns the cudaError_t of its launch).
+cudaError_t launch_score(const ScoreParams& p, dsa_dtype_t dt, dsa_scale_t sk, cudaStream_t s);
+cudaError_t launch_topk(const TopkParams& p, int32_t max_visible, cudaStream_t s);
+cudaError_t launch_sfa(const SfaParams& p, cudaStream_t s);
+cudaError_t launch_sfa_combine(const SfaParams& p, cudaStream_t s);
+
+}  // namespace dsa

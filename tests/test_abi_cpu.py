@@ -1,0 +1,111 @@
+"""The C-ABI library loads, exports every symbol include/dsa.h declares, and rejects bad
+arguments on the host before launching anything (no GPU needed)."""
+import ctypes as C
+import os
+import re
+
+import pytest
+import torch
+
+import sparse_attention_decode_dsa_gb300 as dsa
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def test_exports_every_declared_symbol():
+    hdr = open(os.path.join(ROOT, "include", "dsa.h")).read()
+    hdr = re.sub(r"/\*.*?\*/", "", hdr, flags=re.S)
+    names = set(re.findall(r"\b(dsa_[a-z_]+)\s*\(", hdr))
+    assert len(names) >= 10
+    raw = C.CDLL(dsa.LIB_PATH)
+    missing = [n for n in sorted(names) if not hasattr(raw, n)]
+    assert not missing, missing
+
+
+def test_version_and_strings():
+    assert dsa.lib.dsa_abi_version() == 1
+    assert dsa.lib.dsa_status_string(0) == b"DSA_OK"
+    assert dsa.lib.dsa_status_string(3) == b"DSA_ERR_WORKSPACE"
+
+
+FAKE = 0x7F0000000000  # never dereferenced: every call below fails its host-side checks
+
+
+def _structs(B=2, maxp=4, T=None, heads=64, dim=128, topk=128, dtype=dsa.DSA_BF16,
+             scale=dsa.DSA_SCALE_NONE, lens=(100, 200)):
+    lens_t = torch.tensor(lens, dtype=torch.int32)
+    pages = dsa.PageTable(FAKE, FAKE, C.cast(C.c_void_p(lens_t.data_ptr()), C.POINTER(C.c_int32)),
+                          B, maxp, 64, 16)
+    toks = dsa.Tokens(T if T is not None else B, None, None, None, None)
+    cache = dsa.IndexCache(FAKE, FAKE if scale else None, dtype, scale, dim)
+    args = dsa.IndexerArgs(FAKE, FAKE if scale else None, dtype, scale, FAKE, heads, topk, 0)
+    return pages, toks, cache, args, lens_t
+
+
+def _call_indexer(pages, toks, cache, args, ws=256 * 1000, ws_bytes=1 << 30):
+    return dsa.lib.dsa_indexer_topk(C.byref(args), C.byref(cache), C.byref(pages), C.byref(toks),
+                                    C.c_void_p(FAKE), None, C.c_void_p(ws) if ws else None, ws_bytes,
+                                    None, None)
+
+
+def test_workspace_size_formula():
+    pages, toks, cache, args, keep = _structs(lens=(100, 200))
+    n = dsa.lib.dsa_indexer_workspace_size(C.byref(args), C.byref(cache), C.byref(pages), C.byref(toks))
+    # error word (256 B) + T rows x ceil(max visible / 64) * 64 f32 scores, 256-aligned
+    assert n == 256 + ((2 * 256 * 4 + 255) // 256) * 256
+
+
+@pytest.mark.parametrize("mutate,status", [
+    (lambda p, t, c, a: setattr(p, "page_size", 32), dsa.DSA_ERR_UNSUPPORTED),
+    (lambda p, t, c, a: setattr(a, "top_k", 0), dsa.DSA_ERR_UNSUPPORTED),
+    (lambda p, t, c, a: setattr(a, "top_k", 4096), dsa.DSA_ERR_UNSUPPORTED),
+    (lambda p, t, c, a: setattr(a, "n_heads", 65), dsa.DSA_ERR_UNSUPPORTED),
+    (lambda p, t, c, a: setattr(c, "dim", 96), dsa.DSA_ERR_UNSUPPORTED),
+    (lambda p, t, c, a: setattr(a, "q_dtype", dsa.DSA_E4M3), dsa.DSA_ERR_UNSUPPORTED),
+    (lambda p, t, c, a: setattr(c, "scale_kind", dsa.DSA_SCALE_MX_E8M0_G32), dsa.DSA_ERR_UNSUPPORTED),
+    (lambda p, t, c, a: setattr(t, "n_tokens", 3), dsa.DSA_ERR_INVALID_ARG),
+    (lambda p, t, c, a: setattr(t, "token_seq", C.c_void_p(FAKE)), dsa.DSA_ERR_INVALID_ARG),
+    (lambda p, t, c, a: setattr(p, "max_pages_per_seq", 1), dsa.DSA_ERR_INVALID_ARG),
+    (lambda p, t, c, a: setattr(a, "head_w", None), dsa.DSA_ERR_INVALID_ARG),
+    (lambda p, t, c, a: setattr(a, "act", 7), dsa.DSA_ERR_INVALID_ARG),
+])
+def test_indexer_rejects_bad_arguments(mutate, status):
+    pages, toks, cache, args, keep = _structs()
+    mutate(pages, toks, cache, args)
+    assert _call_indexer(pages, toks, cache, args) == status
+    assert len(dsa.lib.dsa_last_error_message()) > 0
+
+
+def test_e4m3_needs_scales():
+    pages, toks, cache, args, keep = _structs(dtype=dsa.DSA_E4M3, scale=dsa.DSA_SCALE_PER_TOKEN_F32)
+    cache.scale = None
+    assert _call_indexer(pages, toks, cache, args) == dsa.DSA_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("ws,ws_bytes", [(0, 1 << 30), (FAKE + 8, 1 << 30), (FAKE, 100)])
+def test_workspace_checks(ws, ws_bytes):
+    pages, toks, cache, args, keep = _structs()
+    assert _call_indexer(pages, toks, cache, args, ws=ws, ws_bytes=ws_bytes) == dsa.DSA_ERR_WORKSPACE
+
+
+def test_sfa_rejects_bad_shapes():
+    pages, toks, cache, args, keep = _structs()
+    sargs = dsa.SfaArgs(FAKE, 129, 0.04)
+    lat = dsa.LatentCache(FAKE, 576, 512)
+    st = dsa.lib.dsa_sparse_attn(C.byref(sargs), C.byref(lat), C.byref(pages), C.byref(toks), C.c_void_p(FAKE),
+                                 128, C.c_void_p(FAKE), C.c_void_p(FAKE), 1 << 30, None, None)
+    assert st == dsa.DSA_ERR_UNSUPPORTED
+    sargs.n_heads = 128
+    lat.dim = 512
+    st = dsa.lib.dsa_sparse_attn(C.byref(sargs), C.byref(lat), C.byref(pages), C.byref(toks), C.c_void_p(FAKE),
+                                 128, C.c_void_p(FAKE), C.c_void_p(FAKE), 1 << 30, None, None)
+    assert st == dsa.DSA_ERR_UNSUPPORTED
+
+
+def test_product_path_has_no_cpu_fallback():
+    """The package imports nothing from the oracle and offers no CPU implementation."""
+    pkg = os.path.join(ROOT, "sparse_attention_decode_dsa_gb300")
+    for f in os.listdir(pkg):
+        if f.endswith(".py"):
+            src = open(os.path.join(pkg, f)).read()
+            assert "oracle" not in src and "dsa_workloads" not in src, f

@@ -1,0 +1,178 @@
+"""Parity of the CUDA path (through the C ABI) with the float64 oracle.
+
+Indices and their scores must match bit for bit (the exactness certificate guarantees the
+fp32 scores are exact).  Attention outputs must satisfy, against the float64 oracle,
+max |err| <= 2e-2 and relative RMS (||o - r|| / ||r|| over the compared tensor) <= 1e-2:
+the BF16 tolerance of the DSA hot path.  Every sparse-attention output here is bf16 from
+bf16 inputs, so that tolerance applies to all configs, including those whose indexer
+runs in FP8.
+"""
+import numpy as np
+import pytest
+import torch
+
+import dsa_workloads as W
+from oracle import dsa_oracle as O
+
+pytestmark = pytest.mark.gpu
+
+ATOL = 2e-2
+RRMS = 1e-2
+
+
+@pytest.fixture(scope="module")
+def dsa():
+    import sparse_attention_decode_dsa_gb300 as m
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    return m
+
+
+def _device(wl):
+    from dsa_workloads.device import to_device
+    return to_device(wl)
+
+
+def _run_fused(dsa, plan, T, K, H):
+    out_idx = torch.empty((T, K), dtype=torch.int32, device="cuda")
+    out = torch.empty((T, H, 512), dtype=torch.bfloat16, device="cuda")
+    ws = dsa.alloc_workspace(plan.ws_fused())
+    dsa.fused_decode(plan, out_idx, out, ws)
+    torch.cuda.synchronize()
+    assert dsa.read_device_error(ws) == 0
+    return out_idx.cpu().numpy(), out.float().cpu().numpy().astype(np.float64)
+
+
+def _run_indexer(dsa, plan, T, K):
+    out_idx = torch.empty((T, K), dtype=torch.int32, device="cuda")
+    out_sc = torch.empty((T, K), dtype=torch.float32, device="cuda")
+    ws = dsa.alloc_workspace(plan.ws_indexer())
+    dsa.indexer_topk(plan, out_idx, ws, out_score=out_sc)
+    torch.cuda.synchronize()
+    assert dsa.read_device_error(ws) == 0
+    return out_idx.cpu().numpy(), out_sc.cpu().numpy().astype(np.float64)
+
+
+def _run_sfa(dsa, plan, idx_np, H):
+    T, K = idx_np.shape
+    idx = torch.from_numpy(np.ascontiguousarray(idx_np, dtype=np.int32)).cuda()
+    out = torch.empty((T, H, 512), dtype=torch.bfloat16, device="cuda")
+    ws = dsa.alloc_workspace(plan.ws_sfa())
+    dsa.sparse_attn(plan, idx, out, ws)
+    torch.cuda.synchronize()
+    assert dsa.read_device_error(ws) == 0
+    return out.float().cpu().numpy().astype(np.float64)
+
+
+def _check_attn(got, want, label):
+    err = np.abs(got - want)
+    denom = np.linalg.norm(want)
+    rrms = np.linalg.norm(got - want) / denom if denom > 0 else np.linalg.norm(got)
+    assert err.max() <= ATOL, f"{label}: max |err| {err.max():.3e}"
+    assert rrms <= RRMS, f"{label}: relative RMS {rrms:.3e}"
+    return err.max(), rrms
+
+
+def _check_config(dsa, spec, tokens=None):
+    wl = W.make(spec)
+    d = _device(wl)
+    plan = dsa.Plan(d)
+    T, K, H = wl.n_tokens, spec.topk, spec.sfa_heads
+    toks = list(range(T)) if tokens is None else tokens
+    ref = {t: O.step(wl, t) for t in toks}
+
+    idx_g, sc_g = _run_indexer(dsa, plan, T, K)
+    for t in toks:
+        ri, rs, _ = ref[t]
+        assert np.array_equal(idx_g[t], ri), f"{spec.name} token {t}: indices differ"
+        assert np.array_equal(sc_g[t], rs, equal_nan=True), f"{spec.name} token {t}: scores differ"
+
+    fidx, fout = _run_fused(dsa, plan, T, K, H)
+    assert np.array_equal(fidx[toks], idx_g[toks])
+    want = np.stack([ref[t][2] for t in toks])
+    _check_attn(fout[toks], want, f"{spec.name} fused")
+
+    # the attention fed the oracle's own indices (indexer and attention checked apart)
+    oidx = idx_g.copy()
+    for t in toks:
+        oidx[t] = ref[t][0]
+    sout = _run_sfa(dsa, plan, oidx, H)
+    _check_attn(sout[toks], want, f"{spec.name} sfa")
+    return wl
+
+
+@pytest.mark.parametrize("spec", W.SMALL, ids=lambda s: s.name)
+def test_small_configs(dsa, spec):
+    _check_config(dsa, spec)
+
+
+def test_tiny_decode(dsa):
+    _check_config(dsa, W.TINY_DECODE)
+
+
+def test_bf16_decode_sampled(dsa):
+    _check_config(dsa, W.BF16_DECODE, tokens=[0, 13, 31])
+
+
+def test_fp8_decode_sampled(dsa):
+    _check_config(dsa, W.FP8_DECODE, tokens=[1, 30])
+
+
+def test_ragged_mxfp8_decode_sampled(dsa):
+    _check_config(dsa, W.RAGGED_MXFP8_DECODE, tokens=[0, 3, 6, 7])
+
+
+def test_causal_prefill_sampled(dsa):
+    _check_config(dsa, W.CAUSAL_PREFILL, tokens=[0, 1, 63, 64, 2046, 2047, 2048, 5000, 8191])
+
+
+def test_relu_activation(dsa):
+    """The per-head ReLU variant against the oracle's 'relu' reading."""
+    spec = W.SMALL_DECODE_BF16
+    wl = W.make(spec)
+    d = _device(wl)
+    d.act = dsa.DSA_ACT_RELU
+    plan = dsa.Plan(d)
+    idx_g, sc_g = _run_indexer(dsa, plan, wl.n_tokens, spec.topk)
+    for t in range(wl.n_tokens):
+        ri, rs = O.indexer_topk(wl, t, act="relu")
+        assert np.array_equal(idx_g[t], ri)
+        assert np.array_equal(sc_g[t], rs, equal_nan=True)
+
+
+def test_bad_page_id_sets_error_bit_and_gpu_stays_usable(dsa):
+    spec = W.SMALL_DECODE_BF16
+    wl = W.make(spec)
+    d = _device(wl)
+    d.block_table[5, 3] = wl.num_pages + 100     # outside the cache
+    plan = dsa.Plan(d)
+    ws = dsa.alloc_workspace(plan.ws_fused())
+    out_idx = torch.empty((wl.n_tokens, spec.topk), dtype=torch.int32, device="cuda")
+    out = torch.empty((wl.n_tokens, spec.sfa_heads, 512), dtype=torch.bfloat16, device="cuda")
+    dsa.fused_decode(plan, out_idx, out, ws)
+    err = dsa.read_device_error(ws)
+    assert err & dsa.DSA_DEVERR_PAGE_ID
+    dsa.clear_device_error(ws)
+    assert dsa.read_device_error(ws) == 0
+    _check_config(dsa, W.SMALL_H8)               # the context is still healthy
+
+
+def test_out_of_range_index_sets_error_bit(dsa):
+    spec = W.SMALL_DECODE_BF16
+    wl = W.make(spec)
+    plan = dsa.Plan(_device(wl))
+    idx = np.full((wl.n_tokens, spec.topk), -1, np.int32)
+    idx[:, 0] = 0
+    idx[1, 1] = 5000                             # beyond sequence 1's 37 tokens
+    ws = dsa.alloc_workspace(plan.ws_sfa())
+    out = torch.empty((wl.n_tokens, spec.sfa_heads, 512), dtype=torch.bfloat16, device="cuda")
+    dsa.sparse_attn(plan, torch.from_numpy(idx).cuda(), out, ws)
+    assert dsa.read_device_error(ws) & dsa.DSA_DEVERR_INDEX
+
+
+def test_repeated_calls_are_deterministic(dsa):
+    spec = W.SMALL_DECODE_MX
+    wl = W.make(spec)
+    plan = dsa.Plan(_device(wl))
+    a = _run_fused(dsa, plan, wl.n_tokens, spec.topk, spec.sfa_heads)
+    b = _run_fused(dsa, plan, wl.n_tokens, spec.topk, spec.sfa_heads)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
