@@ -247,15 +247,15 @@ def main():
     # per-launch events over the timed region
     traces = []
     for _ in range(args.steps):
-        tr = dsa.Trace()
         evs = [torch.cuda.Event(enable_timing=True) for _ in range(2 * dsa.DSA_TRACE_MAX)]
+        for e in evs:       # torch creates the CUDA event lazily, on its first record
+            e.record(stream)
+        tr = dsa.Trace()
         for i in range(dsa.DSA_TRACE_MAX):
             tr.begin[i] = evs[2 * i].cuda_event
             tr.end[i] = evs[2 * i + 1].cuda_event
+            assert tr.begin[i] and tr.end[i]
         traces.append((tr, evs))
-    for _, evs in traces:   # torch creates CUDA events lazily, on their first record
-        for e in evs:
-            e.record(stream)
     torch.cuda.synchronize()
 
     clocks = ClockSampler(torch.cuda.current_device() if world == 1 else local_rank)

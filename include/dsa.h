@@ -78,6 +78,8 @@ typedef enum { DSA_ACT_IDENTITY = 0, DSA_ACT_RELU = 1 } dsa_act_t;
 #define DSA_DEVERR_SEQ_LEN 0x2u   /* a seq_len outside [0, max_pages_per_seq * 64]        */
 #define DSA_DEVERR_INDEX 0x4u     /* an SFA index outside [-1, visible count of its token]*/
 #define DSA_DEVERR_TOKEN 0x8u     /* token_seq outside [0, batch) or token_pos < -1       */
+#define DSA_DEVERR_TIMEOUT 0x10u  /* an internal pipeline wait gave up (~2 s); the kernel
+                                     unwound without finishing its work                  */
 
 /* Paged-cache addressing shared by the K-index cache and the latent cache. */
 typedef struct {

@@ -19,7 +19,7 @@ DSA_OK, DSA_ERR_INVALID_ARG, DSA_ERR_UNSUPPORTED, DSA_ERR_WORKSPACE, DSA_ERR_CUD
 DSA_BF16, DSA_E4M3 = 0, 1
 DSA_SCALE_NONE, DSA_SCALE_PER_TOKEN_F32, DSA_SCALE_MX_E8M0_G32 = 0, 1, 2
 DSA_ACT_IDENTITY, DSA_ACT_RELU = 0, 1
-DSA_DEVERR_PAGE_ID, DSA_DEVERR_SEQ_LEN, DSA_DEVERR_INDEX, DSA_DEVERR_TOKEN = 1, 2, 4, 8
+DSA_DEVERR_PAGE_ID, DSA_DEVERR_SEQ_LEN, DSA_DEVERR_INDEX, DSA_DEVERR_TOKEN, DSA_DEVERR_TIMEOUT = 1, 2, 4, 8, 16
 DSA_TRACE_MAX = 8
 
 _vp = C.c_void_p

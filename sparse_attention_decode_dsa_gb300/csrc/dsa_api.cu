@@ -182,15 +182,19 @@ struct Tracer {
   explicit Tracer(dsa_trace_t* tr, cudaStream_t st) : t(tr), s(st) {
     if (t) t->n_recorded = 0;
   }
+  cudaError_t status = cudaSuccess;
   void begin() {
-    if (t && n < DSA_TRACE_MAX && t->begin[n]) cudaEventRecord((cudaEvent_t)t->begin[n], s);
+    if (t && n < DSA_TRACE_MAX && t->begin[n]) note(cudaEventRecord((cudaEvent_t)t->begin[n], s));
   }
   void end(const char* name) {
     if (t && n < DSA_TRACE_MAX) {
-      if (t->end[n]) cudaEventRecord((cudaEvent_t)t->end[n], s);
+      if (t->end[n]) note(cudaEventRecord((cudaEvent_t)t->end[n], s));
       t->name[n] = name;
       t->n_recorded = ++n;
     }
+  }
+  void note(cudaError_t e) {
+    if (status == cudaSuccess) status = e;
   }
 };
 
@@ -215,8 +219,9 @@ dsa_status_t run_indexer(const dsa_indexer_args_t* a, const dsa_index_cache_t* c
   sp.act = (int)a->act;
   sp.max_page_blocks = (ip.max_visible + kPage - 1) / kPage;
   if (sp.max_page_blocks > 0) {
+    const bool tc = score_tc_supported(c->dtype, c->dim, a->n_heads);
     tr.begin();
-    cudaError_t e = launch_score(sp, c->dtype, c->scale_kind, s);
+    cudaError_t e = tc ? launch_score_tc(sp, c->dtype, c->scale_kind, s) : launch_score(sp, c->dtype, c->scale_kind, s);
     tr.end("indexer_score");
     if (e != cudaSuccess) return cuda_fail(e, "indexer score launch");
   }
@@ -291,7 +296,9 @@ dsa_status_t dsa_indexer_topk(const dsa_indexer_args_t* args, const dsa_index_ca
   IndexerPlan ip = plan_indexer(mv, tokens->n_tokens);
   if ((st = check_ws(ws, ws_bytes, kAlign + ip.score_bytes)) != DSA_OK) return st;
   Tracer tr(trace, (cudaStream_t)stream);
-  return run_indexer(args, cache, pages, tokens, ip, out_idx, out_score, (uint8_t*)ws, (cudaStream_t)stream, tr);
+  st = run_indexer(args, cache, pages, tokens, ip, out_idx, out_score, (uint8_t*)ws, (cudaStream_t)stream, tr);
+  if (st == DSA_OK && tr.status != cudaSuccess) return cuda_fail(tr.status, "recording a trace event");
+  return st;
 }
 
 size_t dsa_sparse_attn_workspace_size(const dsa_sfa_args_t* args, const dsa_page_table_t* pages,
@@ -317,7 +324,9 @@ dsa_status_t dsa_sparse_attn(const dsa_sfa_args_t* args, const dsa_latent_cache_
   SfaPlan sp = plan_sfa(tokens->n_tokens, args->n_heads, top_k);
   if ((st = check_ws(ws, ws_bytes, kAlign + sp.part_o_bytes + sp.part_lse_bytes)) != DSA_OK) return st;
   Tracer tr(trace, (cudaStream_t)stream);
-  return run_sfa(args, cache, pages, tokens, mv, idx, top_k, out, (uint8_t*)ws, sp, (cudaStream_t)stream, tr);
+  st = run_sfa(args, cache, pages, tokens, mv, idx, top_k, out, (uint8_t*)ws, sp, (cudaStream_t)stream, tr);
+  if (st == DSA_OK && tr.status != cudaSuccess) return cuda_fail(tr.status, "recording a trace event");
+  return st;
 }
 
 size_t dsa_fused_workspace_size(const dsa_indexer_args_t* iargs, const dsa_index_cache_t* icache,
@@ -353,8 +362,10 @@ dsa_status_t dsa_fused_decode(const dsa_indexer_args_t* iargs, const dsa_index_c
   if ((st = run_indexer(iargs, icache, pages, tokens, ip, out_idx, nullptr, (uint8_t*)ws, (cudaStream_t)stream,
                         tr)) != DSA_OK)
     return st;
-  return run_sfa(sargs, lcache, pages, tokens, mv, out_idx, iargs->top_k, out, (uint8_t*)ws, sp,
-                 (cudaStream_t)stream, tr);
+  st = run_sfa(sargs, lcache, pages, tokens, mv, out_idx, iargs->top_k, out, (uint8_t*)ws, sp,
+               (cudaStream_t)stream, tr);
+  if (st == DSA_OK && tr.status != cudaSuccess) return cuda_fail(tr.status, "recording a trace event");
+  return st;
 }
 
 dsa_status_t dsa_read_device_error(const void* ws, uint32_t* err, dsa_stream_t stream) {

@@ -66,6 +66,8 @@ struct SfaParams {
 
 // Launchers (each returns the cudaError_t of its launch).
 cudaError_t launch_score(const ScoreParams& p, dsa_dtype_t dt, dsa_scale_t sk, cudaStream_t s);
+bool score_tc_supported(dsa_dtype_t dt, int dim, int n_heads);
+cudaError_t launch_score_tc(const ScoreParams& p, dsa_dtype_t dt, dsa_scale_t sk, cudaStream_t s);
 cudaError_t launch_topk(const TopkParams& p, int32_t max_visible, cudaStream_t s);
 cudaError_t launch_sfa(const SfaParams& p, cudaStream_t s);
 cudaError_t launch_sfa_combine(const SfaParams& p, cudaStream_t s);

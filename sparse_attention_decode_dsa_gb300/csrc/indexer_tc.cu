@@ -1,0 +1,427 @@
+// Lightning Indexer scoring pass on the 5th-generation tensor cores (tcgen05 + TMA).
+//
+// Computes, for every query row and every visible key t, the weighted head sum
+//   I[t] = sum_h w_h * act(scale_q * scale_k[t] * (q_h . k_t))
+// of "Adapting and Optimizing Inference for a New Model Architecture on Ascend",
+// section 3.1 (relevance scores against the paged K cache, head weighting), with the
+// per-32-element scales of MXFP8 ("Day0 Inference Optimization on Ascend CANN",
+// section 3) applied per group.
+//
+// One persistent CTA per SM walks a contiguous, equal share of the (row, 128-token
+// tile) items.  Warp roles:
+//   warp 0     TMA producer: two 64-token pages of the K-index cache per tile (each a
+//              64 x 128 B box with 128-byte swizzle) into a ring of shared-memory
+//              stages; the row's query [H x d] into one of two query slots;
+//   warp 1     one thread issues tcgen05.mma: D[128 tokens x N heads] (f32, TMEM) =
+//              K_tile[128 x d] . q[N x d]^T, N = H rounded up to 16; MXFP8 keeps one
+//              accumulator per 32-wide group so the group scales apply exactly;
+//   warps 2-5  epilogue: TMEM lane i = token i; each thread reads its token's head
+//              scores with tcgen05.ld, applies scales, activation and head weights,
+//              sums over heads and stores one f32 score.
+// Accumulators are double buffered in TMEM so the epilogue of one tile overlaps the
+// MMA of the next.  Every wait is bounded (see sm100::mbar_wait).
+#include <cudaTypedefs.h>
+
+#include "sm100.cuh"
+
+namespace dsa {
+
+namespace {
+
+using namespace sm100;
+
+constexpr int kTcThreads = 192;
+constexpr int kTileTok = 128;
+constexpr int kMaxRowsPerLaunch = 1024;
+
+template <int KIND, int D>  // KIND 0: bf16; 1: e4m3 + per-token f32; 2: e4m3 + E8M0 per 32
+struct Cfg {
+  static constexpr int kElem = KIND == 0 ? 2 : 1;
+  static constexpr int kRowBytes = D * kElem;              // bytes of one key / query row
+  static constexpr int kRegions = kRowBytes / 128;         // 128-byte swizzle columns per row
+  static constexpr int kBoxInner = 128 / kElem;            // elements in one 128-byte piece
+  static constexpr int kStageBytes = kTileTok * kRowBytes;
+  static constexpr int kStages = KIND == 0 ? 4 : 6;
+  static constexpr int kRegionStageBytes = kTileTok * 128;  // 16 KB
+  static constexpr int kRegionQBytes = 64 * 128;           // 8 KB (up to 64 heads)
+  static constexpr int kQSlotBytes = kRegions * kRegionQBytes;
+  static constexpr int kKSteps = kRowBytes / 32;           // one MMA consumes 32 bytes of K
+  static constexpr int kGroups = KIND == 2 ? D / 32 : 1;
+  static constexpr int kAccCols = 64 * kGroups;
+  static constexpr int kTmemCols = 2 * kAccCols;
+  static constexpr uint32_t kFmt = KIND == 0 ? 1u : 0u;    // bf16 / e4m3
+  static constexpr int kSmem = 1024 /*align*/ + kStages * kStageBytes + 2 * kQSlotBytes + 4096 /*bars*/ +
+                               3 * (kMaxRowsPerLaunch + 1) * 4 + 4 * (64 + 64 * 4 + 4) * 4;
+};
+
+struct TcArgs {
+  ScoreParams p;
+  int32_t row0;   // first query row of this launch
+  int32_t nrows;  // rows in this launch
+};
+
+__device__ __forceinline__ void named_sync_warp() { __syncwarp(); }
+
+template <int KIND, int D>
+__global__ void __launch_bounds__(kTcThreads, 1)
+    score_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap qmap,
+                    const TcArgs a) {
+  using C = Cfg<KIND, D>;
+  const ScoreParams& p = a.p;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int H = p.n_heads;
+  const int N = (H + 15) / 16 * 16;
+
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_u32 = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + ((1024 - (raw_u32 & 1023)) & 1023);
+  uint8_t* stages = smem;
+  uint8_t* qslots = stages + C::kStages * C::kStageBytes;
+  uint64_t* bars = (uint64_t*)(qslots + 2 * C::kQSlotBytes);
+  uint64_t* full = bars;
+  uint64_t* empty = full + C::kStages;
+  uint64_t* acc_full = empty + C::kStages;
+  uint64_t* acc_empty = acc_full + 2;
+  uint64_t* q_full = acc_empty + 2;
+  uint64_t* q_empty = q_full + 2;
+  uint64_t* drain = q_empty + 2;
+  uint32_t* tmem_base_s = (uint32_t*)(drain + 1);
+  volatile int* abort_flag = (volatile int*)(tmem_base_s + 1);
+  int* prefix = (int*)(bars + 512);                 // [nrows + 1] item prefix
+  int* rowb = prefix + kMaxRowsPerLaunch + 1;       // batch row of each query row
+  int* rown = rowb + kMaxRowsPerLaunch + 1;         // visible count of each query row
+  float* epi = (float*)(rown + kMaxRowsPerLaunch + 1);  // per epilogue warp: w[64], qs[64*4], qtok
+
+  // ---- set-up: barriers, TMEM, per-row metadata and this CTA's item range ----------
+  if (tid == 0) {
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&acc_full[i], 1);
+      mbar_init(&acc_empty[i], 4);
+      mbar_init(&q_full[i], 1);
+      mbar_init(&q_empty[i], 1);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&kmap);
+    tma_prefetch_desc(&qmap);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_base_s, C::kTmemCols);
+    tmem_relinquish();
+  }
+  // visible counts and tiles of every row, then an exclusive scan (one warp)
+  for (int r = tid; r < a.nrows; r += kTcThreads) {
+    int b, n;
+    resolve_token(p.tv, a.row0 + r, &b, &n, p.err);
+    rowb[r] = b;
+    rown[r] = n;
+    prefix[r + 1] = (n + kTileTok - 1) / kTileTok;
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 0) {
+    int carry = 0;
+    for (int base = 0; base < a.nrows; base += 32) {
+      const int r = base + lane;
+      int v = r < a.nrows ? prefix[r + 1] : 0;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int u = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v += u;
+      }
+      if (r < a.nrows) prefix[r + 1] = carry + v;
+      carry += __shfl_sync(0xffffffffu, v, 31);
+    }
+    if (lane == 0) prefix[0] = 0;
+  }
+  __syncthreads();
+  const int total = prefix[a.nrows];
+  const int it_begin = (int)((int64_t)total * blockIdx.x / gridDim.x);
+  const int it_end = (int)((int64_t)total * (blockIdx.x + 1) / gridDim.x);
+  const uint32_t tmem_base = *tmem_base_s;
+
+  if (warp == 0) {
+    // ================================ TMA producer ================================
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t armed = 0, armed_parity = 0;  // stages with a load issued, and its phase parity
+      int r = 0, cur_row = -1, qcount = 0;
+      for (int it = it_begin; it < it_end; ++it) {
+        while (prefix[r + 1] <= it) ++r;
+        if (r != cur_row) {
+          cur_row = r;
+          const int slot = qcount & 1;
+          if (!mbar_wait(&q_empty[slot], ((qcount >> 1) & 1) ^ 1, abort_flag, p.err)) break;
+          mbar_arrive_expect_tx(&q_full[slot], C::kRegions * H * 128);
+          const uint32_t qdst = smem_u32(qslots + slot * C::kQSlotBytes);
+          for (int g = 0; g < C::kRegions; ++g)
+            tma_load_2d(qdst + g * C::kRegionQBytes, &qmap, &q_full[slot], g * C::kBoxInner, (a.row0 + r) * H);
+          ++qcount;
+        }
+        if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.err)) break;
+        const int tile = it - prefix[r];
+        const int b = rowb[r];
+        const int npages = (rown[r] + kPage - 1) / kPage;
+        int pg[2] = {-1, -1};
+        uint32_t bytes = 0;
+        for (int u = 0; u < 2; ++u) {
+          const int j = 2 * tile + u;
+          if (j < npages) {
+            pg[u] = physical_page(p.tv, b, j, p.err);
+            if (pg[u] >= 0) bytes += kPage * C::kRowBytes;
+          }
+        }
+        mbar_arrive_expect_tx(&full[stage], bytes);
+        armed |= 1u << stage;
+        armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
+        const uint32_t sdst = smem_u32(stages + stage * C::kStageBytes);
+        for (int u = 0; u < 2; ++u) {
+          if (pg[u] < 0) continue;
+          for (int g = 0; g < C::kRegions; ++g)
+            tma_load_2d(sdst + g * C::kRegionStageBytes + u * (kPage * 128), &kmap, &full[stage],
+                        g * C::kBoxInner, pg[u] * kPage);
+        }
+        if (++stage == C::kStages) {
+          stage = 0;
+          phase ^= 1;
+        }
+      }
+      if (*abort_flag) {
+        // let every copy still in flight land before the shared memory is released
+        for (int st = 0; st < C::kStages; ++st) {
+          if (!(armed >> st & 1)) continue;
+          const long long t0 = clock64();
+          while (!mbar_try_wait(smem_u32(&full[st]), (armed_parity >> st) & 1) && clock64() - t0 < kWaitLimitCycles) {
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ================================ MMA issuer ==================================
+    if (lane == 0) {
+      const uint32_t idesc_v = idesc(128, N, C::kFmt, C::kFmt);
+      int stage = 0, acc = 0;
+      uint32_t phase = 0, acc_phase = 0;
+      int r = 0, cur_row = -1, qcount = 0, slot = 0;
+      for (int it = it_begin; it < it_end; ++it) {
+        while (prefix[r + 1] <= it) ++r;
+        if (r != cur_row) {
+          cur_row = r;
+          slot = qcount & 1;
+          if (!mbar_wait(&q_full[slot], (qcount >> 1) & 1, abort_flag, p.err)) break;
+          ++qcount;
+        }
+        if (!mbar_wait(&full[stage], phase, abort_flag, p.err)) break;
+        if (!mbar_wait(&acc_empty[acc], acc_phase ^ 1, abort_flag, p.err)) break;
+        tc_fence_after();
+        const uint32_t a0 = smem_u32(stages + stage * C::kStageBytes);
+        const uint32_t b0 = smem_u32(qslots + slot * C::kQSlotBytes);
+        const uint32_t d0 = tmem_base + acc * C::kAccCols;
+#pragma unroll
+        for (int k = 0; k < C::kKSteps; ++k) {
+          const int g = k / 4, off = (k % 4) * 32;
+          const uint64_t ad = desc_sw128(a0 + g * C::kRegionStageBytes + off);
+          const uint64_t bd = desc_sw128(b0 + g * C::kRegionQBytes + off);
+          if (KIND == 0) {
+            mma_f16(d0, ad, bd, idesc_v, k > 0);
+          } else if (KIND == 1) {
+            mma_f8(d0, ad, bd, idesc_v, k > 0);
+          } else {
+            mma_f8(d0 + k * 64, ad, bd, idesc_v, 0);  // one accumulator per 32-wide group
+          }
+        }
+        tc_commit(&empty[stage]);
+        tc_commit(&acc_full[acc]);
+        if (it + 1 == it_end || prefix[r + 1] == it + 1) tc_commit(&q_empty[slot]);
+        if (++stage == C::kStages) {
+          stage = 0;
+          phase ^= 1;
+        }
+        if (++acc == 2) {
+          acc = 0;
+          acc_phase ^= 1;
+        }
+      }
+      // every MMA issued above has completed once `drain` flips
+      tc_commit(drain);
+      const long long t0 = clock64();
+      while (!mbar_try_wait(smem_u32(drain), 0) && clock64() - t0 < kWaitLimitCycles) {
+      }
+    }
+  } else {
+    // ================================ epilogue ====================================
+    const int quarter = warp & 3;
+    const int i = quarter * 32 + lane;  // TMEM lane == token within the tile
+    float* w_s = epi + (warp - 2) * (64 + 64 * 4 + 4);
+    float* qs_s = w_s + 64;             // [h][g] query group scales (MX)
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    int r = 0, cur_row = -1;
+    float qtok = 1.f;
+    for (int it = it_begin; it < it_end; ++it) {
+      while (prefix[r + 1] <= it) ++r;
+      const int grow = a.row0 + r;
+      if (r != cur_row) {
+        cur_row = r;
+        named_sync_warp();
+        for (int h = lane; h < H; h += 32) {
+          w_s[h] = p.head_w[(int64_t)grow * H + h];
+          if (KIND == 2) {
+            const uint32_t q4 = *(const uint32_t*)((const uint8_t*)p.q_scale + ((int64_t)grow * H + h) * 4);
+#pragma unroll
+            for (int g = 0; g < 4; ++g) qs_s[h * 4 + g] = e8m0_to_f32((q4 >> (8 * g)) & 0xFF);
+          }
+        }
+        qtok = (KIND == 1) ? ((const float*)p.q_scale)[grow] : 1.f;
+        named_sync_warp();
+      }
+      const int tile = it - prefix[r];
+      const int t = tile * kTileTok + i;
+      const bool valid = t < rown[r];
+      int pg = -1;
+      if (valid) pg = physical_page(p.tv, rowb[r], t >> 6, nullptr);
+      float ks[C::kGroups];
+#pragma unroll
+      for (int g = 0; g < C::kGroups; ++g) ks[g] = 1.f;
+      if (pg >= 0) {
+        const int64_t krow = (int64_t)pg * kPage + (t & 63);
+        if (KIND == 1) ks[0] = ((const float*)p.k_scale)[krow];
+        if (KIND == 2) {
+          const uint32_t k4 = *(const uint32_t*)((const uint8_t*)p.k_scale + krow * 4);
+#pragma unroll
+          for (int g = 0; g < C::kGroups; ++g) ks[g] = e8m0_to_f32((k4 >> (8 * g)) & 0xFF);
+        }
+      }
+      bool ok = true;
+      if (lane == 0) ok = mbar_wait(&acc_full[acc], acc_phase, abort_flag, p.err);
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      tc_fence_after();
+      float score = 0.f;
+      const uint32_t tbase = tmem_base + ((uint32_t)(quarter * 32) << 16) + acc * C::kAccCols;
+#pragma unroll 1
+      for (int hc = 0; hc < 2; ++hc) {
+        if (hc * 32 >= H) break;
+        float hv[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) hv[j] = 0.f;
+#pragma unroll
+        for (int g = 0; g < C::kGroups; ++g) {
+          uint32_t v[32];
+          tmem_ld32(tbase + g * 64 + hc * 32, v);
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const float x = __uint_as_float(v[j]);
+            if (KIND == 2) hv[j] += x * (ks[g] * qs_s[(hc * 32 + j) * 4 + g]);
+            else hv[j] = x;
+          }
+        }
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const int h = hc * 32 + j;
+          if (h < H) {
+            float x = hv[j];
+            if (KIND == 1) x *= qtok * ks[0];
+            if (p.act == DSA_ACT_RELU) x = fmaxf(x, 0.f);
+            score += x * w_s[h];
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acc_empty[acc]);
+      if (valid) p.scores[(int64_t)grow * p.score_stride + t] = pg >= 0 ? score : -INFINITY;
+      if (++acc == 2) {
+        acc = 0;
+        acc_phase ^= 1;
+      }
+    }
+  }
+
+  // ---- tear-down ---------------------------------------------------------------------
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, C::kTmemCols);
+  }
+}
+
+// ---- host side: tensor maps and launch --------------------------------------------------
+PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    cudaDriverEntryPointQueryResult q;
+    void* ptr = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = (PFN_cuTensorMapEncodeTiled_v12000)ptr;
+  }
+  return fn;
+}
+
+// 2-D map over rows of `row_bytes` bytes with 128-byte swizzle; box = 128 B x box_rows.
+bool make_map(CUtensorMap* m, const void* base, uint64_t rows, int elem, int row_elems, int box_rows) {
+  auto enc = get_encode();
+  if (!enc) return false;
+  const CUtensorMapDataType dt = elem == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8;
+  cuuint64_t dims[2] = {(cuuint64_t)row_elems, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)row_elems * elem};
+  cuuint32_t box[2] = {(cuuint32_t)(128 / elem), (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+template <int KIND, int D>
+cudaError_t launch_tc(const ScoreParams& p, cudaStream_t s) {
+  using C = Cfg<KIND, D>;
+  static_assert(C::kSmem <= 232448, "shared memory budget");
+  CUtensorMap kmap, qmap;
+  if (!make_map(&kmap, p.k, (uint64_t)p.tv.num_pages * kPage, C::kElem, D, kPage)) return cudaErrorInvalidValue;
+  cudaError_t e = cudaFuncSetAttribute(score_tc_kernel<KIND, D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       C::kSmem);
+  if (e != cudaSuccess) return e;
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (!make_map(&qmap, p.q, (uint64_t)p.tv.n_tokens * p.n_heads, C::kElem, D, p.n_heads))
+    return cudaErrorInvalidValue;
+  for (int row0 = 0; row0 < p.tv.n_tokens; row0 += kMaxRowsPerLaunch) {
+    TcArgs a;
+    a.p = p;
+    a.row0 = row0;
+    a.nrows = p.tv.n_tokens - row0 < kMaxRowsPerLaunch ? p.tv.n_tokens - row0 : kMaxRowsPerLaunch;
+    score_tc_kernel<KIND, D><<<sms, kTcThreads, C::kSmem, s>>>(kmap, qmap, a);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+}  // namespace
+
+bool score_tc_supported(dsa_dtype_t dt, int dim, int n_heads) {
+  if (n_heads < 1 || n_heads > 64) return false;
+  if (dt == DSA_BF16) return dim == 64 || dim == 128;
+  return dim == 128;
+}
+
+cudaError_t launch_score_tc(const ScoreParams& p, dsa_dtype_t dt, dsa_scale_t sk, cudaStream_t s) {
+  if (dt == DSA_BF16) return p.dim == 64 ? launch_tc<0, 64>(p, s) : launch_tc<0, 128>(p, s);
+  if (sk == DSA_SCALE_PER_TOKEN_F32) return launch_tc<1, 128>(p, s);
+  return launch_tc<2, 128>(p, s);
+}
+
+}  // namespace dsa
