@@ -209,6 +209,31 @@ dsa_status_t dsa_fused_decode(const dsa_indexer_args_t* iargs,
                               void* ws, size_t ws_bytes,
                               dsa_stream_t stream, dsa_trace_t* trace);
 
+/* ---- Lightning Indexer without a caller workspace ------------------------------ */
+/* No counterpart in the pages: an entry point for callers that cannot allocate device
+ * memory -- plugin hosts or serving runtimes that hand this library no allocator and
+ * fix their memory budget up front, or request paths that must not call cudaMalloc
+ * (it can synchronise the device).  Same inputs, outputs and semantics as
+ * dsa_indexer_topk, but its scratch (the error word and the f32 score rows) lives in a
+ * fixed 8 MiB array inside the library, one per device, held from the library's first
+ * use on that device until the process exits.  It allocates nothing.
+ *   - Limit: 256 + n_tokens * ceil(max visible / 64) * 64 * 4 bytes must fit in 8 MiB
+ *     (e.g. 32 decode tokens over 32768 positions, or 8 over 131072); larger requests
+ *     return DSA_ERR_WORKSPACE before any launch.
+ *   - The first call on a device looks up the array's device address (set-up, once per
+ *     device, under a lock); make that first call before any stream capture.
+ *   - Every call on a device shares the one array and it keeps the last call's
+ *     contents; the error word is cleared on `stream` at the start of each call.  Calls
+ *     that overlap on the GPU (different streams, or concurrent threads) race on it:
+ *     order them on one stream.  Device-side error bits are not reported back; use
+ *     dsa_indexer_topk with a workspace to read them. */
+dsa_status_t dsa_indexer_topk_noalloc(const dsa_indexer_args_t* args,
+                                      const dsa_index_cache_t* cache,
+                                      const dsa_page_table_t* pages,
+                                      const dsa_tokens_t* tokens,
+                                      int32_t* out_idx, float* out_score,
+                                      dsa_stream_t stream);
+
 /* ---- Errors and introspection --------------------------------------------------- */
 /* Copies the device error word out of ws (synchronises `stream`) into *err. */
 dsa_status_t dsa_read_device_error(const void* ws, uint32_t* err, dsa_stream_t stream);

@@ -4,6 +4,7 @@
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
+#include <mutex>
 #include <string>
 
 #include "dsa_internal.h"
@@ -399,3 +400,57 @@ const char* dsa_last_error_message(void) { return g_last_error.c_str(); }
 int32_t dsa_abi_version(void) { return DSA_ABI_VERSION; }
 
 }  // extern "C"
+
+// ---- indexer with the library's own fixed scratch ------------------------------------
+// For callers that cannot allocate device memory: the scratch this entry point needs
+// lives in one file-scope device array per GPU.  Host code may not hand the array's
+// name to a kernel (in host code it names a host-side stand-in); its device address is
+// looked up once per device with cudaGetSymbolAddress and passed as a pointer.
+constexpr size_t kNoAllocScratchBytes = size_t(8) << 20;
+static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
+
+namespace {
+std::mutex g_noalloc_mu;
+constexpr int kMaxDevices = 128;
+void* g_noalloc_addr[kMaxDevices] = {};
+
+// Device address of the fixed scratch on the current device (looked up on first use).
+dsa_status_t noalloc_scratch(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return fail(DSA_ERR_UNSUPPORTED, "device ordinal %d beyond %d", dev, kMaxDevices);
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (!g_noalloc_addr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress of the fixed scratch");
+    g_noalloc_addr[dev] = p;
+  }
+  *out = g_noalloc_addr[dev];
+  return DSA_OK;
+}
+}  // namespace
+
+extern "C" dsa_status_t dsa_indexer_topk_noalloc(const dsa_indexer_args_t* args, const dsa_index_cache_t* cache,
+                                                 const dsa_page_table_t* pages, const dsa_tokens_t* tokens,
+                                                 int32_t* out_idx, float* out_score, dsa_stream_t stream) {
+  dsa_status_t st = check_indexer(args, cache);
+  if (st != DSA_OK) return st;
+  int32_t mv = 0;
+  if ((st = check_pages_tokens(pages, tokens, &mv)) != DSA_OK) return st;
+  if (!out_idx) return fail(DSA_ERR_INVALID_ARG, "out_idx is NULL");
+  IndexerPlan ip = plan_indexer(mv, tokens->n_tokens);
+  const size_t need = kAlign + ip.score_bytes;
+  if (need > kNoAllocScratchBytes)
+    return fail(DSA_ERR_WORKSPACE,
+                "dsa_indexer_topk_noalloc needs %zu bytes of scratch; its fixed scratch holds %zu "
+                "(use dsa_indexer_topk with a caller workspace)",
+                need, kNoAllocScratchBytes);
+  void* ws = nullptr;
+  if ((st = noalloc_scratch(&ws)) != DSA_OK) return st;
+  cudaError_t e = cudaMemsetAsync(ws, 0, sizeof(uint32_t), (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "clearing the fixed scratch's error word");
+  Tracer tr(nullptr, (cudaStream_t)stream);
+  return run_indexer(args, cache, pages, tokens, ip, out_idx, out_score, (uint8_t*)ws, (cudaStream_t)stream, tr);
+}
