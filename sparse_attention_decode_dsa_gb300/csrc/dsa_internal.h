@@ -14,7 +14,7 @@ constexpr int kMaxSfaHeads = 128;
 constexpr int kLatentDim = 576;
 constexpr int kValueDim = 512;
 constexpr int kTopkCluster = 8;              // CTAs cooperating on one row's Top-K
-constexpr int kMaxTopkChunk = 32768;         // scores one Top-K CTA holds in shared memory
+constexpr int kMaxTopkChunk = 24576;         // scores one Top-K CTA holds in shared memory
 constexpr int kMaxVisible = kTopkCluster * kMaxTopkChunk;  // longest row the Top-K handles
 
 // Everything a kernel needs to locate a token's row, sequence and visible range.

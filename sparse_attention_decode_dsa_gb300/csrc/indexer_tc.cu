@@ -15,11 +15,13 @@
 //   warp 1     one thread issues tcgen05.mma: D[128 tokens x N heads] (f32, TMEM) =
 //              K_tile[128 x d] . q[N x d]^T, N = H rounded up to 16; MXFP8 keeps one
 //              accumulator per 32-wide group so the group scales apply exactly;
-//   warps 2-5  epilogue: TMEM lane i = token i; each thread reads its token's head
-//              scores with tcgen05.ld, applies scales, activation and head weights,
-//              sums over heads and stores one f32 score.
-// Accumulators are double buffered in TMEM so the epilogue of one tile overlaps the
-// MMA of the next.  Every wait is bounded (see sm100::mbar_wait).
+//   warps 2-9  epilogue, two groups of four warps taking alternate tiles: TMEM lane
+//              i = token i; each thread reads its token's head scores with
+//              tcgen05.ld, applies scales, activation and head weights, sums over
+//              heads and stores one f32 score.
+// Four TMEM accumulators (two for MXFP8, whose four groups need four times the
+// columns) let the MMA run ahead of both epilogue groups.  Every wait is bounded (see
+// sm100::mbar_wait).
 #include <cudaTypedefs.h>
 
 #include "sm100.cuh"
@@ -30,7 +32,8 @@ namespace {
 
 using namespace sm100;
 
-constexpr int kTcThreads = 192;
+constexpr int kEpiGroups = 2;                    // epilogue groups, alternating tiles
+constexpr int kTcThreads = 64 + kEpiGroups * 128; // producer warp, MMA warp, 4 warps per group
 constexpr int kTileTok = 128;
 constexpr int kMaxRowsPerLaunch = 1024;
 
@@ -48,10 +51,11 @@ struct Cfg {
   static constexpr int kKSteps = kRowBytes / 32;           // one MMA consumes 32 bytes of K
   static constexpr int kGroups = KIND == 2 ? D / 32 : 1;
   static constexpr int kAccCols = 64 * kGroups;
-  static constexpr int kTmemCols = 2 * kAccCols;
+  static constexpr int kNumAcc = KIND == 2 ? 2 : 4;        // TMEM accumulator buffers
+  static constexpr int kTmemCols = kNumAcc * kAccCols;
   static constexpr uint32_t kFmt = KIND == 0 ? 1u : 0u;    // bf16 / e4m3
   static constexpr int kSmem = 1024 /*align*/ + kStages * kStageBytes + 2 * kQSlotBytes + 4096 /*bars*/ +
-                               3 * (kMaxRowsPerLaunch + 1) * 4 + 4 * (64 + 64 * 4 + 4) * 4;
+                               3 * (kMaxRowsPerLaunch + 1) * 4 + 4 * kEpiGroups * (64 + 64 * 4 + 4) * 4;
 };
 
 struct TcArgs {
@@ -81,8 +85,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   uint64_t* full = bars;
   uint64_t* empty = full + C::kStages;
   uint64_t* acc_full = empty + C::kStages;
-  uint64_t* acc_empty = acc_full + 2;
-  uint64_t* q_full = acc_empty + 2;
+  uint64_t* acc_empty = acc_full + C::kNumAcc;
+  uint64_t* q_full = acc_empty + C::kNumAcc;
   uint64_t* q_empty = q_full + 2;
   uint64_t* drain = q_empty + 2;
   uint32_t* tmem_base_s = (uint32_t*)(drain + 1);
@@ -98,9 +102,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < C::kNumAcc; ++i) {
       mbar_init(&acc_full[i], 1);
-      mbar_init(&acc_empty[i], 4);
+      mbar_init(&acc_empty[i], 4);  // the four warps of the group that drains it
+    }
+    for (int i = 0; i < 2; ++i) {
       mbar_init(&q_full[i], 1);
       mbar_init(&q_empty[i], 1);
     }
@@ -208,7 +214,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (lane == 0) {
       const uint32_t idesc_v = idesc(128, N, C::kFmt, C::kFmt);
       int stage = 0, acc = 0;
-      uint32_t phase = 0, acc_phase = 0;
+      uint32_t phase = 0, acc_phase = 0;  // acc cycles through kNumAcc buffers
       int r = 0, cur_row = -1, qcount = 0, slot = 0;
       for (int it = it_begin; it < it_end; ++it) {
         while (prefix[r + 1] <= it) ++r;
@@ -244,7 +250,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           stage = 0;
           phase ^= 1;
         }
-        if (++acc == 2) {
+        if (++acc == C::kNumAcc) {
           acc = 0;
           acc_phase ^= 1;
         }
@@ -257,20 +263,25 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
   } else {
     // ================================ epilogue ====================================
+    // Group g drains the tiles n with n % kEpiGroups == g; tile n sits in accumulator
+    // n % kNumAcc.  Within a group, TMEM lane i (warp quarter q = warp & 3) = token i.
+    const int grp = (warp - 2) / 4;
     const int quarter = warp & 3;
-    const int i = quarter * 32 + lane;  // TMEM lane == token within the tile
+    const int i = quarter * 32 + lane;
     float* w_s = epi + (warp - 2) * (64 + 64 * 4 + 4);
     float* qs_s = w_s + 64;             // [h][g] query group scales (MX)
-    int acc = 0;
-    uint32_t acc_phase = 0;
     int r = 0, cur_row = -1;
     float qtok = 1.f;
     for (int it = it_begin; it < it_end; ++it) {
       while (prefix[r + 1] <= it) ++r;
+      const int n = it - it_begin;
+      if (n % kEpiGroups != grp) continue;
+      const int acc = n % C::kNumAcc;
+      const uint32_t acc_phase = (uint32_t)(n / C::kNumAcc) & 1u;
       const int grow = a.row0 + r;
       if (r != cur_row) {
         cur_row = r;
-        named_sync_warp();
+        __syncwarp();
         for (int h = lane; h < H; h += 32) {
           w_s[h] = p.head_w[(int64_t)grow * H + h];
           if (KIND == 2) {
@@ -280,7 +291,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           }
         }
         qtok = (KIND == 1) ? ((const float*)p.q_scale)[grow] : 1.f;
-        named_sync_warp();
+        __syncwarp();
       }
       const int tile = it - prefix[r];
       const int t = tile * kTileTok + i;
@@ -304,45 +315,60 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
       tc_fence_after();
-      float score = 0.f;
       const uint32_t tbase = tmem_base + ((uint32_t)(quarter * 32) << 16) + acc * C::kAccCols;
+      float part[4] = {0.f, 0.f, 0.f, 0.f};  // four independent sums over heads
+      if (KIND != 2) {
+        uint32_t v0[32], v1[32];
+        tmem_ld32(tbase, v0);
+        if (H > 32) tmem_ld32(tbase + 32, v1);
+        tmem_ld_wait();
+        const float sc = (KIND == 1) ? qtok * ks[0] : 1.f;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          if (j < H) {
+            float x = __uint_as_float(v0[j]);
+            if (KIND == 1) x *= sc;
+            if (p.act == DSA_ACT_RELU) x = fmaxf(x, 0.f);
+            part[j & 3] += x * w_s[j];
+          }
+        }
+        if (H > 32) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            if (32 + j < H) {
+              float x = __uint_as_float(v1[j]);
+              if (KIND == 1) x *= sc;
+              if (p.act == DSA_ACT_RELU) x = fmaxf(x, 0.f);
+              part[j & 3] += x * w_s[32 + j];
+            }
+          }
+        }
+      } else {
 #pragma unroll 1
-      for (int hc = 0; hc < 2; ++hc) {
-        if (hc * 32 >= H) break;
-        float hv[32];
+        for (int hc = 0; hc < 2; ++hc) {
+          if (hc * 32 >= H) break;
+          uint32_t v[C::kGroups][32];
 #pragma unroll
-        for (int j = 0; j < 32; ++j) hv[j] = 0.f;
-#pragma unroll
-        for (int g = 0; g < C::kGroups; ++g) {
-          uint32_t v[32];
-          tmem_ld32(tbase + g * 64 + hc * 32, v);
+          for (int g = 0; g < C::kGroups; ++g) tmem_ld32(tbase + g * 64 + hc * 32, v[g]);
           tmem_ld_wait();
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
-            const float x = __uint_as_float(v[j]);
-            if (KIND == 2) hv[j] += x * (ks[g] * qs_s[(hc * 32 + j) * 4 + g]);
-            else hv[j] = x;
-          }
-        }
+            const int h = hc * 32 + j;
+            if (h < H) {
+              float x = 0.f;
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const int h = hc * 32 + j;
-          if (h < H) {
-            float x = hv[j];
-            if (KIND == 1) x *= qtok * ks[0];
-            if (p.act == DSA_ACT_RELU) x = fmaxf(x, 0.f);
-            score += x * w_s[h];
+              for (int g = 0; g < C::kGroups; ++g) x += __uint_as_float(v[g][j]) * (ks[g] * qs_s[h * 4 + g]);
+              if (p.act == DSA_ACT_RELU) x = fmaxf(x, 0.f);
+              part[j & 3] += x * w_s[h];
+            }
           }
         }
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&acc_empty[acc]);
+      const float score = (part[0] + part[1]) + (part[2] + part[3]);
       if (valid) p.scores[(int64_t)grow * p.score_stride + t] = pg >= 0 ? score : -INFINITY;
-      if (++acc == 2) {
-        acc = 0;
-        acc_phase ^= 1;
-      }
     }
   }
 
