@@ -130,7 +130,8 @@ dsa_status_t check_sfa(const dsa_sfa_args_t* a, const dsa_latent_cache_t* c) {
 struct IndexerPlan {
   int32_t max_visible;
   int64_t score_stride;
-  size_t score_bytes;
+  size_t score_bytes;  // f32 score rows, then the per-row key histograms (all after the error word)
+  size_t hist_offset, hist_bytes;
 };
 
 IndexerPlan plan_indexer(int32_t max_visible, int32_t n_tokens) {
@@ -138,7 +139,10 @@ IndexerPlan plan_indexer(int32_t max_visible, int32_t n_tokens) {
   p.max_visible = max_visible;
   p.score_stride = ((int64_t)max_visible + 63) / 64 * 64;
   if (p.score_stride == 0) p.score_stride = 64;
-  p.score_bytes = align_up((size_t)n_tokens * p.score_stride * sizeof(float));
+  const size_t rows = align_up((size_t)n_tokens * p.score_stride * sizeof(float));
+  p.hist_offset = rows;
+  p.hist_bytes = align_up((size_t)n_tokens * kTopkBins * sizeof(uint32_t));
+  p.score_bytes = rows + p.hist_bytes;
   return p;
 }
 
@@ -150,7 +154,8 @@ struct SfaPlan {
 SfaPlan plan_sfa(int32_t n_tokens, int32_t n_heads, int32_t top_k) {
   SfaPlan p;
   const int tiles = (top_k + 63) / 64;
-  const int units = n_tokens * ((n_heads + 63) / 64);
+  (void)n_heads;
+  const int units = n_tokens * 2;  // one CTA pair per (token, split)
   int s = num_sms() / (units > 0 ? units : 1);
   if (s < 1) s = 1;
   if (s > tiles) s = tiles;
@@ -205,6 +210,7 @@ dsa_status_t run_indexer(const dsa_indexer_args_t* a, const dsa_index_cache_t* c
                          int32_t* out_idx, float* out_score, uint8_t* ws, cudaStream_t s, Tracer& tr) {
   uint32_t* err = (uint32_t*)ws;
   float* scores = (float*)(ws + kAlign);
+  uint32_t* hist = (uint32_t*)(ws + kAlign + ip.hist_offset);
   ScoreParams sp;
   sp.tv = token_view(pg, tk, ip.max_visible);
   sp.q = a->q;
@@ -213,12 +219,17 @@ dsa_status_t run_indexer(const dsa_indexer_args_t* a, const dsa_index_cache_t* c
   sp.k = c->data;
   sp.k_scale = c->scale;
   sp.scores = scores;
+  sp.hist = hist;
   sp.score_stride = ip.score_stride;
   sp.err = err;
   sp.n_heads = a->n_heads;
   sp.dim = c->dim;
   sp.act = (int)a->act;
   sp.max_page_blocks = (ip.max_visible + kPage - 1) / kPage;
+  tr.begin();
+  cudaError_t me = cudaMemsetAsync(hist, 0, ip.hist_bytes, s);
+  tr.end("hist_clear");
+  if (me != cudaSuccess) return cuda_fail(me, "clearing the key histograms");
   if (sp.max_page_blocks > 0) {
     const bool tc = score_tc_supported(c->dtype, c->dim, a->n_heads);
     tr.begin();
@@ -229,6 +240,7 @@ dsa_status_t run_indexer(const dsa_indexer_args_t* a, const dsa_index_cache_t* c
   TopkParams tp;
   tp.tv = sp.tv;
   tp.scores = scores;
+  tp.hist = hist;
   tp.score_stride = ip.score_stride;
   tp.out_idx = out_idx;
   tp.out_score = out_score;
@@ -259,7 +271,7 @@ dsa_status_t run_sfa(const dsa_sfa_args_t* a, const dsa_latent_cache_t* c, const
   p.split_len = sp_.split_len;
   p.scale_log2 = a->softmax_scale * 1.4426950408889634f;
   tr.begin();
-  cudaError_t e = launch_sfa(p, s);
+  cudaError_t e = launch_sfa_tc(p, s);
   tr.end("sfa");
   if (e != cudaSuccess) return cuda_fail(e, "sparse attention launch");
   if (p.n_splits > 1) {

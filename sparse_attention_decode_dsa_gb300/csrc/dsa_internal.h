@@ -13,9 +13,8 @@ constexpr int kMaxIdxHeads = 64;
 constexpr int kMaxSfaHeads = 128;
 constexpr int kLatentDim = 576;
 constexpr int kValueDim = 512;
-constexpr int kTopkCluster = 8;              // CTAs cooperating on one row's Top-K
-constexpr int kMaxTopkChunk = 24576;         // scores one Top-K CTA holds in shared memory
-constexpr int kMaxVisible = kTopkCluster * kMaxTopkChunk;  // longest row the Top-K handles
+constexpr int kTopkBins = 4096;              // per-row histogram of the keys' top 12 bits
+constexpr int kMaxVisible = 1 << 20;         // longest row (positions) the indexer handles
 
 // Everything a kernel needs to locate a token's row, sequence and visible range.
 struct TokenView {
@@ -36,6 +35,7 @@ struct ScoreParams {
   const void* k;           // [num_pages, 64, d]
   const void* k_scale;     // null | f32 [num_pages, 64] | u8 [num_pages, 64, d/32]
   float* scores;           // workspace
+  uint32_t* hist;          // workspace [T, kTopkBins]: counts of the keys' top 12 bits (zeroed)
   int64_t score_stride;
   uint32_t* err;
   int32_t n_heads, dim, act, max_page_blocks;
@@ -44,6 +44,7 @@ struct ScoreParams {
 struct TopkParams {
   TokenView tv;
   const float* scores;
+  const uint32_t* hist;
   int64_t score_stride;
   int32_t* out_idx;
   float* out_score;  // may be null
@@ -70,6 +71,7 @@ bool score_tc_supported(dsa_dtype_t dt, int dim, int n_heads);
 cudaError_t launch_score_tc(const ScoreParams& p, dsa_dtype_t dt, dsa_scale_t sk, cudaStream_t s);
 cudaError_t launch_topk(const TopkParams& p, int32_t max_visible, cudaStream_t s);
 cudaError_t launch_sfa(const SfaParams& p, cudaStream_t s);
+cudaError_t launch_sfa_tc(const SfaParams& p, cudaStream_t s);
 cudaError_t launch_sfa_combine(const SfaParams& p, cudaStream_t s);
 
 }  // namespace dsa

@@ -117,7 +117,10 @@ __global__ void __launch_bounds__(kScoreThreads) score_cuda_core_kernel(ScorePar
   // sum the four head lanes of this token
   score += __shfl_xor_sync(0xffffffffu, score, 1);
   score += __shfl_xor_sync(0xffffffffu, score, 2);
-  if (valid && j == 0) p.scores[(int64_t)row * p.score_stride + t] = score;
+  if (valid && j == 0) {
+    p.scores[(int64_t)row * p.score_stride + t] = score;
+    atomicAdd(p.hist + (int64_t)row * kTopkBins + (score_key(score) >> 20), 1u);
+  }
 }
 
 template <int D, int KIND>

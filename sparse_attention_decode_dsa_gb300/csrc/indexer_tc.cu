@@ -18,7 +18,8 @@
 //   warps 2-9  epilogue, two groups of four warps taking alternate tiles: TMEM lane
 //              i = token i; each thread reads its token's head scores with
 //              tcgen05.ld, applies scales, activation and head weights, sums over
-//              heads and stores one f32 score.
+//              heads, stores one f32 score and counts it in the row's histogram of
+//              key top-12-bit bins (what the Top-K pass starts from).
 // Four TMEM accumulators (two for MXFP8, whose four groups need four times the
 // columns) let the MMA run ahead of both epilogue groups.  Every wait is bounded (see
 // sm100::mbar_wait).
@@ -63,8 +64,6 @@ struct TcArgs {
   int32_t row0;   // first query row of this launch
   int32_t nrows;  // rows in this launch
 };
-
-__device__ __forceinline__ void named_sync_warp() { __syncwarp(); }
 
 template <int KIND, int D>
 __global__ void __launch_bounds__(kTcThreads, 1)
@@ -367,8 +366,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&acc_empty[acc]);
-      const float score = (part[0] + part[1]) + (part[2] + part[3]);
-      if (valid) p.scores[(int64_t)grow * p.score_stride + t] = pg >= 0 ? score : -INFINITY;
+      if (valid) {
+        const float v = pg >= 0 ? (part[0] + part[1]) + (part[2] + part[3]) : -INFINITY;
+        p.scores[(int64_t)grow * p.score_stride + t] = v;
+        atomicAdd(p.hist + (int64_t)grow * kTopkBins + (score_key(v) >> 20), 1u);
+      }
     }
   }
 

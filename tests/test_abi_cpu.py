@@ -51,8 +51,9 @@ def _call_indexer(pages, toks, cache, args, ws=256 * 1000, ws_bytes=1 << 30):
 def test_workspace_size_formula():
     pages, toks, cache, args, keep = _structs(lens=(100, 200))
     n = dsa.lib.dsa_indexer_workspace_size(C.byref(args), C.byref(cache), C.byref(pages), C.byref(toks))
-    # error word (256 B) + T rows x ceil(max visible / 64) * 64 f32 scores, 256-aligned
-    assert n == 256 + ((2 * 256 * 4 + 255) // 256) * 256
+    # error word (256 B) + T rows x ceil(max visible / 64) * 64 f32 scores (256-aligned)
+    # + T rows x 4096 u32 key-histogram bins
+    assert n == 256 + ((2 * 256 * 4 + 255) // 256) * 256 + 2 * 4096 * 4
 
 
 @pytest.mark.parametrize("mutate,status", [
