@@ -1,5 +1,6 @@
 // Internal declarations shared by the host API and the kernel translation units.
 #pragma once
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -64,6 +65,10 @@ struct SfaParams {
   int32_t n_heads, top_k, n_splits, split_len;
   float scale_log2;        // softmax_scale * log2(e)
 };
+
+// 2-D TMA map over `rows` rows of `row_elems` elements of `elem` bytes, 128-byte
+// swizzle, box = 128 bytes x box_rows (tma_host.cu).
+bool make_tma_2d_sw128(CUtensorMap* m, const void* base, uint64_t rows, int elem, int row_elems, int box_rows);
 
 // Launchers (each returns the cudaError_t of its launch).
 cudaError_t launch_score(const ScoreParams& p, dsa_dtype_t dt, dsa_scale_t sk, cudaStream_t s);

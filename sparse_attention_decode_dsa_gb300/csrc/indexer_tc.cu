@@ -23,8 +23,6 @@
 // Four TMEM accumulators (two for MXFP8, whose four groups need four times the
 // columns) let the MMA run ahead of both epilogue groups.  Every wait is bounded (see
 // sm100::mbar_wait).
-#include <cudaTypedefs.h>
-
 #include "sm100.cuh"
 
 namespace dsa {
@@ -313,6 +311,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       if (lane == 0) ok = mbar_wait(&acc_full[acc], acc_phase, abort_flag, p.err);
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
+      __syncwarp();
       tc_fence_after();
       const uint32_t tbase = tmem_base + ((uint32_t)(quarter * 32) << 16) + acc * C::kAccCols;
       float part[4] = {0.f, 0.f, 0.f, 0.f};  // four independent sums over heads
@@ -383,48 +382,20 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   }
 }
 
-// ---- host side: tensor maps and launch --------------------------------------------------
-PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (!fn) {
-    cudaDriverEntryPointQueryResult q;
-    void* ptr = nullptr;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = (PFN_cuTensorMapEncodeTiled_v12000)ptr;
-  }
-  return fn;
-}
-
-// 2-D map over rows of `row_bytes` bytes with 128-byte swizzle; box = 128 B x box_rows.
-bool make_map(CUtensorMap* m, const void* base, uint64_t rows, int elem, int row_elems, int box_rows) {
-  auto enc = get_encode();
-  if (!enc) return false;
-  const CUtensorMapDataType dt = elem == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8;
-  cuuint64_t dims[2] = {(cuuint64_t)row_elems, (cuuint64_t)rows};
-  cuuint64_t strides[1] = {(cuuint64_t)row_elems * elem};
-  cuuint32_t box[2] = {(cuuint32_t)(128 / elem), (cuuint32_t)box_rows};
-  cuuint32_t estr[2] = {1, 1};
-  CUresult r = enc(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
-}
-
+// ---- host side: launch ---------------------------------------------------------------
 template <int KIND, int D>
 cudaError_t launch_tc(const ScoreParams& p, cudaStream_t s) {
   using C = Cfg<KIND, D>;
   static_assert(C::kSmem <= 232448, "shared memory budget");
   CUtensorMap kmap, qmap;
-  if (!make_map(&kmap, p.k, (uint64_t)p.tv.num_pages * kPage, C::kElem, D, kPage)) return cudaErrorInvalidValue;
+  if (!make_tma_2d_sw128(&kmap, p.k, (uint64_t)p.tv.num_pages * kPage, C::kElem, D, kPage)) return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(score_tc_kernel<KIND, D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        C::kSmem);
   if (e != cudaSuccess) return e;
   int dev = 0, sms = 0;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  if (!make_map(&qmap, p.q, (uint64_t)p.tv.n_tokens * p.n_heads, C::kElem, D, p.n_heads))
+  if (!make_tma_2d_sw128(&qmap, p.q, (uint64_t)p.tv.n_tokens * p.n_heads, C::kElem, D, p.n_heads))
     return cudaErrorInvalidValue;
   for (int row0 = 0; row0 < p.tv.n_tokens; row0 += kMaxRowsPerLaunch) {
     TcArgs a;

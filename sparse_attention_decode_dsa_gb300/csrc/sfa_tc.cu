@@ -10,21 +10,26 @@
 //
 // Work split inside the pair (CTA c = 0, 1):
 //   * CTA c owns value dims [256c, 256c + 256) of the output, and contracts the logits
-//     over its 288 "own" dims: latent [256c, 256c + 256) and rope [512 + 32c, +32), so
-//     each CTA gathers exactly half of every selected 1152-byte row.
+//     over its 288 "own" dims: latent [256c, 256c + 256) and rope [512 + 32c, +32).
+//     Each CTA gathers its 512 latent bytes and the 128 rope bytes of every selected
+//     row (the pair reads each 1152-byte row once from DRAM).
 //   * Each CTA computes partial logits S_c = Q[:, own] . KV[:, own]^T (tcgen05, A = Q
 //     from tensor memory, B = gathered rows in shared memory), sends them to its peer
-//     through distributed shared memory (st.async, counted on the peer's mbarrier) and
-//     adds the peer's part: both CTAs hold the same S = S_0 + S_1.
+//     through distributed shared memory (each warp stages its 32 rows and moves them
+//     with one bulk copy, counted in bytes on the peer's mbarrier) and adds the peer's
+//     part: both CTAs hold the same S = S_0 + S_1.
 //   * Online softmax per head row (thread = row, no shuffles), base 2; the reference
 //     maximum only moves when a tile's maximum exceeds it by 8 (2^8 headroom), and O is
 //     then rescaled in tensor memory.
 //   * P (bf16) goes to tensor memory; O[128 x 256] += P . V with V read MN-major from
 //     the same shared-memory rows the logits used.
-// Warp roles: warp 0 gathers rows with 16-byte cp.async into a 4-stage ring laid out in
-// 128-byte swizzle atoms; warp 1 (one thread) issues the MMAs; warps 2-5 run softmax
-// and the epilogue.  Tensor memory (512 columns): O [0,256), S [256,320), P [320,352),
-// Q rope [352,368), Q latent [384,512).  Every wait is bounded.
+// Warp roles: warps 0-2 (one thread each) gather rows with TMA gather4 into a 3-stage
+// ring of 128-byte swizzle atoms; warp 3 (one thread) issues each MMA as soon as its
+// inputs are ready; warps 4-7 run softmax and the epilogue, skewed by one tile: they load
+// and send the partial logits of tile n + 1 before finishing tile n, so the exchange
+// overlaps the softmax.  Tensor memory (512 columns): O [0,256), S [256,320), P [320,352),
+// Q rope [352,368), Q latent [384,512).  Every wait is bounded.  Shared memory per stage:
+// 4 latent regions + 1 rope region, each 64 rows x 128 B.
 #include "sm100.cuh"
 
 namespace dsa {
@@ -33,17 +38,20 @@ namespace {
 
 using namespace sm100;
 
-constexpr int kThreads = 192;
+constexpr int kGatherWarps = 3;                  // warps 0-2 gather (TMA), warp 3 issues MMAs,
+constexpr int kMmaWarp = kGatherWarps;           // warps 4-7 run softmax and the epilogue
+constexpr int kThreads = (kGatherWarps + 5) * 32;
 constexpr int kTok = 64;                         // selected positions per tile
-constexpr int kStages = 4;
+constexpr int kStages = 3;
 constexpr int kRegion = kTok * 128;              // 64 rows x 128 B
 constexpr int kStageBytes = 5 * kRegion;         // 4 latent regions + 1 rope region
 constexpr int kXchBytes = 128 * kTok * 4;        // one f32 partial-logit tile
 constexpr int kMaxSplitLen = kMaxTopK;
 constexpr uint32_t kColO = 0, kColS = 256, kColP = 320, kColQr = 352, kColQl = 384;
-constexpr int kSmem = 1024 + kStages * kStageBytes + kXchBytes + kMaxSplitLen * 4 + 512;
+constexpr int kSmem = 1024 + kStages * kStageBytes + 3 * kXchBytes + kMaxSplitLen * 4 + 512;
 
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) sfa_tc_kernel(SfaParams p) {
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    sfa_tc_kernel(const __grid_constant__ CUtensorMap kvmap, SfaParams p) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t c = cluster_rank();
   const uint32_t peer = c ^ 1u;
@@ -54,8 +62,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) sfa_tc_
   const uint32_t raw_u32 = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + ((1024 - (raw_u32 & 1023)) & 1023);
   uint8_t* stages = smem;
-  float* xch = (float*)(stages + kStages * kStageBytes);      // [128 rows][64] peer partial
-  int32_t* rowid = (int32_t*)((uint8_t*)xch + kXchBytes);     // cache row of each slot or -1
+  float* xch = (float*)(stages + kStages * kStageBytes);      // [2][128 rows][64] peer partials
+  float* stg = (float*)((uint8_t*)xch + 2 * kXchBytes);       // [128 rows][64] own partial, outbound
+  int32_t* rowid = (int32_t*)((uint8_t*)stg + kXchBytes);     // cache row of each slot or -1
   uint64_t* bars = (uint64_t*)(rowid + kMaxSplitLen);
   uint64_t* kv_full = bars;
   uint64_t* kv_empty = kv_full + kStages;
@@ -64,11 +73,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) sfa_tc_
   uint64_t* s_free = s_full + 1;
   uint64_t* p_full = s_free + 1;
   uint64_t* pv_done = p_full + 1;
-  uint64_t* xch_full = pv_done + 1;
-  uint64_t* xch_empty = xch_full + 1;
-  uint64_t* drain = xch_empty + 1;
+  uint64_t* xch_full = pv_done + 1;    // [2]: peer partial of tile t in buffer t & 1
+  uint64_t* xch_empty = xch_full + 2;  // [2]: the peer has read our partial of tile t
+  uint64_t* drain = xch_empty + 2;
   uint32_t* tmem_base_s = (uint32_t*)(drain + 1);
   volatile int* abort_flag = (volatile int*)(tmem_base_s + 1);
+  int* fill_row_s = (int*)(abort_flag + 1);  // a selected row that stands in for empty slots
 
   int b, n_vis;
   resolve_token(p.tv, tok, &b, &n_vis, nullptr);
@@ -79,7 +89,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) sfa_tc_
 
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(&kv_full[s], 1);
+      mbar_init(&kv_full[s], kGatherWarps);
       mbar_init(&kv_empty[s], 1);
     }
     mbar_init(q_ready, 4);
@@ -87,110 +97,134 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) sfa_tc_
     mbar_init(s_free, 4);
     mbar_init(p_full, 4);
     mbar_init(pv_done, 1);
-    mbar_init(xch_full, 1);
-    mbar_init(xch_empty, 4);  // the peer's four softmax warps
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&xch_full[i], 1);   // armed locally per tile; the peer's four copies count bytes
+      mbar_init(&xch_empty[i], 4);  // the peer's four softmax warps, after reading their rows
+    }
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
-    if (n_tiles > 0) mbar_arrive_expect_tx(xch_full, kXchBytes);  // the peer's tile-0 partial
   }
-  if (warp == 1) {
+  if (warp == kMmaWarp) {
     tmem_alloc(tmem_base_s, 512);
     tmem_relinquish();
   }
-  // cache rows of the selected positions of this split (-1: padding or invalid)
-  for (int j = tid; j < n_tiles * kTok; j += kThreads) {
-    const int jj = j_begin + j;
-    int rid = -1;
-    if (jj < j_end) {
-      const int pos = __ldg(p.idx + (int64_t)tok * p.top_k + jj);
-      if (pos >= n_vis || pos < -1) {
+  // cache rows of the selected positions of this split (-1: padding or invalid); all
+  // index loads of a thread are in flight together, then all page-table loads
+  {
+    constexpr int kPer = (kMaxSplitLen + kThreads - 1) / kThreads;
+    int pos[kPer];
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) {
+      const int j = tid + u * kThreads;
+      pos[u] = (j < n_tiles * kTok && j_begin + j < j_end) ? __ldg(p.idx + (int64_t)tok * p.top_k + j_begin + j)
+                                                            : -1;
+      if (pos[u] >= n_vis || pos[u] < -1) {
         if (c == 0) atomicOr(p.err, DSA_DEVERR_INDEX);
-      } else if (pos >= 0) {
-        const int pg = physical_page(p.tv, b, pos >> 6, c == 0 ? p.err : nullptr);
-        if (pg >= 0) rid = pg * kPage + (pos & 63);
+        pos[u] = -1;
       }
     }
-    rowid[j] = rid;
+    int pg[kPer];
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) pg[u] = pos[u] >= 0 ? __ldg(p.tv.block_table + (int64_t)b * p.tv.max_pages + (pos[u] >> 6)) : -1;
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) {
+      const int j = tid + u * kThreads;
+      if (j >= n_tiles * kTok) break;
+      int rid = -1;
+      if (pos[u] >= 0) {
+        if (pg[u] < 0 || pg[u] >= p.tv.num_pages) {
+          if (c == 0) atomicOr(p.err, DSA_DEVERR_PAGE_ID);
+        } else {
+          rid = pg[u] * kPage + (pos[u] & 63);
+        }
+      }
+      rowid[j] = rid;
+    }
+  }
+  __syncthreads();
+  if (tid == 0) {
+    int fr = -1;
+    for (int j = 0; j < n_tiles * kTok && fr < 0; ++j) fr = rowid[j];
+    *fill_row_s = fr;
+    if (fr >= 0) tma_prefetch_desc(&kvmap);
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // A split without any selected row attends to nothing: skip the pipeline entirely.
+  const int n_tiles_run = *fill_row_s >= 0 ? n_tiles : 0;
+  if (tid == 0)
+    for (int t = 0; t < 2 && t < n_tiles_run; ++t) mbar_arrive_expect_tx(&xch_full[t], kXchBytes);  // tiles 0, 1
   cluster_sync_all();  // both CTAs' barriers exist before any remote traffic
   const uint32_t tmem = *tmem_base_s;
 
-  if (warp == 0) {
-    // ============================ gather (cp.async) ====================================
-    // Tile n's copies are known complete (cp.async.wait_group) when tile n + kLag has
-    // been issued; only then is it signalled.  Before the producer blocks on a stage
-    // (tile n needs the stage of tile n - kStages, freed by P.V of that tile, which the
-    // MMA issues after the logits of tile n - kStages + 1), that tile must already be
-    // signalled: n - 1 - kLag >= n - kStages + 1, i.e. kLag <= kStages - 2.
-    constexpr int kLag = kStages - 2;
-    const uint16_t* kv = p.kv;
-    int n = 0, signalled = 0;
-    for (; n < n_tiles; ++n) {
-      const int stage = n % kStages;
-      bool ok = true;
-      if (lane == 0) ok = mbar_wait(&kv_empty[stage], ((n / kStages) & 1) ^ 1, abort_flag, p.err);
-      if (!__shfl_sync(0xffffffffu, ok, 0)) break;
-      const uint32_t sbase = smem_u32(stages + stage * kStageBytes);
+  if (warp < kGatherWarps) {
+    // ============================ gather (TMA) =========================================
+    // Per tile and per group of 4 slots: four 128-byte pieces of this CTA's latent dims
+    // and the 128-byte rope piece, each one gather4 of four rows, landing as 128-byte
+    // swizzled rows.  Gather warp w issues the groups g with g % kGatherWarps == w.
+    // Empty slots fetch a selected row; their logits are masked.
+    if (lane == 0) {
+      constexpr int kAllGroups = kTok / 4;
+      const int my_groups = (kAllGroups - warp + kGatherWarps - 1) / kGatherWarps;
+      const int fill = *fill_row_s;
+      for (int n = 0; n < n_tiles_run; ++n) {
+        const int stage = n % kStages;
+        if (!mbar_wait(&kv_empty[stage], ((n / kStages) & 1) ^ 1, abort_flag, p.err)) break;
+        mbar_arrive_expect_tx(&kv_full[stage], my_groups * 5 * 512);
+        const uint32_t sbase = smem_u32(stages + stage * kStageBytes);
+        const int32_t* rt = rowid + n * kTok;
+#pragma unroll 1
+        for (int g = warp; g < kAllGroups; g += kGatherWarps) {
+          int r[4];
 #pragma unroll
-      for (int rr = 0; rr < 2; ++rr) {
-        const int j = lane + 32 * rr;
-        const int rid = rowid[n * kTok + j];
-        const int bytes = rid >= 0 ? 16 : 0;
-        const uint16_t* src = kv + (int64_t)(rid >= 0 ? rid : 0) * kLatentDim;
-        const uint32_t rowbase = sbase + j * 128;
-        const uint32_t sw = (uint32_t)(j & 7);
+          for (int i = 0; i < 4; ++i) {
+            const int v = rt[4 * g + i];
+            r[i] = v >= 0 ? v : fill;
+          }
 #pragma unroll
-        for (int u = 0; u < 32; ++u) {  // own latent dims: 4 regions x 8 chunks of 16 B
-          cp_async_16(rowbase + (u >> 3) * kRegion + ((((uint32_t)u & 7u) ^ sw) << 4), src + 256 * c + u * 8, bytes);
-        }
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {  // own rope dims: first 64 B of the rope region row
-          cp_async_16(rowbase + 4 * kRegion + (((uint32_t)u ^ sw) << 4), src + 512 + 32 * c + u * 8, bytes);
+          for (int q = 0; q < 4; ++q)
+            tma_gather4(sbase + q * kRegion + g * 512, &kvmap, &kv_full[stage], 256 * (int)c + 64 * q, r[0], r[1],
+                        r[2], r[3]);
+          tma_gather4(sbase + 4 * kRegion + g * 512, &kvmap, &kv_full[stage], 512, r[0], r[1], r[2], r[3]);
         }
       }
-      cp_async_commit();
-      if (n >= kLag) {
-        cp_async_wait<kLag>();
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&kv_full[(n - kLag) % kStages]);
-        signalled = n - kLag + 1;
-      }
     }
-    cp_async_wait<0>();
-    fence_proxy_async_smem();
-    __syncwarp();
-    if (lane == 0 && !*abort_flag) {
-      for (int m = signalled; m < n; ++m) mbar_arrive(&kv_full[m % kStages]);
-    }
-  } else if (warp == 1) {
+  } else if (warp == kMmaWarp) {
     // ============================ MMA issuer ==========================================
+    // Event driven: the logits of tile t (QK(t): needs its rows and the softmax to have
+    // taken S(t - 1)) and P.V of tile m (needs P(m)) are issued as soon as their inputs
+    // are ready, so neither waits behind the other.  QK(t) writes S over the 288 own
+    // dims: 16 latent steps (A = Q latent columns) and 2 rope steps (this CTA's 32 of
+    // the 64 gathered rope dims).
     if (lane == 0) {
       const uint32_t id_qk = idesc(128, kTok, 1u, 1u);
       const uint32_t id_pv = idesc_bmn(128, 256, 1u, 1u);
       bool ok = mbar_wait(q_ready, 0, abort_flag, p.err);
-      for (int n = 0; ok && n <= n_tiles; ++n) {
-        if (n < n_tiles) {
-          const int stage = n % kStages;
-          if (!(ok = mbar_wait(&kv_full[stage], (n / kStages) & 1, abort_flag, p.err))) break;
-          if (n > 0 && !(ok = mbar_wait(s_free, (n - 1) & 1, abort_flag, p.err))) break;
-          tc_fence_after();
-          const uint32_t sb = smem_u32(stages + stage * kStageBytes);
+      int next_qk = 0, next_pv = 0;
+      long long idle_since = clock64();
+      while (ok && next_pv < n_tiles_run) {
+        bool progress = false;
+        if (next_qk < n_tiles_run) {
+          const int t = next_qk, stage = t % kStages;
+          if (mbar_try_wait(smem_u32(&kv_full[stage]), (t / kStages) & 1) &&
+              (t == 0 || mbar_try_wait(smem_u32(s_free), (t - 1) & 1))) {
+            tc_fence_after();
+            const uint32_t sb = smem_u32(stages + stage * kStageBytes);
 #pragma unroll
-          for (int k = 0; k < 18; ++k) {  // 16 latent steps + 2 rope steps of 16 dims
-            const uint32_t a = tmem + (k < 16 ? kColQl + 8 * k : kColQr + 8 * (k - 16));
-            const uint32_t boff = k < 16 ? (k >> 2) * kRegion + (k & 3) * 32 : 4 * kRegion + (k - 16) * 32;
-            mma_f16_ts(tmem + kColS, a, desc_sw128(sb + boff), id_qk, k > 0);
+            for (int k = 0; k < 18; ++k) {
+              const uint32_t a = tmem + (k < 16 ? kColQl + 8 * k : kColQr + 8 * (k - 16));
+              const uint32_t boff = k < 16 ? (k >> 2) * kRegion + (k & 3) * 32 : 4 * kRegion + 64 * c + (k - 16) * 32;
+              mma_f16_ts(tmem + kColS, a, desc_sw128(sb + boff), id_qk, k > 0);
+            }
+            tc_commit(s_full);
+            ++next_qk;
+            progress = true;
           }
-          tc_commit(s_full);
         }
-        if (n > 0) {
-          const int m = n - 1, stage = m % kStages;
-          if (!(ok = mbar_wait(p_full, m & 1, abort_flag, p.err))) break;
+        if (next_pv < next_qk && mbar_try_wait(smem_u32(p_full), next_pv & 1)) {
+          const int m = next_pv, stage = m % kStages;
           tc_fence_after();
           const uint32_t sb = smem_u32(stages + stage * kStageBytes);
 #pragma unroll
@@ -199,6 +233,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) sfa_tc_
                        (m > 0 || j > 0) ? 1u : 0u);
           tc_commit(pv_done);
           tc_commit(&kv_empty[stage]);
+          ++next_pv;
+          progress = true;
+        }
+        if (progress) {
+          idle_since = clock64();
+        } else if (*abort_flag) {
+          ok = false;
+        } else if (clock64() - idle_since > kWaitLimitCycles) {
+          atomicOr(p.err, DSA_DEVERR_TIMEOUT);
+          *abort_flag = 1;
+          ok = false;
         }
       }
       tc_commit(drain);
@@ -243,19 +288,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) sfa_tc_
       __syncwarp();
       if (lane == 0) mbar_arrive(q_ready);
     }
-    const uint32_t xch_local = smem_u32(xch);
-    const uint32_t xch_peer = map_to_rank(xch_local, peer);
-    const uint32_t xfull_peer = map_to_rank(smem_u32(xch_full), peer);
-    const uint32_t xempty_peer = map_to_rank(smem_u32(xch_empty), peer);
+    const uint32_t warp_rows = (uint32_t)(quarter * 32) * (kTok * 4);  // this warp's 8 KB slice
+    const uint32_t xch_peer0 = map_to_rank(smem_u32(xch) + warp_rows, peer);
+    const uint32_t stg_local = smem_u32(stg) + warp_rows;
+    const uint32_t xfull_peer0 = map_to_rank(smem_u32(&xch_full[0]), peer);
+    const uint32_t xempty_peer0 = map_to_rank(smem_u32(&xch_empty[0]), peer);
     const uint32_t myrow = (uint32_t)h * (kTok * 4);
     const uint32_t sw = (uint32_t)(h & 7);
     float m_ref = -INFINITY, l = 0.f;
     bool ok = true;
-    for (int n = 0; n < n_tiles; ++n) {
-      if (lane == 0) ok = mbar_wait(s_full, n & 1, abort_flag, p.err);
-      if (!__shfl_sync(0xffffffffu, ok, 0)) { ok = false; break; }
+
+    // Loads this CTA's partial logits of tile t into `dst`, frees the logit columns for
+    // the next QK, and sends them (staging + one bulk copy per warp) to the peer's
+    // buffer t & 1 once the peer has read tile t - 2 from it.  Returns false on abort.
+    auto load_and_send = [&](int t, float (&dst)[kTok]) -> bool {
+      bool good = true;
+      if (lane == 0) good = mbar_wait(s_full, t & 1, abort_flag, p.err);
+      if (!__shfl_sync(0xffffffffu, good, 0)) return false;
+      __syncwarp();
       tc_fence_after();
-      float s[kTok];
       {
         uint32_t v0[32], v1[32];
         tmem_ld32(tmem + lane_off + kColS, v0);
@@ -263,48 +314,76 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) sfa_tc_
         tmem_ld_wait();
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
-          s[j] = __uint_as_float(v0[j]);
-          s[32 + j] = __uint_as_float(v1[j]);
+          dst[j] = __uint_as_float(v0[j]);
+          dst[32 + j] = __uint_as_float(v1[j]);
         }
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(s_free);
-      // exchange partial logits with the peer
-      if (n > 0) {
-        if (lane == 0) ok = mbar_wait(xch_empty, (n - 1) & 1, abort_flag, p.err);
-        if (!__shfl_sync(0xffffffffu, ok, 0)) { ok = false; break; }
+      if (lane == 0) {
+        mbar_arrive(s_free);
+        if (t > 0) bulk_wait_read0();  // staging free again
       }
+      __syncwarp();
 #pragma unroll
       for (int u = 0; u < kTok / 4; ++u)
-        st_async_v4(xch_peer + myrow + (((uint32_t)u ^ sw) << 4),
-                    make_float4(s[4 * u], s[4 * u + 1], s[4 * u + 2], s[4 * u + 3]), xfull_peer);
-      if (lane == 0) ok = mbar_wait(xch_full, n & 1, abort_flag, p.err);
+        *(float4*)((uint8_t*)stg + myrow + (((uint32_t)u ^ sw) << 4)) =
+            make_float4(dst[4 * u], dst[4 * u + 1], dst[4 * u + 2], dst[4 * u + 3]);
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        const int bb = t & 1;
+        if (t >= 2) good = mbar_wait_cluster(&xch_empty[bb], ((t >> 1) & 1) ^ 1, abort_flag, p.err);
+        if (good) {
+          bulk_copy_to_peer(xch_peer0 + bb * kXchBytes, stg_local, 32 * kTok * 4, xfull_peer0 + bb * 8);
+          bulk_commit();
+        }
+      }
+      return __shfl_sync(0xffffffffu, good, 0);
+    };
+
+    float sc[kTok];  // own partial logits of the tile being finished
+    if (n_tiles_run > 0) ok = load_and_send(0, sc);
+    for (int n = 0; ok && n < n_tiles_run; ++n) {
+      // ---- start tile n + 1: its exchange overlaps the rest of tile n --------------
+      float sn[kTok];
+      if (n + 1 < n_tiles_run && !(ok = load_and_send(n + 1, sn))) break;
+      // ---- finish tile n -----------------------------------------------------------
+      const int bb = n & 1;
+      const int32_t* rt = rowid + n * kTok;
+      const uint32_t vlo = __ballot_sync(0xffffffffu, rt[lane] >= 0);
+      const uint32_t vhi = __ballot_sync(0xffffffffu, rt[32 + lane] >= 0);
+      if (lane == 0) {
+        ok = mbar_wait(&xch_full[bb], (n >> 1) & 1, abort_flag, p.err);
+        if (ok && h == 0 && n + 2 < n_tiles_run) mbar_arrive_expect_tx(&xch_full[bb], kXchBytes);  // tile n + 2
+      }
       if (!__shfl_sync(0xffffffffu, ok, 0)) { ok = false; break; }
-      if (h == 0 && n + 1 < n_tiles) mbar_arrive_expect_tx(xch_full, kXchBytes);  // next tile's partial
+      __syncwarp();
+      const uint8_t* recv = (const uint8_t*)xch + bb * kXchBytes + myrow;
+      float* s = sc;  // full logits of tile n, summed in place
 #pragma unroll
       for (int u = 0; u < kTok / 4; ++u) {
-        const float4 r = *(const float4*)((const uint8_t*)xch + myrow + (((uint32_t)u ^ sw) << 4));
+        const float4 r = *(const float4*)(recv + (((uint32_t)u ^ sw) << 4));
         s[4 * u] += r.x;
         s[4 * u + 1] += r.y;
         s[4 * u + 2] += r.z;
         s[4 * u + 3] += r.w;
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive_remote(xempty_peer);
+      if (lane == 0) mbar_arrive_remote_relaxed(xempty_peer0 + bb * 8);  // its loads fed the adds above
       // online softmax (base 2), masked positions get no weight
-      const int32_t* rt = rowid + n * kTok;
       float tmax = -INFINITY;
 #pragma unroll
       for (int j = 0; j < kTok; ++j) {
-        s[j] = rt[j] >= 0 ? s[j] * p.scale_log2 : -INFINITY;
+        const bool v = ((j < 32 ? vlo : vhi) >> (j & 31)) & 1u;
+        s[j] = v ? s[j] * p.scale_log2 : -INFINITY;
         tmax = fmaxf(tmax, s[j]);
       }
       float alpha = 1.f;
       bool rescale = false;
       if (tmax != -INFINITY && (m_ref == -INFINITY || tmax > m_ref + 8.f)) {
         if (m_ref != -INFINITY) {
-          alpha = exp2f(m_ref - tmax);
+          alpha = fast_exp2(m_ref - tmax);
           rescale = true;
         }
         m_ref = tmax;
@@ -313,13 +392,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) sfa_tc_
       const float msub = m_ref == -INFINITY ? 0.f : m_ref;  // nothing visible yet: all weights 0
 #pragma unroll
       for (int j = 0; j < kTok; ++j) {
-        s[j] = exp2f(s[j] - msub);  // exp2(-inf) = 0 for masked positions
+        s[j] = fast_exp2(s[j] - msub);  // 2^-inf = 0 for masked positions
         rs += s[j];
       }
       l = l * alpha + rs;
-      if (n > 0) {
+      if (n > 0) {  // P.V of tile n - 1 has consumed P and updated O
         if (lane == 0) ok = mbar_wait(pv_done, (n - 1) & 1, abort_flag, p.err);
         if (!__shfl_sync(0xffffffffu, ok, 0)) { ok = false; break; }
+        __syncwarp();
         tc_fence_after();
       }
       if (__any_sync(0xffffffffu, rescale)) {  // rare: move O to the new reference maximum
@@ -343,11 +423,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) sfa_tc_
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(p_full);
+#pragma unroll
+      for (int j = 0; j < kTok; ++j) sc[j] = sn[j];  // own logits of tile n + 1
     }
     // ---- epilogue: O / l -> this CTA's 256 value dims ----------------------------------
-    if (ok && n_tiles > 0) {
-      if (lane == 0) ok = mbar_wait(pv_done, (n_tiles - 1) & 1, abort_flag, p.err);
+    if (ok && n_tiles_run > 0) {
+      if (lane == 0) ok = mbar_wait(pv_done, (n_tiles_run - 1) & 1, abort_flag, p.err);
       ok = __shfl_sync(0xffffffffu, ok, 0);
+      __syncwarp();
     }
     if (ok) {
       tc_fence_after();
@@ -356,7 +439,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) sfa_tc_
 #pragma unroll 1
       for (int ch = 0; ch < 8; ++ch) {
         uint32_t v[32];
-        if (n_tiles > 0) {
+        if (n_tiles_run > 0) {
           tmem_ld32(tmem + lane_off + kColO + 32 * ch, v);
           tmem_ld_wait();
         } else {
@@ -390,10 +473,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) sfa_tc_
   }
 
   // ---- tear-down ---------------------------------------------------------------------
+  if (warp > kMmaWarp && lane == 0) bulk_wait_read0();
   tc_fence_before();
   __syncthreads();
   cluster_sync_all();  // the peer's last remote arrivals and stores have landed
-  if (warp == 1) {
+  if (warp == kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
@@ -402,10 +486,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) sfa_tc_
 }  // namespace
 
 cudaError_t launch_sfa_tc(const SfaParams& p, cudaStream_t s) {
+  CUtensorMap kvmap;  // the latent cache as [pages * 64 rows, 576], one-row boxes of 64 elements
+  if (!make_tma_2d_sw128(&kvmap, p.kv, (uint64_t)p.tv.num_pages * kPage, 2, kLatentDim, 1))
+    return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(sfa_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
   if (e != cudaSuccess) return e;
   dim3 grid(2 * p.n_splits, p.tv.n_tokens);
-  sfa_tc_kernel<<<grid, kThreads, kSmem, s>>>(p);
+  sfa_tc_kernel<<<grid, kThreads, kSmem, s>>>(kvmap, p);
   return cudaGetLastError();
 }
 

@@ -8,29 +8,37 @@
 //
 // Scores are compared through an order-preserving 32-bit key (score_key).  The scoring
 // pass already counted, per row, how many keys fall in each of the 4096 bins of their
-// top 12 bits (kept in the workspace).  One CTA per row then
-//   1. finds the bin holding the K-th largest key from that histogram;
-//   2. gathers the keys of that bin (the candidates) into shared memory;
-//   3. finds the exact K-th largest key T among them with an MSB-first radix select
-//      over the remaining 20 bits (8 + 8 + 4), and how many keys equal to T to take;
-//   4. writes, in position order, every key > T and the first (K - #{> T}) keys == T:
-//      each warp owns contiguous ranges; a count, a block scan that places the warps,
-//      and a write.
-// Keys are read from the score row in blocks of 32768 positions held in registers (32
-// per thread, all loads issued together), so a row of up to 32768 positions is read
-// from L2 once.
-// If the candidates overflow shared memory (a row with very many equal top bits), step
-// 3 scans the whole row instead of the candidate list, with the same result.
+// top 12 bits (kept in the workspace).  A cluster of 8 CTAs shares each row, CTA r
+// owning the r-th eighth of its positions:
+//   1. every CTA finds, from that histogram, the bin holding the K-th largest key;
+//   2. each CTA gathers the keys of that bin (the candidates) from its eighth;
+//   3. the candidates are pooled through distributed shared memory and every CTA finds
+//      the same exact K-th largest key T among them with an MSB-first radix select over
+//      the remaining 20 bits (8 + 8 + 4), and how many keys equal to T to take;
+//   4. each CTA counts its keys > T and == T, learns the counts of the CTAs before it,
+//      and writes, in position order, every key > T and the first (K - #{> T}) keys
+//      == T (warps own contiguous ranges; block scans place them).
+// Keys are read from the score row (in L2) in blocks of 4096 positions held in
+// registers, all loads of a block in flight together.  If the candidates overflow the
+// pool (a row with very many equal top bits), step 3 rescans the whole row instead,
+// with the same result.
+#include <cooperative_groups.h>
+
 #include "common.cuh"
+
+namespace cg = cooperative_groups;
 
 namespace dsa {
 
 namespace {
 
-constexpr int kTopkThreads = 1024;
-constexpr int kCandCap = 24576;  // candidate keys kept in shared memory
-constexpr int kChunks = 32;                          // 32-position chunks per warp per block
-constexpr int kBlock = kTopkThreads * kChunks;       // positions whose keys sit in registers
+constexpr int kCluster = 8;                      // CTAs per row
+constexpr int kThreads = 256;
+constexpr int kWarpsPerCta = kThreads / 32;
+constexpr int kChunks = 16;                      // 32-position chunks per warp per block
+constexpr int kBlock = kThreads * kChunks;       // positions whose keys sit in registers
+constexpr int kLocalCap = 2048;                  // candidates one CTA may contribute
+constexpr int kCandCap = 8192;                   // candidates pooled over the cluster
 
 // Exclusive prefix sum of v over the CTA in thread order, and the CTA total.
 __device__ __forceinline__ int block_excl_sum(int v, int* buf, int* total) {
@@ -43,26 +51,51 @@ __device__ __forceinline__ int block_excl_sum(int v, int* buf, int* total) {
   }
   if (lane == 31) buf[warp] = incl;
   __syncthreads();
-  if (warp == 0) {
-    const int c = buf[lane];  // 32 warps
-    int s = c;
+  int before = 0, tot = 0;
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int u = __shfl_up_sync(0xffffffffu, s, o);
-      if (lane >= o) s += u;
-    }
-    buf[lane] = s - c;            // exclusive prefix of the warp totals
-    if (lane == 31) buf[32] = s;  // CTA total
+  for (int w = 0; w < kWarpsPerCta; ++w) {
+    const int c = buf[w];
+    before += (w < warp) ? c : 0;
+    tot += c;
   }
-  __syncthreads();
-  const int before = buf[warp];
-  *total = buf[32];
   __syncthreads();  // buf is reused by the next call
+  *total = tot;
   return before + incl - v;
 }
 
-__global__ void __launch_bounds__(kTopkThreads) topk_row_kernel(TopkParams p) {
-  const int row = blockIdx.x;
+// Finds, over a 256-bin histogram (high to low), the bin holding the `remaining`-th
+// largest entry; warp 0 writes the bin and the count above it.
+__device__ __forceinline__ void find_bin256(const uint32_t* hist, uint32_t remaining, uint32_t* s_digit,
+                                            uint32_t* s_above) {
+  const int lane = threadIdx.x & 31;
+  uint32_t loc = 0;
+#pragma unroll
+  for (int u = 0; u < 8; ++u) loc += hist[255 - 8 * lane - u];
+  uint32_t incl = loc;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  const uint32_t ex = incl - loc;
+  if (ex < remaining && remaining <= incl) {
+    uint32_t cum = ex;
+    for (int u = 0; u < 8; ++u) {
+      const int bin = 255 - 8 * lane - u;
+      if (cum + hist[bin] >= remaining) {
+        *s_digit = (uint32_t)bin;
+        *s_above = cum;
+        break;
+      }
+      cum += hist[bin];
+    }
+  }
+}
+
+__global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads) topk_cluster_kernel(TopkParams p) {
+  cg::cluster_group cluster = cg::this_cluster();
+  const int rank = (int)cluster.block_rank();
+  const int row = blockIdx.y;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int K = p.top_k;
 
@@ -72,32 +105,35 @@ __global__ void __launch_bounds__(kTopkThreads) topk_row_kernel(TopkParams p) {
   float* outs = p.out_score ? p.out_score + (int64_t)row * K : nullptr;
   const float* srow = p.scores + (int64_t)row * p.score_stride;
 
-  if (n <= K) {  // every visible position is selected
-    for (int i = tid; i < K; i += kTopkThreads) {
+  if (n <= K) {  // every visible position is selected (uniform over the cluster)
+    for (int i = rank * kThreads + tid; i < K; i += kCluster * kThreads) {
       out[i] = i < n ? i : -1;
       if (outs) outs[i] = i < n ? srow[i] : __uint_as_float(0x7FC00000u);
     }
     return;
   }
 
-  extern __shared__ uint32_t cand[];  // [kCandCap] keys of the boundary bin
-  __shared__ int buf[33];
+  __shared__ uint32_t cand_local[kLocalCap];
+  __shared__ uint32_t cand[kCandCap];
   __shared__ uint32_t hist[256];
+  __shared__ int buf[kWarpsPerCta];
+  __shared__ int s_nlocal;
+  __shared__ int cnt[2];  // this CTA's #{key > T}, #{key == T}
   __shared__ uint32_t s_digit, s_above;
-  __shared__ int s_ncand;
+  __shared__ int s_taken_before, s_eq_before;
 
-  // ---- 1. bin of the K-th largest key among the 4096 top-12-bit bins ----------------
-  // thread t owns bins 4095-4t .. 4092-4t (high to low)
+  // ---- 1. bin of the K-th largest key among the 4096 top-12-bit bins (all CTAs alike)
+  // thread t owns bins 4095-16t .. 4080-16t (high to low)
   const uint32_t* h12 = p.hist + (int64_t)row * kTopkBins;
-  uint32_t hb[4];
+  uint32_t hb[16];
   uint32_t local = 0;
 #pragma unroll
-  for (int u = 0; u < 4; ++u) {
-    hb[u] = __ldg(h12 + kTopkBins - 1 - 4 * tid - u);
+  for (int u = 0; u < 16; ++u) {
+    hb[u] = __ldg(h12 + kTopkBins - 1 - 16 * tid - u);
     local += hb[u];
   }
   if (tid == 0) {
-    s_ncand = 0;
+    s_nlocal = 0;
     s_digit = 0;
     s_above = 0;
   }
@@ -106,9 +142,9 @@ __global__ void __launch_bounds__(kTopkThreads) topk_row_kernel(TopkParams p) {
   uint32_t remaining = (uint32_t)K;
   if (excl < remaining && remaining <= excl + local) {
     uint32_t cum = excl;
-    for (int u = 0; u < 4; ++u) {
+    for (int u = 0; u < 16; ++u) {
       if (cum + hb[u] >= remaining) {
-        s_digit = (uint32_t)(kTopkBins - 1 - 4 * tid - u);
+        s_digit = (uint32_t)(kTopkBins - 1 - 16 * tid - u);
         s_above = cum;
         break;
       }
@@ -119,55 +155,72 @@ __global__ void __launch_bounds__(kTopkThreads) topk_row_kernel(TopkParams p) {
   uint32_t prefix = s_digit << 20, mask = 0xFFF00000u;
   remaining -= s_above;
 
-  // Positions are visited in blocks of kBlock; within a block warp w owns the kChunks
-  // consecutive 32-position chunks starting at w * kChunks * 32, lane l the l-th of each.
-  // A block's keys are loaded into registers with all loads in flight at once.
-  const int nblocks = (n + kBlock - 1) / kBlock;
+  // This CTA's positions [lo, hi), visited in blocks of kBlock whose keys sit in
+  // registers: warp w owns kChunks consecutive 32-position chunks of each block.
+  const int chunk = ((n + kCluster - 1) / kCluster + 31) / 32 * 32;
+  const int lo = min(n, rank * chunk), hi = min(n, lo + chunk);
+  const int nblocks = (hi - lo + kBlock - 1) / kBlock;
   uint32_t kr[kChunks];
   auto load_block = [&](int blk) {
-    const int base = blk * kBlock + warp * (kChunks * 32) + lane;
+    const int base = lo + blk * kBlock + warp * (kChunks * 32) + lane;
 #pragma unroll
     for (int c = 0; c < kChunks; ++c) {
       const int i = base + c * 32;
-      kr[c] = i < n ? score_key(__ldg(srow + i)) : 0u;
+      kr[c] = i < hi ? score_key(__ldg(srow + i)) : 0u;
     }
   };
   int loaded = -1;
 
-  // ---- 2. gather the keys of that bin ---------------------------------------------
+  // ---- 2. this CTA's keys of the boundary bin ------------------------------------
   for (int blk = 0; blk < nblocks; ++blk) {
     load_block(blk);
     loaded = blk;
-    const int base = blk * kBlock + warp * (kChunks * 32) + lane;
+    const int base = lo + blk * kBlock + warp * (kChunks * 32) + lane;
 #pragma unroll
     for (int c = 0; c < kChunks; ++c) {
-      const bool in = base + c * 32 < n && (kr[c] & mask) == prefix;
+      const bool in = base + c * 32 < hi && (kr[c] & mask) == prefix;
       const unsigned bal = __ballot_sync(0xffffffffu, in);
       if (bal) {
         int slot = 0;
-        if (lane == 0) slot = atomicAdd(&s_ncand, __popc(bal));
+        if (lane == 0) slot = atomicAdd(&s_nlocal, __popc(bal));
         slot = __shfl_sync(0xffffffffu, slot, 0) + __popc(bal & ((1u << lane) - 1u));
-        if (in && slot < kCandCap) cand[slot] = kr[c];
+        if (in && slot < kLocalCap) cand_local[slot] = kr[c];
       }
     }
   }
-  __syncthreads();
-  const int ncand = s_ncand;
-  const bool use_cand = ncand <= kCandCap;
+  cluster.sync();
 
-  // ---- 3. exact K-th largest key: radix select over the low 20 bits ---------------
+  // ---- 3. pool the candidates; every CTA selects the same exact K-th largest key ----
+  int ncand = 0;
+  bool pooled = true;
+  for (int r = 0; r < kCluster; ++r) {
+    const int nr = *cluster.map_shared_rank(&s_nlocal, r);
+    if (nr > kLocalCap) pooled = false;
+    ncand += nr;
+  }
+  if (ncand > kCandCap) pooled = false;
+  if (pooled) {
+    int off = 0;
+    for (int r = 0; r < kCluster; ++r) {
+      const int nr = *cluster.map_shared_rank(&s_nlocal, r);
+      const uint32_t* src = cluster.map_shared_rank(cand_local, r);
+      for (int i = tid; i < nr; i += kThreads) cand[off + i] = src[i];
+      off += nr;
+    }
+  }
+  __syncthreads();
 #pragma unroll 1
   for (int pass = 0; pass < 3; ++pass) {
     const int shift = pass == 0 ? 12 : (pass == 1 ? 4 : 0);
     const uint32_t dmask = pass == 2 ? 0xFu : 0xFFu;
-    if (tid < 256) hist[tid] = 0;
+    hist[tid] = 0;
     __syncthreads();
-    const int cnt = use_cand ? ncand : n;
-    for (int base = 0; base < cnt; base += kTopkThreads) {
+    const int cnt_all = pooled ? ncand : n;  // without the pool, rescan the whole row
+    for (int base = 0; base < cnt_all; base += kThreads) {
       const int i = base + tid;
       uint32_t k = 0;
-      if (i < cnt) k = use_cand ? cand[i] : score_key(srow[i]);
-      const bool in = i < cnt && (k & mask) == prefix;
+      if (i < cnt_all) k = pooled ? cand[i] : score_key(__ldg(srow + i));
+      const bool in = i < cnt_all && (k & mask) == prefix;
       const uint32_t dgt = (k >> shift) & dmask;
       const unsigned act = __ballot_sync(0xffffffffu, in);
       if (in) {
@@ -176,31 +229,7 @@ __global__ void __launch_bounds__(kTopkThreads) topk_row_kernel(TopkParams p) {
       }
     }
     __syncthreads();
-    if (warp == 0) {
-      // lane l owns bins 255-8l .. 248-8l (high to low)
-      uint32_t loc = 0;
-#pragma unroll
-      for (int u = 0; u < 8; ++u) loc += hist[255 - 8 * lane - u];
-      uint32_t incl = loc;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t v = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += v;
-      }
-      const uint32_t ex = incl - loc;
-      if (ex < remaining && remaining <= incl) {
-        uint32_t cum = ex;
-        for (int u = 0; u < 8; ++u) {
-          const int bin = 255 - 8 * lane - u;
-          if (cum + hist[bin] >= remaining) {
-            s_digit = (uint32_t)bin;
-            s_above = cum;
-            break;
-          }
-          cum += hist[bin];
-        }
-      }
-    }
+    if (warp == 0) find_bin256(hist, remaining, &s_digit, &s_above);
     __syncthreads();
     prefix |= s_digit << shift;
     mask |= dmask << shift;
@@ -208,32 +237,67 @@ __global__ void __launch_bounds__(kTopkThreads) topk_row_kernel(TopkParams p) {
   }
   const uint32_t T = prefix;  // the K-th largest key; take `remaining` of the keys == T
 
-  // ---- 4. ordered output, block by block ---------------------------------------------
-  const unsigned lt = (1u << lane) - 1u;
-  int taken = 0, ties = 0;  // row-wide, before the current block
+  // ---- 4. ordered output: count, place this CTA among the cluster, write -----------
+  int gt_c = 0, eq_c = 0;  // this CTA's totals
   for (int blk = 0; blk < nblocks; ++blk) {
     if (loaded != blk) {
       load_block(blk);
       loaded = blk;
     }
-    const int base = blk * kBlock + warp * (kChunks * 32) + lane;
+    const int base = lo + blk * kBlock + warp * (kChunks * 32) + lane;
+#pragma unroll
+    for (int c = 0; c < kChunks; ++c) {
+      const bool ok = base + c * 32 < hi;
+      gt_c += (ok && kr[c] > T);
+      eq_c += (ok && kr[c] == T);
+    }
+  }
+  for (int o = 16; o; o >>= 1) {
+    gt_c += __shfl_xor_sync(0xffffffffu, gt_c, o);
+    eq_c += __shfl_xor_sync(0xffffffffu, eq_c, o);
+  }
+  if (tid == 0) cnt[0] = cnt[1] = 0;
+  __syncthreads();
+  if (lane == 0) {
+    atomicAdd(&cnt[0], gt_c);
+    atomicAdd(&cnt[1], eq_c);
+  }
+  cluster.sync();
+  if (tid == 0) {
+    int taken = 0, eq_before = 0;
+    for (int r = 0; r < rank; ++r) {
+      const int* c = cluster.map_shared_rank(cnt, r);
+      taken += c[0] + max(0, min((int)remaining - eq_before, c[1]));
+      eq_before += c[1];
+    }
+    s_taken_before = taken;
+    s_eq_before = eq_before;
+  }
+  cluster.sync();  // no CTA leaves while another may still read its shared memory
+  const unsigned lt = (1u << lane) - 1u;
+  int taken = s_taken_before, ties = s_eq_before;  // before the current block
+  for (int blk = 0; blk < nblocks; ++blk) {
+    if (loaded != blk) {
+      load_block(blk);
+      loaded = blk;
+    }
+    const int base = lo + blk * kBlock + warp * (kChunks * 32) + lane;
     int gt_w = 0, eq_w = 0;
 #pragma unroll
     for (int c = 0; c < kChunks; ++c) {
-      const bool ok = base + c * 32 < n;
+      const bool ok = base + c * 32 < hi;
       gt_w += __popc(__ballot_sync(0xffffffffu, ok && kr[c] > T));
       eq_w += __popc(__ballot_sync(0xffffffffu, ok && kr[c] == T));
     }
-    int eq_tot;
+    int eq_tot, tk_tot;
     // every lane of a warp holds the warp's counts; lane 0 alone enters them in the scans
     const int eq_before = ties + __shfl_sync(0xffffffffu, block_excl_sum(lane == 0 ? eq_w : 0, buf, &eq_tot), 0);
     const int take_w = gt_w + max(0, min((int)remaining - eq_before, eq_w));
-    int tk_tot;
     int pos = taken + __shfl_sync(0xffffffffu, block_excl_sum(lane == 0 ? take_w : 0, buf, &tk_tot), 0);
     int tie = eq_before;
 #pragma unroll
     for (int c = 0; c < kChunks; ++c) {
-      const bool ok = base + c * 32 < n;
+      const bool ok = base + c * 32 < hi;
       const bool gt = ok && kr[c] > T;
       const bool eq = ok && kr[c] == T;
       const unsigned eqb = __ballot_sync(0xffffffffu, eq);
@@ -256,10 +320,8 @@ __global__ void __launch_bounds__(kTopkThreads) topk_row_kernel(TopkParams p) {
 
 cudaError_t launch_topk(const TopkParams& p, int32_t max_visible, cudaStream_t s) {
   (void)max_visible;
-  const size_t smem = (size_t)kCandCap * sizeof(uint32_t);
-  cudaError_t e = cudaFuncSetAttribute(topk_row_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
-  topk_row_kernel<<<p.tv.n_tokens, kTopkThreads, smem, s>>>(p);
+  dim3 grid(kCluster, p.tv.n_tokens);
+  topk_cluster_kernel<<<grid, kThreads, 0, s>>>(p);
   return cudaGetLastError();
 }
 
