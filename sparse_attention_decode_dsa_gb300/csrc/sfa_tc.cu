@@ -14,22 +14,26 @@
 //     Each CTA gathers its 512 latent bytes and the 128 rope bytes of every selected
 //     row (the pair reads each 1152-byte row once from DRAM).
 //   * Each CTA computes partial logits S_c = Q[:, own] . KV[:, own]^T (tcgen05, A = Q
-//     from tensor memory, B = gathered rows in shared memory), sends them to its peer
-//     through distributed shared memory (each warp stages its 32 rows and moves them
-//     with one bulk copy, counted in bytes on the peer's mbarrier) and adds the peer's
-//     part: both CTAs hold the same S = S_0 + S_1.
+//     from tensor memory, B = gathered rows in shared memory), multiplies them by
+//     softmax_scale * log2(e), rounds them to fp16 (relative 2^-11, below the bf16
+//     rounding P gets anyway), sends them to its peer through distributed shared
+//     memory (each warp stages its 32 rows and moves them with one bulk copy, counted
+//     in bytes on the peer's mbarrier) and adds the peer's part: both CTAs hold the
+//     same S = S_0 + S_1 of the same rounded halves.
 //   * Online softmax per head row (thread = row, no shuffles), base 2; the reference
 //     maximum only moves when a tile's maximum exceeds it by 8 (2^8 headroom), and O is
 //     then rescaled in tensor memory.
 //   * P (bf16) goes to tensor memory; O[128 x 256] += P . V with V read MN-major from
 //     the same shared-memory rows the logits used.
-// Warp roles: warps 0-2 (one thread each) gather rows with TMA gather4 into a 3-stage
+// Warp roles: warps 0-2 (one thread each) gather rows with TMA gather4 into a 4-stage
 // ring of 128-byte swizzle atoms; warp 3 (one thread) issues each MMA as soon as its
 // inputs are ready; warps 4-7 run softmax and the epilogue, skewed by one tile: they load
 // and send the partial logits of tile n + 1 before finishing tile n, so the exchange
 // overlaps the softmax.  Tensor memory (512 columns): O [0,256), S [256,320), P [320,352),
 // Q rope [352,368), Q latent [384,512).  Every wait is bounded.  Shared memory per stage:
 // 4 latent regions + 1 rope region, each 64 rows x 128 B.
+#include <cuda_fp16.h>
+
 #include "sm100.cuh"
 
 namespace dsa {
@@ -42,10 +46,10 @@ constexpr int kGatherWarps = 3;                  // warps 0-2 gather (TMA), warp
 constexpr int kMmaWarp = kGatherWarps;           // warps 4-7 run softmax and the epilogue
 constexpr int kThreads = (kGatherWarps + 5) * 32;
 constexpr int kTok = 64;                         // selected positions per tile
-constexpr int kStages = 3;
+constexpr int kStages = 4;
 constexpr int kRegion = kTok * 128;              // 64 rows x 128 B
 constexpr int kStageBytes = 5 * kRegion;         // 4 latent regions + 1 rope region
-constexpr int kXchBytes = 128 * kTok * 4;        // one f32 partial-logit tile
+constexpr int kXchBytes = 128 * kTok * 2;        // one fp16 partial-logit tile (128 rows x 128 B)
 constexpr int kMaxSplitLen = kMaxTopK;
 constexpr uint32_t kColO = 0, kColS = 256, kColP = 320, kColQr = 352, kColQl = 384;
 constexpr int kSmem = 1024 + kStages * kStageBytes + 3 * kXchBytes + kMaxSplitLen * 4 + 512;
@@ -62,8 +66,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const uint32_t raw_u32 = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + ((1024 - (raw_u32 & 1023)) & 1023);
   uint8_t* stages = smem;
-  float* xch = (float*)(stages + kStages * kStageBytes);      // [2][128 rows][64] peer partials
-  float* stg = (float*)((uint8_t*)xch + 2 * kXchBytes);       // [128 rows][64] own partial, outbound
+  uint8_t* xch = stages + kStages * kStageBytes;              // [2][128 rows][64 fp16] peer partials
+  uint8_t* stg = xch + 2 * kXchBytes;                         // [128 rows][64 fp16] own partial, outbound
   int32_t* rowid = (int32_t*)((uint8_t*)stg + kXchBytes);     // cache row of each slot or -1
   uint64_t* bars = (uint64_t*)(rowid + kMaxSplitLen);
   uint64_t* kv_full = bars;
@@ -288,20 +292,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(q_ready);
     }
-    const uint32_t warp_rows = (uint32_t)(quarter * 32) * (kTok * 4);  // this warp's 8 KB slice
+    const uint32_t warp_rows = (uint32_t)(quarter * 32) * (kTok * 2);  // this warp's 4 KB slice
     const uint32_t xch_peer0 = map_to_rank(smem_u32(xch) + warp_rows, peer);
     const uint32_t stg_local = smem_u32(stg) + warp_rows;
     const uint32_t xfull_peer0 = map_to_rank(smem_u32(&xch_full[0]), peer);
     const uint32_t xempty_peer0 = map_to_rank(smem_u32(&xch_empty[0]), peer);
-    const uint32_t myrow = (uint32_t)h * (kTok * 4);
+    const uint32_t myrow = (uint32_t)h * (kTok * 2);
     const uint32_t sw = (uint32_t)(h & 7);
     float m_ref = -INFINITY, l = 0.f;
     bool ok = true;
 
-    // Loads this CTA's partial logits of tile t into `dst`, frees the logit columns for
-    // the next QK, and sends them (staging + one bulk copy per warp) to the peer's
-    // buffer t & 1 once the peer has read tile t - 2 from it.  Returns false on abort.
-    auto load_and_send = [&](int t, float (&dst)[kTok]) -> bool {
+    // Loads this CTA's partial logits of tile t, scales them by softmax_scale * log2(e)
+    // and rounds them to fp16 into `dst` (kept: both CTAs sum the same rounded halves,
+    // so their softmax is identical), frees the logit columns for the next QK, and
+    // sends them (staging + one bulk copy per warp) to the peer's buffer t & 1 once the
+    // peer has read tile t - 2 from it.  Returns false on abort.
+    auto load_and_send = [&](int t, uint32_t (&dst)[kTok / 2]) -> bool {
       bool good = true;
       if (lane == 0) good = mbar_wait(s_full, t & 1, abort_flag, p.err);
       if (!__shfl_sync(0xffffffffu, good, 0)) return false;
@@ -313,9 +319,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         tmem_ld32(tmem + lane_off + kColS + 32, v1);
         tmem_ld_wait();
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          dst[j] = __uint_as_float(v0[j]);
-          dst[32 + j] = __uint_as_float(v1[j]);
+        for (int j = 0; j < 16; ++j) {
+          const __half2 a = __floats2half2_rn(__uint_as_float(v0[2 * j]) * p.scale_log2,
+                                              __uint_as_float(v0[2 * j + 1]) * p.scale_log2);
+          const __half2 b = __floats2half2_rn(__uint_as_float(v1[2 * j]) * p.scale_log2,
+                                              __uint_as_float(v1[2 * j + 1]) * p.scale_log2);
+          dst[j] = *(const uint32_t*)&a;
+          dst[16 + j] = *(const uint32_t*)&b;
         }
       }
       tc_fence_before();
@@ -326,27 +336,27 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
       __syncwarp();
 #pragma unroll
-      for (int u = 0; u < kTok / 4; ++u)
-        *(float4*)((uint8_t*)stg + myrow + (((uint32_t)u ^ sw) << 4)) =
-            make_float4(dst[4 * u], dst[4 * u + 1], dst[4 * u + 2], dst[4 * u + 3]);
+      for (int u = 0; u < kTok / 8; ++u)
+        *(uint4*)(stg + myrow + (((uint32_t)u ^ sw) << 4)) =
+            make_uint4(dst[4 * u], dst[4 * u + 1], dst[4 * u + 2], dst[4 * u + 3]);
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) {
         const int bb = t & 1;
         if (t >= 2) good = mbar_wait_cluster(&xch_empty[bb], ((t >> 1) & 1) ^ 1, abort_flag, p.err);
         if (good) {
-          bulk_copy_to_peer(xch_peer0 + bb * kXchBytes, stg_local, 32 * kTok * 4, xfull_peer0 + bb * 8);
+          bulk_copy_to_peer(xch_peer0 + bb * kXchBytes, stg_local, 32 * kTok * 2, xfull_peer0 + bb * 8);
           bulk_commit();
         }
       }
       return __shfl_sync(0xffffffffu, good, 0);
     };
 
-    float sc[kTok];  // own partial logits of the tile being finished
+    uint32_t sc[kTok / 2];  // own partial logits of the tile being finished (fp16 pairs)
     if (n_tiles_run > 0) ok = load_and_send(0, sc);
     for (int n = 0; ok && n < n_tiles_run; ++n) {
       // ---- start tile n + 1: its exchange overlaps the rest of tile n --------------
-      float sn[kTok];
+      uint32_t sn[kTok / 2];
       if (n + 1 < n_tiles_run && !(ok = load_and_send(n + 1, sn))) break;
       // ---- finish tile n -----------------------------------------------------------
       const int bb = n & 1;
@@ -359,26 +369,37 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
       if (!__shfl_sync(0xffffffffu, ok, 0)) { ok = false; break; }
       __syncwarp();
-      const uint8_t* recv = (const uint8_t*)xch + bb * kXchBytes + myrow;
-      float* s = sc;  // full logits of tile n, summed in place
+      const uint8_t* recv = xch + bb * kXchBytes + myrow;
+      float s[kTok];  // full scaled logits of tile n
 #pragma unroll
-      for (int u = 0; u < kTok / 4; ++u) {
-        const float4 r = *(const float4*)(recv + (((uint32_t)u ^ sw) << 4));
-        s[4 * u] += r.x;
-        s[4 * u + 1] += r.y;
-        s[4 * u + 2] += r.z;
-        s[4 * u + 3] += r.w;
+      for (int u = 0; u < kTok / 8; ++u) {
+        const uint4 r = *(const uint4*)(recv + (((uint32_t)u ^ sw) << 4));
+        const uint32_t rr[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float2 mine = __half22float2(*(const __half2*)&sc[4 * u + i]);
+          const float2 theirs = __half22float2(*(const __half2*)&rr[i]);
+          s[8 * u + 2 * i] = mine.x + theirs.x;
+          s[8 * u + 2 * i + 1] = mine.y + theirs.y;
+        }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive_remote_relaxed(xempty_peer0 + bb * 8);  // its loads fed the adds above
       // online softmax (base 2), masked positions get no weight
-      float tmax = -INFINITY;
+      if ((vlo & vhi) != 0xffffffffu) {
 #pragma unroll
-      for (int j = 0; j < kTok; ++j) {
-        const bool v = ((j < 32 ? vlo : vhi) >> (j & 31)) & 1u;
-        s[j] = v ? s[j] * p.scale_log2 : -INFINITY;
-        tmax = fmaxf(tmax, s[j]);
+        for (int j = 0; j < kTok; ++j) {
+          const bool v = ((j < 32 ? vlo : vhi) >> (j & 31)) & 1u;
+          s[j] = v ? s[j] : -INFINITY;
+        }
       }
+      float mx[8];  // independent partial maxima
+#pragma unroll
+      for (int i = 0; i < 8; ++i) mx[i] = s[i];
+#pragma unroll
+      for (int j = 8; j < kTok; ++j) mx[j & 7] = fmaxf(mx[j & 7], s[j]);
+      const float tmax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                               fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
       float alpha = 1.f;
       bool rescale = false;
       if (tmax != -INFINITY && (m_ref == -INFINITY || tmax > m_ref + 8.f)) {
@@ -388,13 +409,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         m_ref = tmax;
       }
-      float rs = 0.f;
       const float msub = m_ref == -INFINITY ? 0.f : m_ref;  // nothing visible yet: all weights 0
+      float ps[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};  // independent partial sums
 #pragma unroll
       for (int j = 0; j < kTok; ++j) {
         s[j] = fast_exp2(s[j] - msub);  // 2^-inf = 0 for masked positions
-        rs += s[j];
+        ps[j & 7] += s[j];
       }
+      const float rs = ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
       l = l * alpha + rs;
       if (n > 0) {  // P.V of tile n - 1 has consumed P and updated O
         if (lane == 0) ok = mbar_wait(pv_done, (n - 1) & 1, abort_flag, p.err);
@@ -416,7 +438,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       {
         uint32_t pw[32];
 #pragma unroll
-        for (int j = 0; j < 32; ++j) pw[j] = pack_bf16x2(s[2 * j], s[2 * j + 1]);
+        for (int j = 0; j < 32; ++j) pw[j] = cvt_bf16x2(s[2 * j], s[2 * j + 1]);
         tmem_st32(tmem + lane_off + kColP, pw);
       }
       tmem_st_wait();
@@ -424,7 +446,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(p_full);
 #pragma unroll
-      for (int j = 0; j < kTok; ++j) sc[j] = sn[j];  // own logits of tile n + 1
+      for (int j = 0; j < kTok / 2; ++j) sc[j] = sn[j];  // own logits of tile n + 1
     }
     // ---- epilogue: O / l -> this CTA's 256 value dims ----------------------------------
     if (ok && n_tiles_run > 0) {

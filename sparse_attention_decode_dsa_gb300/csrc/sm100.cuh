@@ -214,6 +214,13 @@ __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.comm
 // Waits until every committed bulk copy of this thread has finished reading its source.
 __device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;\n" ::: "memory"); }
 
+// Two floats -> packed bf16 pair (round to nearest even), lower half = `lo`.
+__device__ __forceinline__ uint32_t cvt_bf16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;\n" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
 // 2^x with the hardware approximation (ftz): used for softmax weights.
 __device__ __forceinline__ float fast_exp2(float x) {
   float y;
