@@ -81,7 +81,7 @@ def algorithmic(wl):
         "indexer_score": {"bytes": key_tokens * k_row + q_bytes + meta, "flops": score_flops},
         "indexer_topk": {"bytes": idx_bytes, "flops": 0.0},
         "sfa": {"bytes": sfa_bytes, "flops": sfa_flops},
-        "sfa_combine": {"bytes": T * s.sfa_heads * 512 * 2, "flops": 0.0},
+        "hist_clear": {"bytes": T * 4096 * 4, "flops": 0.0},
         "step": {"bytes": key_tokens * k_row + q_bytes + meta + sfa_bytes, "flops": score_flops + sfa_flops},
     }
 
@@ -139,8 +139,7 @@ class ClockSampler:
 # Traffic measured by ncu (profiles/traffic.json), used only while the kernel source is
 # unchanged since the capture.
 # ---------------------------------------------------------------------------------------
-KERNEL_SOURCES = {"indexer_score": "indexer_score.cu", "indexer_topk": "topk.cu", "sfa": "sfa.cu",
-                  "sfa_combine": "sfa.cu"}
+KERNEL_SOURCES = {"indexer_score": "indexer_tc.cu", "indexer_topk": "topk.cu", "sfa": "sfa_tc.cu"}
 
 
 def _src_sha(kernel):

@@ -127,11 +127,14 @@ dsa_status_t check_sfa(const dsa_sfa_args_t* a, const dsa_latent_cache_t* c) {
 }
 
 // ---- workspace plans ------------------------------------------------------------------
+// Workspace: [0, 256) the device error word; for split attention, the split counters;
+// then one region the passes use in turn (the indexer's key histograms and score rows,
+// later the attention's split partials).
 struct IndexerPlan {
   int32_t max_visible;
   int64_t score_stride;
-  size_t score_bytes;  // f32 score rows, then the per-row key histograms (all after the error word)
-  size_t hist_offset, hist_bytes;
+  size_t score_bytes;  // the per-row key histograms, then the f32 score rows
+  size_t hist_bytes;
 };
 
 IndexerPlan plan_indexer(int32_t max_visible, int32_t n_tokens) {
@@ -140,15 +143,16 @@ IndexerPlan plan_indexer(int32_t max_visible, int32_t n_tokens) {
   p.score_stride = ((int64_t)max_visible + 63) / 64 * 64;
   if (p.score_stride == 0) p.score_stride = 64;
   const size_t rows = align_up((size_t)n_tokens * p.score_stride * sizeof(float));
-  p.hist_offset = rows;
   p.hist_bytes = align_up((size_t)n_tokens * kTopkBins * sizeof(uint32_t));
-  p.score_bytes = rows + p.hist_bytes;
+  p.score_bytes = p.hist_bytes + rows;
   return p;
 }
 
 struct SfaPlan {
   int32_t n_splits, split_len;
-  size_t part_o_bytes, part_lse_bytes;
+  size_t cnt_bytes;                    // split counters, right after the error word
+  size_t part_o_bytes, part_lse_bytes;  // in the shared region
+  size_t region_bytes() const { return part_o_bytes + part_lse_bytes; }
 };
 
 SfaPlan plan_sfa(int32_t n_tokens, int32_t n_heads, int32_t top_k) {
@@ -164,10 +168,11 @@ SfaPlan plan_sfa(int32_t n_tokens, int32_t n_heads, int32_t top_k) {
   p.split_len = (tiles + s - 1) / s * 64;
   p.n_splits = (tiles * 64 + p.split_len - 1) / p.split_len;  // drop empty splits
   if (p.n_splits > 1) {
+    p.cnt_bytes = align_up((size_t)n_tokens * 2 * sizeof(uint32_t));
     p.part_o_bytes = align_up((size_t)n_tokens * p.n_splits * n_heads * kValueDim * sizeof(float));
-    p.part_lse_bytes = align_up((size_t)n_tokens * p.n_splits * n_heads * sizeof(float));
+    p.part_lse_bytes = align_up((size_t)n_tokens * p.n_splits * 2 * n_heads * sizeof(float));
   } else {
-    p.part_o_bytes = p.part_lse_bytes = 0;
+    p.cnt_bytes = p.part_o_bytes = p.part_lse_bytes = 0;
   }
   return p;
 }
@@ -205,12 +210,15 @@ struct Tracer {
 };
 
 // ---- the three passes -----------------------------------------------------------------
+// `region`: the pass region (histograms first); `clear` / `clear_bytes`: what to zero
+// before the score kernel (the histograms, plus the split counters that precede them
+// when the attention pass follows).
 dsa_status_t run_indexer(const dsa_indexer_args_t* a, const dsa_index_cache_t* c,
                          const dsa_page_table_t* pg, const dsa_tokens_t* tk, const IndexerPlan& ip,
-                         int32_t* out_idx, float* out_score, uint8_t* ws, cudaStream_t s, Tracer& tr) {
-  uint32_t* err = (uint32_t*)ws;
-  float* scores = (float*)(ws + kAlign);
-  uint32_t* hist = (uint32_t*)(ws + kAlign + ip.hist_offset);
+                         int32_t* out_idx, float* out_score, uint32_t* err, uint8_t* region, void* clear,
+                         size_t clear_bytes, cudaStream_t s, Tracer& tr) {
+  uint32_t* hist = (uint32_t*)region;
+  float* scores = (float*)(region + ip.hist_bytes);
   ScoreParams sp;
   sp.tv = token_view(pg, tk, ip.max_visible);
   sp.q = a->q;
@@ -227,7 +235,7 @@ dsa_status_t run_indexer(const dsa_indexer_args_t* a, const dsa_index_cache_t* c
   sp.act = (int)a->act;
   sp.max_page_blocks = (ip.max_visible + kPage - 1) / kPage;
   tr.begin();
-  cudaError_t me = cudaMemsetAsync(hist, 0, ip.hist_bytes, s);
+  cudaError_t me = cudaMemsetAsync(clear, 0, clear_bytes, s);
   tr.end("hist_clear");
   if (me != cudaSuccess) return cuda_fail(me, "clearing the key histograms");
   if (sp.max_page_blocks > 0) {
@@ -253,33 +261,35 @@ dsa_status_t run_indexer(const dsa_indexer_args_t* a, const dsa_index_cache_t* c
   return DSA_OK;
 }
 
+// `cnt`: the split counters (zero on entry when `cnt_zeroed`, else cleared here);
+// `region`: the pass region for the split partials.
 dsa_status_t run_sfa(const dsa_sfa_args_t* a, const dsa_latent_cache_t* c, const dsa_page_table_t* pg,
                      const dsa_tokens_t* tk, int32_t max_visible, const int32_t* idx, int32_t top_k, void* out,
-                     uint8_t* ws, const SfaPlan& sp_, cudaStream_t s, Tracer& tr) {
+                     uint32_t* err, uint32_t* cnt, bool cnt_zeroed, uint8_t* region, const SfaPlan& sp_,
+                     cudaStream_t s, Tracer& tr) {
   SfaParams p;
   p.tv = token_view(pg, tk, max_visible);
   p.q = (const uint16_t*)a->q;
   p.kv = (const uint16_t*)c->data;
   p.idx = idx;
   p.out = (uint16_t*)out;
-  p.part_o = sp_.n_splits > 1 ? (float*)(ws + kAlign) : nullptr;
-  p.part_lse = sp_.n_splits > 1 ? (float*)(ws + kAlign + sp_.part_o_bytes) : nullptr;
-  p.err = (uint32_t*)ws;
+  p.part_o = sp_.n_splits > 1 ? (float*)region : nullptr;
+  p.part_lse = sp_.n_splits > 1 ? (float*)(region + sp_.part_o_bytes) : nullptr;
+  p.merge_cnt = sp_.n_splits > 1 ? cnt : nullptr;
+  p.err = err;
   p.n_heads = a->n_heads;
   p.top_k = top_k;
   p.n_splits = sp_.n_splits;
   p.split_len = sp_.split_len;
   p.scale_log2 = a->softmax_scale * 1.4426950408889634f;
+  if (p.n_splits > 1 && !cnt_zeroed) {
+    cudaError_t me = cudaMemsetAsync(cnt, 0, sp_.cnt_bytes, s);
+    if (me != cudaSuccess) return cuda_fail(me, "clearing the split counters");
+  }
   tr.begin();
   cudaError_t e = launch_sfa_tc(p, s);
   tr.end("sfa");
   if (e != cudaSuccess) return cuda_fail(e, "sparse attention launch");
-  if (p.n_splits > 1) {
-    tr.begin();
-    e = launch_sfa_combine(p, s);
-    tr.end("sfa_combine");
-    if (e != cudaSuccess) return cuda_fail(e, "split combine launch");
-  }
   return DSA_OK;
 }
 
@@ -309,7 +319,9 @@ dsa_status_t dsa_indexer_topk(const dsa_indexer_args_t* args, const dsa_index_ca
   IndexerPlan ip = plan_indexer(mv, tokens->n_tokens);
   if ((st = check_ws(ws, ws_bytes, kAlign + ip.score_bytes)) != DSA_OK) return st;
   Tracer tr(trace, (cudaStream_t)stream);
-  st = run_indexer(args, cache, pages, tokens, ip, out_idx, out_score, (uint8_t*)ws, (cudaStream_t)stream, tr);
+  uint8_t* region = (uint8_t*)ws + kAlign;
+  st = run_indexer(args, cache, pages, tokens, ip, out_idx, out_score, (uint32_t*)ws, region, region, ip.hist_bytes,
+                   (cudaStream_t)stream, tr);
   if (st == DSA_OK && tr.status != cudaSuccess) return cuda_fail(tr.status, "recording a trace event");
   return st;
 }
@@ -320,7 +332,7 @@ size_t dsa_sparse_attn_workspace_size(const dsa_sfa_args_t* args, const dsa_page
   if (check_sfa(args, nullptr) != DSA_OK || check_pages_tokens(pages, tokens, &mv) != DSA_OK) return 0;
   if (top_k < 1 || top_k > kMaxTopK) return 0;
   SfaPlan sp = plan_sfa(tokens->n_tokens, args->n_heads, top_k);
-  return kAlign + sp.part_o_bytes + sp.part_lse_bytes;
+  return kAlign + sp.cnt_bytes + sp.region_bytes();
 }
 
 dsa_status_t dsa_sparse_attn(const dsa_sfa_args_t* args, const dsa_latent_cache_t* cache,
@@ -335,9 +347,11 @@ dsa_status_t dsa_sparse_attn(const dsa_sfa_args_t* args, const dsa_latent_cache_
   if (!idx || !out) return fail(DSA_ERR_INVALID_ARG, "idx and out are required");
   if (top_k < 1 || top_k > kMaxTopK) return fail(DSA_ERR_UNSUPPORTED, "top_k must be in [1, %d]", kMaxTopK);
   SfaPlan sp = plan_sfa(tokens->n_tokens, args->n_heads, top_k);
-  if ((st = check_ws(ws, ws_bytes, kAlign + sp.part_o_bytes + sp.part_lse_bytes)) != DSA_OK) return st;
+  if ((st = check_ws(ws, ws_bytes, kAlign + sp.cnt_bytes + sp.region_bytes())) != DSA_OK) return st;
   Tracer tr(trace, (cudaStream_t)stream);
-  st = run_sfa(args, cache, pages, tokens, mv, idx, top_k, out, (uint8_t*)ws, sp, (cudaStream_t)stream, tr);
+  uint8_t* w8 = (uint8_t*)ws;
+  st = run_sfa(args, cache, pages, tokens, mv, idx, top_k, out, (uint32_t*)ws, (uint32_t*)(w8 + kAlign), false,
+               w8 + kAlign + sp.cnt_bytes, sp, (cudaStream_t)stream, tr);
   if (st == DSA_OK && tr.status != cudaSuccess) return cuda_fail(tr.status, "recording a trace event");
   return st;
 }
@@ -351,8 +365,8 @@ size_t dsa_fused_workspace_size(const dsa_indexer_args_t* iargs, const dsa_index
     return 0;
   IndexerPlan ip = plan_indexer(mv, tokens->n_tokens);
   SfaPlan sp = plan_sfa(tokens->n_tokens, sargs->n_heads, iargs->top_k);
-  const size_t sfa_b = sp.part_o_bytes + sp.part_lse_bytes;
-  return kAlign + (ip.score_bytes > sfa_b ? ip.score_bytes : sfa_b);  // the passes reuse one region
+  const size_t sfa_b = sp.region_bytes();
+  return kAlign + sp.cnt_bytes + (ip.score_bytes > sfa_b ? ip.score_bytes : sfa_b);  // the passes reuse one region
 }
 
 dsa_status_t dsa_fused_decode(const dsa_indexer_args_t* iargs, const dsa_index_cache_t* icache,
@@ -368,14 +382,19 @@ dsa_status_t dsa_fused_decode(const dsa_indexer_args_t* iargs, const dsa_index_c
   if (!out_idx || !out) return fail(DSA_ERR_INVALID_ARG, "out_idx and out are required");
   IndexerPlan ip = plan_indexer(mv, tokens->n_tokens);
   SfaPlan sp = plan_sfa(tokens->n_tokens, sargs->n_heads, iargs->top_k);
-  const size_t sfa_b = sp.part_o_bytes + sp.part_lse_bytes;
-  if ((st = check_ws(ws, ws_bytes, kAlign + (ip.score_bytes > sfa_b ? ip.score_bytes : sfa_b))) != DSA_OK)
+  const size_t sfa_b = sp.region_bytes();
+  if ((st = check_ws(ws, ws_bytes, kAlign + sp.cnt_bytes + (ip.score_bytes > sfa_b ? ip.score_bytes : sfa_b))) !=
+      DSA_OK)
     return st;
   Tracer tr(trace, (cudaStream_t)stream);
-  if ((st = run_indexer(iargs, icache, pages, tokens, ip, out_idx, nullptr, (uint8_t*)ws, (cudaStream_t)stream,
-                        tr)) != DSA_OK)
+  uint8_t* w8 = (uint8_t*)ws;
+  uint32_t* cnt = (uint32_t*)(w8 + kAlign);
+  uint8_t* region = w8 + kAlign + sp.cnt_bytes;
+  // one clear covers the split counters and the histograms that follow them
+  if ((st = run_indexer(iargs, icache, pages, tokens, ip, out_idx, nullptr, (uint32_t*)ws, region, cnt,
+                        sp.cnt_bytes + ip.hist_bytes, (cudaStream_t)stream, tr)) != DSA_OK)
     return st;
-  st = run_sfa(sargs, lcache, pages, tokens, mv, out_idx, iargs->top_k, out, (uint8_t*)ws, sp,
+  st = run_sfa(sargs, lcache, pages, tokens, mv, out_idx, iargs->top_k, out, (uint32_t*)ws, cnt, true, region, sp,
                (cudaStream_t)stream, tr);
   if (st == DSA_OK && tr.status != cudaSuccess) return cuda_fail(tr.status, "recording a trace event");
   return st;
@@ -464,5 +483,7 @@ extern "C" dsa_status_t dsa_indexer_topk_noalloc(const dsa_indexer_args_t* args,
   cudaError_t e = cudaMemsetAsync(ws, 0, sizeof(uint32_t), (cudaStream_t)stream);
   if (e != cudaSuccess) return cuda_fail(e, "clearing the fixed scratch's error word");
   Tracer tr(nullptr, (cudaStream_t)stream);
-  return run_indexer(args, cache, pages, tokens, ip, out_idx, out_score, (uint8_t*)ws, (cudaStream_t)stream, tr);
+  uint8_t* region = (uint8_t*)ws + kAlign;
+  return run_indexer(args, cache, pages, tokens, ip, out_idx, out_score, (uint32_t*)ws, region, region,
+                     ip.hist_bytes, (cudaStream_t)stream, tr);
 }

@@ -59,8 +59,9 @@ struct SfaParams {
   const uint16_t* kv;      // bf16 [num_pages, 64, 576]
   const int32_t* idx;      // [T, K]
   uint16_t* out;           // bf16 [T, H, 512]
-  float* part_o;           // [T, S, H, 512] (null when S == 1)
-  float* part_lse;         // [T, S, H]
+  float* part_o;           // [T, S, 2 halves, 256 dims, H]: each split's O / l (null when S == 1)
+  float* part_lse;         // [T, S, 2 halves, H]: each split's log2-sum-exp of its logits
+  uint32_t* merge_cnt;     // [T, 2 halves]: splits done so far; zero before the launch, left zero
   uint32_t* err;
   int32_t n_heads, top_k, n_splits, split_len;
   float scale_log2;        // softmax_scale * log2(e)
@@ -68,15 +69,16 @@ struct SfaParams {
 
 // 2-D TMA map over `rows` rows of `row_elems` elements of `elem` bytes, 128-byte
 // swizzle, box = 128 bytes x box_rows (tma_host.cu).
-bool make_tma_2d_sw128(CUtensorMap* m, const void* base, uint64_t rows, int elem, int row_elems, int box_rows);
+// `promote_l2`: let L2 fetch 256-byte blocks around each request (good for boxes of
+// consecutive rows; for gathers of scattered rows it fetches bytes nobody asked for).
+bool make_tma_2d_sw128(CUtensorMap* m, const void* base, uint64_t rows, int elem, int row_elems, int box_rows,
+                       bool promote_l2 = true);
 
 // Launchers (each returns the cudaError_t of its launch).
 cudaError_t launch_score(const ScoreParams& p, dsa_dtype_t dt, dsa_scale_t sk, cudaStream_t s);
 bool score_tc_supported(dsa_dtype_t dt, int dim, int n_heads);
 cudaError_t launch_score_tc(const ScoreParams& p, dsa_dtype_t dt, dsa_scale_t sk, cudaStream_t s);
 cudaError_t launch_topk(const TopkParams& p, int32_t max_visible, cudaStream_t s);
-cudaError_t launch_sfa(const SfaParams& p, cudaStream_t s);
 cudaError_t launch_sfa_tc(const SfaParams& p, cudaStream_t s);
-cudaError_t launch_sfa_combine(const SfaParams& p, cudaStream_t s);
 
 }  // namespace dsa

@@ -53,6 +53,13 @@ constexpr int kXchBytes = 128 * kTok * 2;        // one fp16 partial-logit tile 
 constexpr int kMaxSplitLen = kMaxTopK;
 constexpr uint32_t kColO = 0, kColS = 256, kColP = 320, kColQr = 352, kColQl = 384;
 constexpr int kSmem = 1024 + kStages * kStageBytes + 3 * kXchBytes + kMaxSplitLen * 4 + 512;
+// Split merge: 64-column chunks of other splits' partials stream through the (then idle)
+// stage buffers, four at a time.
+constexpr int kMergeCols = 64;
+constexpr int kMergeBuf = kMergeCols * kMaxSfaHeads * 4;  // 32 KB
+static_assert(4 * kMergeBuf <= kStages * kStageBytes, "merge ring fits in the stage buffers");
+static_assert(16 * kMaxSfaHeads * 4 <= 2 * kXchBytes, "split weights fit in the exchange buffers");
+constexpr uint32_t kMergeThreads = 5 * 32;                 // gather warp 0 + the four softmax warps
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     sfa_tc_kernel(const __grid_constant__ CUtensorMap kvmap, SfaParams p) {
@@ -80,9 +87,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   uint64_t* xch_full = pv_done + 1;    // [2]: peer partial of tile t in buffer t & 1
   uint64_t* xch_empty = xch_full + 2;  // [2]: the peer has read our partial of tile t
   uint64_t* drain = xch_empty + 2;
-  uint32_t* tmem_base_s = (uint32_t*)(drain + 1);
+  uint64_t* mfull = drain + 1;   // [4]: split merge, a chunk of another split's partial landed
+  uint64_t* mempty = mfull + 4;  // [4]: the softmax warps are done with that chunk buffer
+  uint32_t* tmem_base_s = (uint32_t*)(mempty + 4);
   volatile int* abort_flag = (volatile int*)(tmem_base_s + 1);
   int* fill_row_s = (int*)(abort_flag + 1);  // a selected row that stands in for empty slots
+  volatile int* last_s = (volatile int*)(fill_row_s + 1);  // this CTA merges the splits
 
   int b, n_vis;
   resolve_token(p.tv, tok, &b, &n_vis, nullptr);
@@ -106,6 +116,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       mbar_init(&xch_empty[i], 4);  // the peer's four softmax warps, after reading their rows
     }
     mbar_init(drain, 1);
+    for (int i = 0; i < 4; ++i) {
+      mbar_init(&mfull[i], 1);
+      mbar_init(&mempty[i], 4);
+    }
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -192,6 +206,36 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             tma_gather4(sbase + q * kRegion + g * 512, &kvmap, &kv_full[stage], 256 * (int)c + 64 * q, r[0], r[1],
                         r[2], r[3]);
           tma_gather4(sbase + 4 * kRegion + g * 512, &kvmap, &kv_full[stage], 512, r[0], r[1], r[2], r[3]);
+        }
+      }
+    }
+    if (p.n_splits > 1 && warp == 0) {
+      // ---- split merge, producer: the other splits' partials, chunk by chunk -----------
+      __syncwarp();
+      named_bar_sync(1, kMergeThreads);  // partials published
+      named_bar_sync(1, kMergeThreads);  // the counter says whether this CTA merges
+      if (*last_s && lane == 0) {
+        fence_proxy_async_global();
+        const int S = p.n_splits;
+        const int64_t base = (int64_t)tok * S * 2 + c;
+        const uint32_t bytes = kMergeCols * H * 4;
+        int q = 0;
+        bool good = true;
+        for (int k = 0; good && k < 256 / kMergeCols; ++k)
+          for (int s2 = 0; good && s2 < S; ++s2) {
+            if (s2 == split) continue;
+            const int bi = q & 3;
+            if (q >= 4 && !(good = mbar_wait(&mempty[bi], ((q >> 2) - 1) & 1, abort_flag, p.err))) break;
+            mbar_arrive_expect_tx(&mfull[bi], bytes);
+            bulk_load(smem_u32(stages) + bi * kMergeBuf, p.part_o + ((base + 2 * s2) * 256 + kMergeCols * k) * H,
+                      bytes, &mfull[bi]);
+            ++q;
+          }
+        // nothing may still be landing in shared memory when the CTA exits
+        for (int i = q > 4 ? q - 4 : 0; i < q; ++i) {
+          const long long t0 = clock64();
+          while (!mbar_try_wait(smem_u32(&mfull[i & 3]), (i >> 2) & 1) && clock64() - t0 < kWaitLimitCycles) {
+          }
         }
       }
     }
@@ -454,24 +498,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       ok = __shfl_sync(0xffffffffu, ok, 0);
       __syncwarp();
     }
-    if (ok) {
-      tc_fence_after();
-      const float inv = l > 0.f ? 1.f / l : 0.f;
-      const bool live = h < H;
+    tc_fence_after();
+    const float inv = l > 0.f ? 1.f / l : 0.f;
+    const bool live = h < H;
+    if (p.n_splits == 1) {
+      if (ok) {
 #pragma unroll 1
-      for (int ch = 0; ch < 8; ++ch) {
-        uint32_t v[32];
-        if (n_tiles_run > 0) {
-          tmem_ld32(tmem + lane_off + kColO + 32 * ch, v);
-          tmem_ld_wait();
-        } else {
+        for (int ch = 0; ch < 8; ++ch) {
+          uint32_t v[32];
+          if (n_tiles_run > 0) {
+            tmem_ld32(tmem + lane_off + kColO + 32 * ch, v);
+            tmem_ld_wait();
+          } else {
 #pragma unroll
-          for (int j = 0; j < 32; ++j) v[j] = 0u;
-        }
-        if (!live) continue;
-        const int d0 = 256 * (int)c + 32 * ch;
-        if (p.n_splits == 1) {
-          uint4* dst = (uint4*)(p.out + ((int64_t)tok * H + h) * kValueDim + d0);
+            for (int j = 0; j < 32; ++j) v[j] = 0u;
+          }
+          if (!live) continue;
+          uint4* dst = (uint4*)(p.out + ((int64_t)tok * H + h) * kValueDim + 256 * (int)c + 32 * ch);
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             uint4 w;
@@ -481,16 +524,113 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             w.w = pack_bf16x2(__uint_as_float(v[8 * q + 6]) * inv, __uint_as_float(v[8 * q + 7]) * inv);
             dst[q] = w;
           }
-        } else {
-          float4* dst = (float4*)(p.part_o + (((int64_t)tok * p.n_splits + split) * H + h) * kValueDim + d0);
-#pragma unroll
-          for (int q = 0; q < 8; ++q)
-            dst[q] = make_float4(__uint_as_float(v[4 * q]) * inv, __uint_as_float(v[4 * q + 1]) * inv,
-                                 __uint_as_float(v[4 * q + 2]) * inv, __uint_as_float(v[4 * q + 3]) * inv);
         }
       }
-      if (live && p.n_splits > 1 && c == 0)
-        p.part_lse[((int64_t)tok * p.n_splits + split) * H + h] = l > 0.f ? m_ref + __log2f(l) : -INFINITY;
+    } else {
+      // Publish this split's part of the CTA's value half: O / l (column-major, so the
+      // stores and the merge's loads are coalesced across heads) and log2-sum-exp.
+      const int64_t half_id = ((int64_t)tok * p.n_splits + split) * 2 + c;
+      if (ok) {
+        float* po = p.part_o + half_id * 256 * H;
+#pragma unroll 1
+        for (int ch = 0; ch < 8; ++ch) {
+          uint32_t v[32];
+          if (n_tiles_run > 0) {
+            tmem_ld32(tmem + lane_off + kColO + 32 * ch, v);
+            tmem_ld_wait();
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] = 0u;
+          }
+          if (!live) continue;
+#pragma unroll
+          for (int j = 0; j < 32; ++j) po[(32 * ch + j) * H + h] = __uint_as_float(v[j]) * inv;
+        }
+        if (live) p.part_lse[half_id * H + h] = l > 0.f ? m_ref + __log2f(l) : -INFINITY;
+        __threadfence();
+      }
+      // The last split to publish (per token and value half) merges them all, in split
+      // order and with the same arithmetic for its own part (from tensor memory) as for
+      // the others (streamed in by warp 0), so the result does not depend on which CTA
+      // finished last; it then resets the counter for the next call.  Both barriers are
+      // passed by warp 0 and all four softmax warps whatever happened before.
+      named_bar_sync(1, kMergeThreads);
+      if (warp == kMmaWarp + 1 && lane == 0) {
+        const uint32_t prev = atomicAdd(p.merge_cnt + tok * 2 + c, 1u);
+        *last_s = prev == (uint32_t)(p.n_splits - 1);
+      }
+      named_bar_sync(1, kMergeThreads);
+      if (*last_s) {
+        __threadfence();
+        const int S = p.n_splits;
+        const int64_t base = (int64_t)tok * S * 2 + c;  // + 2 * s: split s of this half
+        const int hh = live ? h : 0;
+        // split weights 2^(lse_s - max) of this head, kept in the (now idle) exchange
+        // buffer; their sum in split order
+        float* wsm = (float*)xch + hh;
+        float mx = -INFINITY;
+        for (int s2 = 0; s2 < S; ++s2) mx = fmaxf(mx, __ldcg(p.part_lse + (base + 2 * s2) * H + hh));
+        float wsum = 0.f;
+        for (int s2 = 0; s2 < S; ++s2) {
+          const float w = mx != -INFINITY ? exp2f(__ldcg(p.part_lse + (base + 2 * s2) * H + hh) - mx) : 0.f;
+          wsm[s2 * kMaxSfaHeads] = w;
+          wsum += w;
+        }
+        const float winv = wsum > 0.f ? 1.f / wsum : 0.f;
+        const float* ring = (const float*)stages;
+        int q = 0;
+        bool good = ok;
+#pragma unroll 1
+        for (int k = 0; k < 256 / kMergeCols; ++k) {
+          float acc[kMergeCols];
+#pragma unroll
+          for (int j = 0; j < kMergeCols; ++j) acc[j] = 0.f;
+#pragma unroll 1
+          for (int s2 = 0; s2 < S && good; ++s2) {
+            const float w = wsm[s2 * kMaxSfaHeads];
+            if (s2 == split) {
+#pragma unroll
+              for (int u = 0; u < kMergeCols / 32; ++u) {
+                uint32_t v[32];
+                if (n_tiles_run > 0) {
+                  tmem_ld32(tmem + lane_off + kColO + kMergeCols * k + 32 * u, v);
+                  tmem_ld_wait();
+                } else {
+#pragma unroll
+                  for (int j = 0; j < 32; ++j) v[j] = 0u;
+                }
+#pragma unroll
+                for (int j = 0; j < 32; ++j) acc[32 * u + j] += w * (__uint_as_float(v[j]) * inv);
+              }
+            } else {
+              if (lane == 0) good = mbar_wait(&mfull[q & 3], (q >> 2) & 1, abort_flag, p.err);
+              good = __shfl_sync(0xffffffffu, good, 0);
+              __syncwarp();
+              if (good) {
+                const float* b = ring + (q & 3) * (kMergeBuf / 4) + hh;
+#pragma unroll
+                for (int j = 0; j < kMergeCols; ++j) acc[j] += w * b[j * H];
+              }
+              __syncwarp();
+              if (lane == 0) mbar_arrive(&mempty[q & 3]);
+              ++q;
+            }
+          }
+          if (good && live) {
+            uint4* dst = (uint4*)(p.out + ((int64_t)tok * H + h) * kValueDim + 256 * (int)c + kMergeCols * k);
+#pragma unroll
+            for (int j = 0; j < kMergeCols / 8; ++j) {
+              uint4 o;
+              o.x = pack_bf16x2(acc[8 * j] * winv, acc[8 * j + 1] * winv);
+              o.y = pack_bf16x2(acc[8 * j + 2] * winv, acc[8 * j + 3] * winv);
+              o.z = pack_bf16x2(acc[8 * j + 4] * winv, acc[8 * j + 5] * winv);
+              o.w = pack_bf16x2(acc[8 * j + 6] * winv, acc[8 * j + 7] * winv);
+              dst[j] = o;
+            }
+          }
+        }
+        if (warp == kMmaWarp + 1 && lane == 0) p.merge_cnt[tok * 2 + c] = 0u;
+      }
     }
   }
 
@@ -509,7 +649,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
 cudaError_t launch_sfa_tc(const SfaParams& p, cudaStream_t s) {
   CUtensorMap kvmap;  // the latent cache as [pages * 64 rows, 576], one-row boxes of 64 elements
-  if (!make_tma_2d_sw128(&kvmap, p.kv, (uint64_t)p.tv.num_pages * kPage, 2, kLatentDim, 1))
+  if (!make_tma_2d_sw128(&kvmap, p.kv, (uint64_t)p.tv.num_pages * kPage, 2, kLatentDim, 1, false))
     return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(sfa_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
   if (e != cudaSuccess) return e;

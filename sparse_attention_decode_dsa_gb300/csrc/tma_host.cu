@@ -23,7 +23,8 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
 
 // 2-D map over `rows` rows of `row_elems` elements (elem = 1 or 2 bytes), 128-byte
 // swizzle, box = 128 bytes x box_rows.
-bool make_tma_2d_sw128(CUtensorMap* m, const void* base, uint64_t rows, int elem, int row_elems, int box_rows) {
+bool make_tma_2d_sw128(CUtensorMap* m, const void* base, uint64_t rows, int elem, int row_elems, int box_rows,
+                       bool promote_l2) {
   auto enc = get_encode();
   if (!enc) return false;
   const CUtensorMapDataType dt = elem == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8;
@@ -32,7 +33,8 @@ bool make_tma_2d_sw128(CUtensorMap* m, const void* base, uint64_t rows, int elem
   cuuint32_t box[2] = {(cuuint32_t)(128 / elem), (cuuint32_t)box_rows};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = enc(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_SWIZZLE_128B,
+                   promote_l2 ? CU_TENSOR_MAP_L2_PROMOTION_L2_256B : CU_TENSOR_MAP_L2_PROMOTION_NONE,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
