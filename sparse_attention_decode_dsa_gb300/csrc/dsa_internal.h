@@ -73,6 +73,9 @@ struct SfaParams {
 // consecutive rows; for gathers of scattered rows it fetches bytes nobody asked for).
 bool make_tma_2d_sw128(CUtensorMap* m, const void* base, uint64_t rows, int elem, int row_elems, int box_rows,
                        bool promote_l2 = true);
+// Same with 64-byte swizzle and a 64-byte box inner extent (one-row boxes, no L2
+// promotion): for gathering 64-byte pieces of scattered rows.
+bool make_tma_2d_sw64_rows(CUtensorMap* m, const void* base, uint64_t rows, int elem, int row_elems);
 
 // Launchers (each returns the cudaError_t of its launch).
 cudaError_t launch_score(const ScoreParams& p, dsa_dtype_t dt, dsa_scale_t sk, cudaStream_t s);

@@ -11,7 +11,7 @@
 // Work split inside the pair (CTA c = 0, 1):
 //   * CTA c owns value dims [256c, 256c + 256) of the output, and contracts the logits
 //     over its 288 "own" dims: latent [256c, 256c + 256) and rope [512 + 32c, +32).
-//     Each CTA gathers its 512 latent bytes and the 128 rope bytes of every selected
+//     Each CTA gathers its 512 latent bytes and its 64 rope bytes of every selected
 //     row (the pair reads each 1152-byte row once from DRAM).
 //   * Each CTA computes partial logits S_c = Q[:, own] . KV[:, own]^T (tcgen05, A = Q
 //     from tensor memory, B = gathered rows in shared memory), multiplies them by
@@ -25,13 +25,19 @@
 //     then rescaled in tensor memory.
 //   * P (bf16) goes to tensor memory; O[128 x 256] += P . V with V read MN-major from
 //     the same shared-memory rows the logits used.
-// Warp roles: warps 0-2 (one thread each) gather rows with TMA gather4 into a 4-stage
-// ring of 128-byte swizzle atoms; warp 3 (one thread) issues each MMA as soon as its
-// inputs are ready; warps 4-7 run softmax and the epilogue, skewed by one tile: they load
-// and send the partial logits of tile n + 1 before finishing tile n, so the exchange
-// overlaps the softmax.  Tensor memory (512 columns): O [0,256), S [256,320), P [320,352),
-// Q rope [352,368), Q latent [384,512).  Every wait is bounded.  Shared memory per stage:
-// 4 latent regions + 1 rope region, each 64 rows x 128 B.
+// Warp roles: warps 0-2 gather rows with TMA gather4 into a 4-stage ring of swizzled
+// rows, each lane issuing its own gathers (a gather's cost is in its issue); warp 3 (one thread) issues each MMA as soon as its
+// inputs are ready; warps 4-7 run softmax and the epilogue, loading and sending a tile's
+// partial logits as soon as they are ready and finishing a tile as soon as the peer's
+// part has arrived, so the exchange overlaps the softmax.  Tensor memory (512 columns): O [0,256), two logit buffers
+// S0 [256,320) and S1 [320,384), Q latent [384,512).  Tile n uses logit buffer n & 1;
+// its P (bf16) is written over the peer's partial logits of tile n in the receive
+// buffer n & 1 (same 128-byte-swizzled rows, each thread its own row), and P.V(n)'s
+// completion hands that buffer back to the peer.  So QK(n + 1), the softmax of tile n
+// and P.V(n - 1) proceed at the same time; QK(n) only waits for the softmax to have
+// read S(n - 2).  Q's rope dims are an MMA operand in shared memory.  Every wait is bounded.  Shared memory per stage:
+// 4 latent regions of 64 rows x 128 B (128-byte swizzle) + 1 rope region of 64 rows
+// x 64 B (64-byte swizzle).
 #include <cuda_fp16.h>
 
 #include "sm100.cuh"
@@ -48,11 +54,14 @@ constexpr int kThreads = (kGatherWarps + 5) * 32;
 constexpr int kTok = 64;                         // selected positions per tile
 constexpr int kStages = 4;
 constexpr int kRegion = kTok * 128;              // 64 rows x 128 B
-constexpr int kStageBytes = 5 * kRegion;         // 4 latent regions + 1 rope region
+constexpr int kRopeRegion = kTok * 64;           // 64 rows x 64 B
+constexpr int kGathers = (kTok / 4) * 5;         // per tile: 16 groups of 4 slots x 5 pieces
+constexpr int kStageBytes = 4 * kRegion + kRopeRegion;  // 4 latent regions + 1 rope region
 constexpr int kXchBytes = 128 * kTok * 2;        // one fp16 partial-logit tile (128 rows x 128 B)
 constexpr int kMaxSplitLen = kMaxTopK;
-constexpr uint32_t kColO = 0, kColS = 256, kColP = 320, kColQr = 352, kColQl = 384;
-constexpr int kSmem = 1024 + kStages * kStageBytes + 3 * kXchBytes + kMaxSplitLen * 4 + 512;
+constexpr uint32_t kColO = 0, kColS = 256, kColQl = 384;  // S buffer b: kColS + 64 b
+constexpr int kQropeBytes = 128 * 64;             // Q rope (own 32 dims) [128 rows][64 B], 64-byte swizzle
+constexpr int kSmem = 1024 + kStages * kStageBytes + kQropeBytes + 3 * kXchBytes + kMaxSplitLen * 4 + 512;
 // Split merge: 64-column chunks of other splits' partials stream through the (then idle)
 // stage buffers, four at a time.
 constexpr int kMergeCols = 64;
@@ -62,7 +71,7 @@ static_assert(16 * kMaxSfaHeads * 4 <= 2 * kXchBytes, "split weights fit in the 
 constexpr uint32_t kMergeThreads = 5 * 32;                 // gather warp 0 + the four softmax warps
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
-    sfa_tc_kernel(const __grid_constant__ CUtensorMap kvmap, SfaParams p) {
+    sfa_tc_kernel(const __grid_constant__ CUtensorMap kvmap, const __grid_constant__ CUtensorMap ropemap, SfaParams p) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t c = cluster_rank();
   const uint32_t peer = c ^ 1u;
@@ -73,19 +82,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const uint32_t raw_u32 = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + ((1024 - (raw_u32 & 1023)) & 1023);
   uint8_t* stages = smem;
-  uint8_t* xch = stages + kStages * kStageBytes;              // [2][128 rows][64 fp16] peer partials
+  uint8_t* qrope = stages + kStages * kStageBytes;            // Q rope operand
+  uint8_t* xch = qrope + kQropeBytes;                         // [2][128 rows][64 fp16] peer partials, then P
   uint8_t* stg = xch + 2 * kXchBytes;                         // [128 rows][64 fp16] own partial, outbound
-  int32_t* rowid = (int32_t*)((uint8_t*)stg + kXchBytes);     // cache row of each slot or -1
+  int32_t* rowid = (int32_t*)(stg + kXchBytes);               // cache row of each slot or -1
   uint64_t* bars = (uint64_t*)(rowid + kMaxSplitLen);
   uint64_t* kv_full = bars;
   uint64_t* kv_empty = kv_full + kStages;
   uint64_t* q_ready = kv_empty + kStages;
-  uint64_t* s_full = q_ready + 1;
-  uint64_t* s_free = s_full + 1;
-  uint64_t* p_full = s_free + 1;
-  uint64_t* pv_done = p_full + 1;
-  uint64_t* xch_full = pv_done + 1;    // [2]: peer partial of tile t in buffer t & 1
-  uint64_t* xch_empty = xch_full + 2;  // [2]: the peer has read our partial of tile t
+  uint64_t* s_full = q_ready + 1;     // [2] per logit buffer: QK done
+  uint64_t* s_free = s_full + 2;      // [2]: every softmax warp has read the logits
+  uint64_t* p_full = s_free + 2;      // [2] per receive buffer: P stored
+  uint64_t* pv_done = p_full + 2;     // [2]: P.V done (P read, O updated)
+  uint64_t* xch_full = pv_done + 2;   // [2]: peer partial of tile t in buffer t & 1
+  uint64_t* xch_empty = xch_full + 2;  // [2]: the peer is done with our partial of tile t (its P.V ran)
   uint64_t* drain = xch_empty + 2;
   uint64_t* mfull = drain + 1;   // [4]: split merge, a chunk of another split's partial landed
   uint64_t* mempty = mfull + 4;  // [4]: the softmax warps are done with that chunk buffer
@@ -107,13 +117,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       mbar_init(&kv_empty[s], 1);
     }
     mbar_init(q_ready, 4);
-    mbar_init(s_full, 1);
-    mbar_init(s_free, 4);
-    mbar_init(p_full, 4);
-    mbar_init(pv_done, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s_full[i], 1);
+      mbar_init(&s_free[i], 4);
+      mbar_init(&p_full[i], 4);
+      mbar_init(&pv_done[i], 1);
+    }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&xch_full[i], 1);   // armed locally per tile; the peer's four copies count bytes
-      mbar_init(&xch_empty[i], 4);  // the peer's four softmax warps, after reading their rows
+      mbar_init(&xch_empty[i], 1);  // the peer's P.V(t) completion, multicast by its MMA thread
     }
     mbar_init(drain, 1);
     for (int i = 0; i < 4; ++i) {
@@ -165,7 +177,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     int fr = -1;
     for (int j = 0; j < n_tiles * kTok && fr < 0; ++j) fr = rowid[j];
     *fill_row_s = fr;
-    if (fr >= 0) tma_prefetch_desc(&kvmap);
+    if (fr >= 0) {
+      tma_prefetch_desc(&kvmap);
+      tma_prefetch_desc(&ropemap);
+    }
   }
   tc_fence_before();
   __syncthreads();
@@ -179,33 +194,33 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
   if (warp < kGatherWarps) {
     // ============================ gather (TMA) =========================================
-    // Per tile and per group of 4 slots: four 128-byte pieces of this CTA's latent dims
-    // and the 128-byte rope piece, each one gather4 of four rows, landing as 128-byte
-    // swizzled rows.  Gather warp w issues the groups g with g % kGatherWarps == w.
-    // Empty slots fetch a selected row; their logits are masked.
-    if (lane == 0) {
-      constexpr int kAllGroups = kTok / 4;
-      const int my_groups = (kAllGroups - warp + kGatherWarps - 1) / kGatherWarps;
+    // Per tile and per group g of 4 slots: four 128-byte pieces q = 0..3 of this CTA's
+    // latent dims (128-byte swizzled rows) and the 64-byte piece q = 4 of its rope dims
+    // (64-byte swizzled rows), each one gather4 of four rows.  Gather i = 5g + q of a
+    // tile is issued by lane i / 3 of warp i % 3.  Empty slots fetch a selected row;
+    // their logits are masked.
+    {
+      const int i = lane * kGatherWarps + warp;
+      const bool mine = i < kGathers;
+      const int g = i / 5, q = i - 5 * (i / 5);
+      const int x = q < 4 ? 256 * (int)c + 64 * q : 512 + 32 * (int)c;
+      const uint32_t doff = q < 4 ? q * kRegion + g * 512 : 4 * kRegion + g * 256;
+      const CUtensorMap* map = q < 4 ? &kvmap : &ropemap;
+      const uint32_t my_bytes = __reduce_add_sync(0xffffffffu, mine ? (q < 4 ? 512u : 256u) : 0u);
       const int fill = *fill_row_s;
       for (int n = 0; n < n_tiles_run; ++n) {
         const int stage = n % kStages;
-        if (!mbar_wait(&kv_empty[stage], ((n / kStages) & 1) ^ 1, abort_flag, p.err)) break;
-        mbar_arrive_expect_tx(&kv_full[stage], my_groups * 5 * 512);
-        const uint32_t sbase = smem_u32(stages + stage * kStageBytes);
-        const int32_t* rt = rowid + n * kTok;
-#pragma unroll 1
-        for (int g = warp; g < kAllGroups; g += kGatherWarps) {
-          int r[4];
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const int v = rt[4 * g + i];
-            r[i] = v >= 0 ? v : fill;
-          }
-#pragma unroll
-          for (int q = 0; q < 4; ++q)
-            tma_gather4(sbase + q * kRegion + g * 512, &kvmap, &kv_full[stage], 256 * (int)c + 64 * q, r[0], r[1],
-                        r[2], r[3]);
-          tma_gather4(sbase + 4 * kRegion + g * 512, &kvmap, &kv_full[stage], 512, r[0], r[1], r[2], r[3]);
+        bool good = true;
+        if (lane == 0) {
+          good = mbar_wait(&kv_empty[stage], ((n / kStages) & 1) ^ 1, abort_flag, p.err);
+          if (good) mbar_arrive_expect_tx(&kv_full[stage], my_bytes);
+        }
+        if (!__shfl_sync(0xffffffffu, good, 0)) break;
+        __syncwarp();
+        if (mine) {
+          const int4 v = *(const int4*)(rowid + n * kTok + 4 * g);
+          tma_gather4(smem_u32(stages + stage * kStageBytes) + doff, map, &kv_full[stage], x,
+                      v.x >= 0 ? v.x : fill, v.y >= 0 ? v.y : fill, v.z >= 0 ? v.z : fill, v.w >= 0 ? v.w : fill);
         }
       }
     }
@@ -241,46 +256,51 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
   } else if (warp == kMmaWarp) {
     // ============================ MMA issuer ==========================================
-    // Event driven: the logits of tile t (QK(t): needs its rows and the softmax to have
-    // taken S(t - 1)) and P.V of tile m (needs P(m)) are issued as soon as their inputs
-    // are ready, so neither waits behind the other.  QK(t) writes S over the 288 own
-    // dims: 16 latent steps (A = Q latent columns) and 2 rope steps (this CTA's 32 of
-    // the 64 gathered rope dims).
+    // Event driven: the logits of tile t (QK(t): needs its rows, and its logit buffer
+    // t & 1 back from tile t - 2, whose logits the softmax has read) and P.V of tile m
+    // (needs P(m)) are issued as soon as their inputs are ready, so neither waits behind
+    // the other.  QK(t) contracts the 288 own dims: 16 latent steps
+    // (A = Q latent columns in tensor memory) and 2 rope steps (A = Q rope in shared
+    // memory, B = this CTA's 32 of the 64 gathered rope dims).
     if (lane == 0) {
       const uint32_t id_qk = idesc(128, kTok, 1u, 1u);
       const uint32_t id_pv = idesc_bmn(128, 256, 1u, 1u);
+      const uint32_t qr = smem_u32(qrope);
       bool ok = mbar_wait(q_ready, 0, abort_flag, p.err);
       int next_qk = 0, next_pv = 0;
       long long idle_since = clock64();
       while (ok && next_pv < n_tiles_run) {
         bool progress = false;
         if (next_qk < n_tiles_run) {
-          const int t = next_qk, stage = t % kStages;
-          if (mbar_try_wait(smem_u32(&kv_full[stage]), (t / kStages) & 1) &&
-              (t == 0 || mbar_try_wait(smem_u32(s_free), (t - 1) & 1))) {
+          const int t = next_qk, stage = t % kStages, b = t & 1;
+          if (mbar_test(smem_u32(&kv_full[stage]), (t / kStages) & 1) &&
+              (t < 2 || mbar_test(smem_u32(&s_free[b]), ((t - 2) >> 1) & 1))) {
             tc_fence_after();
             const uint32_t sb = smem_u32(stages + stage * kStageBytes);
+            const uint32_t d = tmem + kColS + 64 * b;
 #pragma unroll
-            for (int k = 0; k < 18; ++k) {
-              const uint32_t a = tmem + (k < 16 ? kColQl + 8 * k : kColQr + 8 * (k - 16));
-              const uint32_t boff = k < 16 ? (k >> 2) * kRegion + (k & 3) * 32 : 4 * kRegion + 64 * c + (k - 16) * 32;
-              mma_f16_ts(tmem + kColS, a, desc_sw128(sb + boff), id_qk, k > 0);
-            }
-            tc_commit(s_full);
+            for (int k = 0; k < 16; ++k)
+              mma_f16_ts(d, tmem + kColQl + 8 * k, desc_sw128(sb + (k >> 2) * kRegion + (k & 3) * 32), id_qk, k > 0);
+#pragma unroll
+            for (int k = 0; k < 2; ++k)
+              mma_f16(d, desc_sw64(qr + 32 * k), desc_sw64(sb + 4 * kRegion + 32 * k), id_qk, 1u);
+            tc_commit(&s_full[b]);
             ++next_qk;
             progress = true;
           }
         }
-        if (next_pv < next_qk && mbar_try_wait(smem_u32(p_full), next_pv & 1)) {
+        if (next_pv < next_qk && mbar_test(smem_u32(&p_full[next_pv & 1]), (next_pv >> 1) & 1)) {
           const int m = next_pv, stage = m % kStages;
           tc_fence_after();
           const uint32_t sb = smem_u32(stages + stage * kStageBytes);
+          const uint32_t pb = smem_u32(xch + (m & 1) * kXchBytes);
 #pragma unroll
           for (int j = 0; j < kTok / 16; ++j)
-            mma_f16_ts(tmem + kColO, tmem + kColP + 8 * j, desc_sw128_mn(sb + j * 2048, kRegion, 1024), id_pv,
-                       (m > 0 || j > 0) ? 1u : 0u);
-          tc_commit(pv_done);
+            mma_f16(tmem + kColO, desc_sw128(pb + 32 * j), desc_sw128_mn(sb + j * 2048, kRegion, 1024), id_pv,
+                    (m > 0 || j > 0) ? 1u : 0u);
+          tc_commit(&pv_done[m & 1]);
           tc_commit(&kv_empty[stage]);
+          tc_commit_mc(&xch_empty[m & 1], (uint16_t)(1u << peer));  // the peer may send tile m + 2
           ++next_pv;
           progress = true;
         }
@@ -292,6 +312,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           atomicOr(p.err, DSA_DEVERR_TIMEOUT);
           *abort_flag = 1;
           ok = false;
+        } else {
+          __nanosleep(20);
         }
       }
       tc_commit(drain);
@@ -321,16 +343,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         tmem_st32(tmem + lane_off + kColQl + 32 * ch, w);
       }
-      uint32_t wr[16];
+      // rope: this CTA's 32 dims, row h of the 64-byte-swizzled operand
 #pragma unroll
       for (int v = 0; v < 4; ++v) {
         const uint4 x = live ? __ldg(q4 + (512 + 32 * c) / 8 + v) : make_uint4(0, 0, 0, 0);
-        wr[4 * v] = x.x;
-        wr[4 * v + 1] = x.y;
-        wr[4 * v + 2] = x.z;
-        wr[4 * v + 3] = x.w;
+        *(uint4*)(qrope + h * 64 + ((v ^ ((h >> 1) & 3)) << 4)) = x;
       }
-      tmem_st16(tmem + lane_off + kColQr, wr);
+      fence_proxy_async_smem();  // visible to the MMA (async proxy)
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
@@ -340,7 +359,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const uint32_t xch_peer0 = map_to_rank(smem_u32(xch) + warp_rows, peer);
     const uint32_t stg_local = smem_u32(stg) + warp_rows;
     const uint32_t xfull_peer0 = map_to_rank(smem_u32(&xch_full[0]), peer);
-    const uint32_t xempty_peer0 = map_to_rank(smem_u32(&xch_empty[0]), peer);
     const uint32_t myrow = (uint32_t)h * (kTok * 2);
     const uint32_t sw = (uint32_t)(h & 7);
     float m_ref = -INFINITY, l = 0.f;
@@ -348,34 +366,34 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
     // Loads this CTA's partial logits of tile t, scales them by softmax_scale * log2(e)
     // and rounds them to fp16 into `dst` (kept: both CTAs sum the same rounded halves,
-    // so their softmax is identical), frees the logit columns for the next QK, and
-    // sends them (staging + one bulk copy per warp) to the peer's buffer t & 1 once the
-    // peer has read tile t - 2 from it.  Returns false on abort.
+    // so their softmax is identical), frees the logit buffer for QK(t + 2), and stores
+    // sends them (staging + one bulk copy per warp) to the peer's receive buffer t & 1
+    // once the peer is done with tile t - 2 there.  Returns false on abort.
     auto load_and_send = [&](int t, uint32_t (&dst)[kTok / 2]) -> bool {
       bool good = true;
-      if (lane == 0) good = mbar_wait(s_full, t & 1, abort_flag, p.err);
+      if (lane == 0) good = mbar_wait(&s_full[t & 1], (t >> 1) & 1, abort_flag, p.err);
       if (!__shfl_sync(0xffffffffu, good, 0)) return false;
       __syncwarp();
       tc_fence_after();
       {
         uint32_t v0[32], v1[32];
-        tmem_ld32(tmem + lane_off + kColS, v0);
-        tmem_ld32(tmem + lane_off + kColS + 32, v1);
+        tmem_ld32(tmem + lane_off + kColS + 64 * (t & 1), v0);
+        tmem_ld32(tmem + lane_off + kColS + 64 * (t & 1) + 32, v1);
         tmem_ld_wait();
+        const uint64_t sc2 = f2_pack(p.scale_log2, p.scale_log2);
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
-          const __half2 a = __floats2half2_rn(__uint_as_float(v0[2 * j]) * p.scale_log2,
-                                              __uint_as_float(v0[2 * j + 1]) * p.scale_log2);
-          const __half2 b = __floats2half2_rn(__uint_as_float(v1[2 * j]) * p.scale_log2,
-                                              __uint_as_float(v1[2 * j + 1]) * p.scale_log2);
-          dst[j] = *(const uint32_t*)&a;
-          dst[16 + j] = *(const uint32_t*)&b;
+          float a0, a1, b0, b1;
+          f2_unpack(f2_mul(f2_pack(__uint_as_float(v0[2 * j]), __uint_as_float(v0[2 * j + 1])), sc2), a0, a1);
+          f2_unpack(f2_mul(f2_pack(__uint_as_float(v1[2 * j]), __uint_as_float(v1[2 * j + 1])), sc2), b0, b1);
+          dst[j] = cvt_f16x2(a0, a1);
+          dst[16 + j] = cvt_f16x2(b0, b1);
         }
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
-        mbar_arrive(s_free);
+        mbar_arrive(&s_free[t & 1]);
         if (t > 0) bulk_wait_read0();  // staging free again
       }
       __syncwarp();
@@ -396,39 +414,33 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       return __shfl_sync(0xffffffffu, good, 0);
     };
 
-    uint32_t sc[kTok / 2];  // own partial logits of the tile being finished (fp16 pairs)
-    if (n_tiles_run > 0) ok = load_and_send(0, sc);
-    for (int n = 0; ok && n < n_tiles_run; ++n) {
-      // ---- start tile n + 1: its exchange overlaps the rest of tile n --------------
-      uint32_t sn[kTok / 2];
-      if (n + 1 < n_tiles_run && !(ok = load_and_send(n + 1, sn))) break;
-      // ---- finish tile n -----------------------------------------------------------
+    // Finishes tile n from this CTA's rounded partial logits `own`: adds the peer's part,
+    // runs the online softmax and stores P.  Returns false on abort.
+    auto finish = [&](int n, const uint32_t (&own)[kTok / 2]) -> bool {
+      bool good = true;
       const int bb = n & 1;
       const int32_t* rt = rowid + n * kTok;
       const uint32_t vlo = __ballot_sync(0xffffffffu, rt[lane] >= 0);
       const uint32_t vhi = __ballot_sync(0xffffffffu, rt[32 + lane] >= 0);
       if (lane == 0) {
-        ok = mbar_wait(&xch_full[bb], (n >> 1) & 1, abort_flag, p.err);
-        if (ok && h == 0 && n + 2 < n_tiles_run) mbar_arrive_expect_tx(&xch_full[bb], kXchBytes);  // tile n + 2
+        good = mbar_wait(&xch_full[bb], (n >> 1) & 1, abort_flag, p.err);
+        if (good && h == 0 && n + 2 < n_tiles_run) mbar_arrive_expect_tx(&xch_full[bb], kXchBytes);  // tile n + 2
       }
-      if (!__shfl_sync(0xffffffffu, ok, 0)) { ok = false; break; }
+      if (!__shfl_sync(0xffffffffu, good, 0)) return false;
       __syncwarp();
       const uint8_t* recv = xch + bb * kXchBytes + myrow;
-      float s[kTok];  // full scaled logits of tile n
+      float s[kTok];  // full scaled logits of tile n: widen the peer's half, add ours
 #pragma unroll
       for (int u = 0; u < kTok / 8; ++u) {
         const uint4 r = *(const uint4*)(recv + (((uint32_t)u ^ sw) << 4));
         const uint32_t rr[4] = {r.x, r.y, r.z, r.w};
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-          const float2 mine = __half22float2(*(const __half2*)&sc[4 * u + i]);
-          const float2 theirs = __half22float2(*(const __half2*)&rr[i]);
-          s[8 * u + 2 * i] = mine.x + theirs.x;
-          s[8 * u + 2 * i + 1] = mine.y + theirs.y;
+          f16x2_to_f32(rr[i], s[8 * u + 2 * i], s[8 * u + 2 * i + 1]);
+          add_f16x2_to(own[4 * u + i], s[8 * u + 2 * i], s[8 * u + 2 * i + 1]);
         }
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive_remote_relaxed(xempty_peer0 + bb * 8);  // its loads fed the adds above
       // online softmax (base 2), masked positions get no weight
       if ((vlo & vhi) != 0xffffffffu) {
 #pragma unroll
@@ -437,13 +449,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           s[j] = v ? s[j] : -INFINITY;
         }
       }
-      float mx[8];  // independent partial maxima
+      float mx[8];  // independent partial maxima, three inputs per step
 #pragma unroll
       for (int i = 0; i < 8; ++i) mx[i] = s[i];
 #pragma unroll
-      for (int j = 8; j < kTok; ++j) mx[j & 7] = fmaxf(mx[j & 7], s[j]);
-      const float tmax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                               fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+      for (int j = 8; j < kTok; j += 16)
+#pragma unroll
+        for (int i = 0; i < 8; ++i) mx[i] = j + 8 + i < kTok ? max3f(mx[i], s[j + i], s[j + 8 + i]) : fmaxf(mx[i], s[j + i]);
+      const float tmax = max3f(max3f(mx[0], mx[1], mx[2]), max3f(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
       float alpha = 1.f;
       bool rescale = false;
       if (tmax != -INFINITY && (m_ref == -INFINITY || tmax > m_ref + 8.f)) {
@@ -454,21 +467,30 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         m_ref = tmax;
       }
       const float msub = m_ref == -INFINITY ? 0.f : m_ref;  // nothing visible yet: all weights 0
-      float ps[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};  // independent partial sums
+      const uint64_t negm = f2_pack(-msub, -msub);
+      uint64_t ps[4] = {0ull, 0ull, 0ull, 0ull};  // paired partial sums
+      uint32_t pw[kTok / 2];
 #pragma unroll
-      for (int j = 0; j < kTok; ++j) {
-        s[j] = fast_exp2(s[j] - msub);  // 2^-inf = 0 for masked positions
-        ps[j & 7] += s[j];
+      for (int j = 0; j < kTok / 2; ++j) {
+        float x0, x1;
+        f2_unpack(f2_add(f2_pack(s[2 * j], s[2 * j + 1]), negm), x0, x1);
+        x0 = fast_exp2(x0);  // 2^-inf = 0 for masked positions
+        x1 = fast_exp2(x1);
+        ps[j & 3] = f2_add(ps[j & 3], f2_pack(x0, x1));
+        pw[j] = cvt_bf16x2(x0, x1);
       }
-      const float rs = ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
+      float r0, r1, r2, r3;
+      f2_unpack(f2_add(ps[0], ps[1]), r0, r1);
+      f2_unpack(f2_add(ps[2], ps[3]), r2, r3);
+      const float rs = (r0 + r2) + (r1 + r3);
       l = l * alpha + rs;
-      if (n > 0) {  // P.V of tile n - 1 has consumed P and updated O
-        if (lane == 0) ok = mbar_wait(pv_done, (n - 1) & 1, abort_flag, p.err);
-        if (!__shfl_sync(0xffffffffu, ok, 0)) { ok = false; break; }
-        __syncwarp();
-        tc_fence_after();
-      }
       if (__any_sync(0xffffffffu, rescale)) {  // rare: move O to the new reference maximum
+        if (n > 0) {  // ... once P.V(n - 1), the last one issued, has updated it
+          if (lane == 0) good = mbar_wait(&pv_done[(n - 1) & 1], ((n - 1) >> 1) & 1, abort_flag, p.err);
+          if (!__shfl_sync(0xffffffffu, good, 0)) return false;
+          __syncwarp();
+          tc_fence_after();
+        }
 #pragma unroll 1
         for (int ch = 0; ch < 8; ++ch) {
           uint32_t v[32];
@@ -479,22 +501,67 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           tmem_st32(tmem + lane_off + kColO + 32 * ch, v);
         }
       }
-      {
-        uint32_t pw[32];
+      {  // row h of P(n) over the peer's row h of tile n (read above): 128-byte swizzle,
+         // the K-major A operand of P.V
+        uint8_t* prow = xch + bb * kXchBytes + myrow;
 #pragma unroll
-        for (int j = 0; j < 32; ++j) pw[j] = cvt_bf16x2(s[2 * j], s[2 * j + 1]);
-        tmem_st32(tmem + lane_off + kColP, pw);
+        for (int u = 0; u < 8; ++u)
+          *(uint4*)(prow + (((uint32_t)u ^ (uint32_t)(h & 7)) << 4)) =
+              make_uint4(pw[4 * u], pw[4 * u + 1], pw[4 * u + 2], pw[4 * u + 3]);
       }
-      tmem_st_wait();
+      fence_proxy_async_smem();  // visible to the MMA (async proxy)
+      tmem_st_wait();            // (rescaled O)
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(p_full);
+      if (lane == 0) mbar_arrive(&p_full[n & 1]);
+      return true;
+    };
+
+    // Event loop: load-and-send the next tile a as soon as its logits are ready (that
+    // frees its logit buffer and feeds the peer), else finish the oldest tile b once the
+    // peer's part of it has arrived.  At most two own partials are held: sc for tile b,
+    // sn for tile b + 1.
+    uint32_t sc[kTok / 2], sn[kTok / 2];
+    int a = 0, b = 0;
+    long long idle_since = clock64();
+    while (ok && b < n_tiles_run) {
+      bool s_ready = false, x_ready = false;
+      if (lane == 0) {
+        s_ready = a < n_tiles_run && a <= b + 1 && mbar_test(smem_u32(&s_full[a & 1]), (a >> 1) & 1);
+        x_ready = b < a && mbar_test(smem_u32(&xch_full[b & 1]), (b >> 1) & 1);
+      }
+      s_ready = __shfl_sync(0xffffffffu, s_ready, 0);
+      x_ready = __shfl_sync(0xffffffffu, x_ready, 0);
+      if (s_ready) {
+        ok = a == b ? load_and_send(a, sc) : load_and_send(a, sn);
+        ++a;
+      } else if (x_ready) {
+        ok = finish(b, sc);
 #pragma unroll
-      for (int j = 0; j < kTok / 2; ++j) sc[j] = sn[j];  // own logits of tile n + 1
+        for (int j = 0; j < kTok / 2; ++j) sc[j] = sn[j];
+        ++b;
+      } else {
+        // nothing ready: back off; the whole warp gives up (lane 0 decides) on abort or
+        // when nothing has moved for the wait limit
+        bool quit = false;
+        if (lane == 0) {
+          if (*abort_flag) {
+            quit = true;
+          } else if (clock64() - idle_since > kWaitLimitCycles) {
+            atomicOr(p.err, DSA_DEVERR_TIMEOUT);
+            *abort_flag = 1;
+            quit = true;
+          }
+        }
+        if (__shfl_sync(0xffffffffu, quit, 0)) ok = false;
+        else __nanosleep(20);
+        continue;
+      }
+      idle_since = clock64();
     }
     // ---- epilogue: O / l -> this CTA's 256 value dims ----------------------------------
     if (ok && n_tiles_run > 0) {
-      if (lane == 0) ok = mbar_wait(pv_done, (n_tiles_run - 1) & 1, abort_flag, p.err);
+      if (lane == 0) ok = mbar_wait(&pv_done[(n_tiles_run - 1) & 1], ((n_tiles_run - 1) >> 1) & 1, abort_flag, p.err);
       ok = __shfl_sync(0xffffffffu, ok, 0);
       __syncwarp();
     }
@@ -648,13 +715,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 }  // namespace
 
 cudaError_t launch_sfa_tc(const SfaParams& p, cudaStream_t s) {
-  CUtensorMap kvmap;  // the latent cache as [pages * 64 rows, 576], one-row boxes of 64 elements
-  if (!make_tma_2d_sw128(&kvmap, p.kv, (uint64_t)p.tv.num_pages * kPage, 2, kLatentDim, 1, false))
+  // the latent cache as [pages * 64 rows, 576]: one-row boxes of 64 elements (latent
+  // pieces, 128-byte swizzle) and of 32 elements (rope pieces, 64-byte swizzle)
+  CUtensorMap kvmap, ropemap;
+  if (!make_tma_2d_sw128(&kvmap, p.kv, (uint64_t)p.tv.num_pages * kPage, 2, kLatentDim, 1, false) ||
+      !make_tma_2d_sw64_rows(&ropemap, p.kv, (uint64_t)p.tv.num_pages * kPage, 2, kLatentDim))
     return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(sfa_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
   if (e != cudaSuccess) return e;
   dim3 grid(2 * p.n_splits, p.tv.n_tokens);
-  sfa_tc_kernel<<<grid, kThreads, kSmem, s>>>(kvmap, p);
+  sfa_tc_kernel<<<grid, kThreads, kSmem, s>>>(kvmap, ropemap, p);
   return cudaGetLastError();
 }
 

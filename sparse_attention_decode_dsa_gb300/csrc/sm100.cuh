@@ -120,6 +120,16 @@ __device__ __forceinline__ void tc_commit(uint64_t* bar) {
                : "memory");
 }
 
+// Same, arriving (once) on the barrier at this shared-memory offset in every CTA of
+// the cluster whose bit is set in `cta_mask`.
+__device__ __forceinline__ void tc_commit_mc(uint64_t* bar, uint16_t cta_mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;\n" ::"r"(
+          smem_u32(bar)),
+      "h"(cta_mask)
+      : "memory");
+}
+
 // D[tmem] (+)= A[smem] * B[smem]^T, bf16/f16 inputs.
 __device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
                                         uint32_t accumulate) {
@@ -248,6 +258,51 @@ __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.comm
 // Waits until every committed bulk copy of this thread has finished reading its source.
 __device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;\n" ::: "memory"); }
 
+// ---- paired fp32 arithmetic (one instruction for two lanes of a 64-bit register pair) --
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};\n" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;\n" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;\n" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("mul.rn.f32x2 %0, %1, %2;\n" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+// max(a, b, c) in one instruction.
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;\n" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+// The two fp16 halves of `h2` widened to fp32 and added to (lo, hi): exact widening,
+// one rounding of each sum.
+__device__ __forceinline__ void add_f16x2_to(uint32_t h2, float& lo, float& hi) {
+  asm("{\n .reg .b16 a, b;\n mov.b32 {a, b}, %2;\n add.rn.f32.f16 %0, a, %0;\n add.rn.f32.f16 %1, b, %1;\n}\n"
+      : "+f"(lo), "+f"(hi)
+      : "r"(h2));
+}
+// fp16 pair -> two fp32 (exact).
+__device__ __forceinline__ void f16x2_to_f32(uint32_t h2, float& lo, float& hi) {
+  asm("{\n .reg .b16 a, b;\n mov.b32 {a, b}, %2;\n cvt.f32.f16 %0, a;\n cvt.f32.f16 %1, b;\n}\n"
+      : "=f"(lo), "=f"(hi)
+      : "r"(h2));
+}
+// Two floats -> packed fp16 pair (round to nearest even), lower half = `lo`.
+__device__ __forceinline__ uint32_t cvt_f16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;\n" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
 // Two floats -> packed bf16 pair (round to nearest even), lower half = `lo`.
 __device__ __forceinline__ uint32_t cvt_bf16x2(float lo, float hi) {
   uint32_t r;
@@ -300,6 +355,19 @@ __device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr) {
   d |= (uint64_t)(1024 >> 4) << 32;          // stride byte offset: next 8-row group
   d |= (uint64_t)1 << 46;                    // descriptor version (sm_100)
   d |= (uint64_t)2 << 61;                    // 128-byte swizzle
+  return d;
+}
+
+// Same for a K-major operand in 64-byte swizzle atoms: rows of 64 B (32 bf16), 8-row
+// (512-byte) atoms stacked along M/N; the 16-byte chunk c of row r sits at chunk
+// c ^ ((r >> 1) & 3).  A K step of 16 elements advances the start address by 32 B.
+__device__ __forceinline__ uint64_t desc_sw64(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)1 << 16;
+  d |= (uint64_t)(512 >> 4) << 32;  // next 8-row group
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)4 << 61;           // 64-byte swizzle
   return d;
 }
 
