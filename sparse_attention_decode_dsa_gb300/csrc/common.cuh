@@ -95,6 +95,13 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
 }
 
 // 16-byte global->shared copy; src_bytes = 0 zero-fills the destination.
+// Programmatic dependent launch.  pdl_trigger: this CTA no longer holds back the launch
+// of the next kernel in the stream (which may then start its own set-up early);
+// pdl_wait: wait until the previous kernel in the stream has completed and its memory
+// writes are visible.  Both are no-ops for a kernel launched without the attribute.
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
+
 __device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src, int src_bytes) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src),
                "r"(src_bytes));

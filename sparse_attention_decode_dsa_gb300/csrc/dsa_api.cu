@@ -7,6 +7,7 @@
 #include <mutex>
 #include <string>
 
+#include "common.cuh"
 #include "dsa_internal.h"
 
 namespace dsa {
@@ -126,6 +127,17 @@ dsa_status_t check_sfa(const dsa_sfa_args_t* a, const dsa_latent_cache_t* c) {
   return DSA_OK;
 }
 
+// ---- zeroing (histograms, split counters) --------------------------------------------
+// A kernel rather than a memset so that it takes part in programmatic dependent launch:
+// it waits for the previous kernel (which may still use this workspace) and lets the
+// next one start its set-up meanwhile.
+__global__ void __launch_bounds__(256) clear_kernel(uint4* p, size_t n16) {
+  pdl_trigger();
+  pdl_wait();
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n16; i += (size_t)gridDim.x * blockDim.x)
+    p[i] = make_uint4(0u, 0u, 0u, 0u);
+}
+
 // ---- workspace plans ------------------------------------------------------------------
 // Workspace: [0, 256) the device error word; for split attention, the split counters;
 // then one region the passes use in turn (the indexer's key histograms and score rows,
@@ -235,7 +247,7 @@ dsa_status_t run_indexer(const dsa_indexer_args_t* a, const dsa_index_cache_t* c
   sp.act = (int)a->act;
   sp.max_page_blocks = (ip.max_visible + kPage - 1) / kPage;
   tr.begin();
-  cudaError_t me = cudaMemsetAsync(clear, 0, clear_bytes, s);
+  cudaError_t me = launch_clear(clear, clear_bytes, s);
   tr.end("hist_clear");
   if (me != cudaSuccess) return cuda_fail(me, "clearing the key histograms");
   if (sp.max_page_blocks > 0) {
@@ -283,7 +295,7 @@ dsa_status_t run_sfa(const dsa_sfa_args_t* a, const dsa_latent_cache_t* c, const
   p.split_len = sp_.split_len;
   p.scale_log2 = a->softmax_scale * 1.4426950408889634f;
   if (p.n_splits > 1 && !cnt_zeroed) {
-    cudaError_t me = cudaMemsetAsync(cnt, 0, sp_.cnt_bytes, s);
+    cudaError_t me = launch_clear(cnt, sp_.cnt_bytes, s);
     if (me != cudaSuccess) return cuda_fail(me, "clearing the split counters");
   }
   tr.begin();
@@ -294,6 +306,14 @@ dsa_status_t run_sfa(const dsa_sfa_args_t* a, const dsa_latent_cache_t* c, const
 }
 
 }  // namespace
+
+cudaError_t launch_clear(void* p, size_t bytes, cudaStream_t s) {
+  const size_t n16 = bytes / 16;
+  if (n16 == 0) return cudaSuccess;
+  const unsigned blocks = (unsigned)(n16 < (size_t)256 * 4 * 152 ? (n16 + 1023) / 1024 : 4 * 152);
+  return launch_pdl(clear_kernel, dim3(blocks), dim3(256), 0, s, (uint4*)p, n16);
+}
+
 }  // namespace dsa
 
 using namespace dsa;

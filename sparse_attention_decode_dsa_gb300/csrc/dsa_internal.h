@@ -77,11 +77,31 @@ bool make_tma_2d_sw128(CUtensorMap* m, const void* base, uint64_t rows, int elem
 // promotion): for gathering 64-byte pieces of scattered rows.
 bool make_tma_2d_sw64_rows(CUtensorMap* m, const void* base, uint64_t rows, int elem, int row_elems);
 
+// Launch with programmatic stream serialization: the kernel may start while the previous
+// kernel in the stream is finishing; it calls pdl_wait() before touching what that
+// kernel writes (or anything a later pass overwrites).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                       Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
+}
+
 // Launchers (each returns the cudaError_t of its launch).
 cudaError_t launch_score(const ScoreParams& p, dsa_dtype_t dt, dsa_scale_t sk, cudaStream_t s);
 bool score_tc_supported(dsa_dtype_t dt, int dim, int n_heads);
 cudaError_t launch_score_tc(const ScoreParams& p, dsa_dtype_t dt, dsa_scale_t sk, cudaStream_t s);
 cudaError_t launch_topk(const TopkParams& p, int32_t max_visible, cudaStream_t s);
 cudaError_t launch_sfa_tc(const SfaParams& p, cudaStream_t s);
+cudaError_t launch_clear(void* p, size_t bytes, cudaStream_t s);  // bytes: multiple of 16
 
 }  // namespace dsa

@@ -23,6 +23,8 @@ __global__ void __launch_bounds__(kScoreThreads) score_cuda_core_kernel(ScorePar
   constexpr int G = (KIND == 2) ? D / 32 : 1;  // scale groups per row
   const int row = blockIdx.y;
   const int pblk = blockIdx.x;
+  pdl_trigger();
+  pdl_wait();
   int b, n_vis;
   resolve_token(p.tv, row, &b, &n_vis, threadIdx.x == 0 ? p.err : nullptr);
   if (pblk * kPage >= n_vis) return;
@@ -126,8 +128,7 @@ __global__ void __launch_bounds__(kScoreThreads) score_cuda_core_kernel(ScorePar
 template <int D, int KIND>
 cudaError_t launch_one(const ScoreParams& p, cudaStream_t s) {
   dim3 grid(p.max_page_blocks, p.tv.n_tokens);
-  score_cuda_core_kernel<D, KIND><<<grid, kScoreThreads, 0, s>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(score_cuda_core_kernel<D, KIND>, grid, dim3(kScoreThreads), 0, s, p);
 }
 
 }  // namespace

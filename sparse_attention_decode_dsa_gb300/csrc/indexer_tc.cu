@@ -70,6 +70,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   using C = Cfg<KIND, D>;
   const ScoreParams& p = a.p;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  pdl_trigger();  // the next kernel may start its set-up; it waits for this one to finish
   const int H = p.n_heads;
   const int N = (H + 15) / 16 * 16;
 
@@ -262,6 +263,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // ================================ epilogue ====================================
     // Group g drains the tiles n with n % kEpiGroups == g; tile n sits in accumulator
     // n % kNumAcc.  Within a group, TMEM lane i (warp quarter q = warp & 3) = token i.
+    // The scores and histograms it writes share workspace with the previous pass, so
+    // it first waits for the previous kernel (the loads and MMAs above need not).
+    pdl_wait();
     const int grp = (warp - 2) / 4;
     const int quarter = warp & 3;
     const int i = quarter * 32 + lane;
@@ -402,8 +406,7 @@ cudaError_t launch_tc(const ScoreParams& p, cudaStream_t s) {
     a.p = p;
     a.row0 = row0;
     a.nrows = p.tv.n_tokens - row0 < kMaxRowsPerLaunch ? p.tv.n_tokens - row0 : kMaxRowsPerLaunch;
-    score_tc_kernel<KIND, D><<<sms, kTcThreads, C::kSmem, s>>>(kmap, qmap, a);
-    e = cudaGetLastError();
+    e = launch_pdl(score_tc_kernel<KIND, D>, dim3(sms), dim3(kTcThreads), C::kSmem, s, kmap, qmap, a);
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;

@@ -77,6 +77,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const uint32_t peer = c ^ 1u;
   const int split = blockIdx.x >> 1, tok = blockIdx.y;
   const int H = p.n_heads;
+  pdl_trigger();  // the next kernel may start its set-up; it waits for this one to finish
 
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_u32 = smem_u32(smem_raw);
@@ -139,6 +140,46 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     tmem_alloc(tmem_base_s, 512);
     tmem_relinquish();
   }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_base_s;
+  if (warp > kMmaWarp) {
+    // Q does not depend on the previous kernel: stage it while that one finishes.
+    const int quarter = warp & 3;
+    const int h = quarter * 32 + lane;  // head row == TMEM lane
+    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    // Q (own dims) into tensor memory as packed bf16 pairs
+    {
+      const bool live = h < H;
+      const uint4* q4 = (const uint4*)(p.q + ((int64_t)tok * H + (live ? h : 0)) * kLatentDim);
+#pragma unroll 1
+      for (int ch = 0; ch < 4; ++ch) {  // latent: 4 x 32 columns (64 dims each)
+        uint32_t w[32];
+#pragma unroll
+        for (int v = 0; v < 8; ++v) {
+          const uint4 x = live ? __ldg(q4 + (256 * c + 64 * ch) / 8 + v) : make_uint4(0, 0, 0, 0);
+          w[4 * v] = x.x;
+          w[4 * v + 1] = x.y;
+          w[4 * v + 2] = x.z;
+          w[4 * v + 3] = x.w;
+        }
+        tmem_st32(tmem + lane_off + kColQl + 32 * ch, w);
+      }
+      // rope: this CTA's 32 dims, row h of the 64-byte-swizzled operand
+#pragma unroll
+      for (int v = 0; v < 4; ++v) {
+        const uint4 x = live ? __ldg(q4 + (512 + 32 * c) / 8 + v) : make_uint4(0, 0, 0, 0);
+        *(uint4*)(qrope + h * 64 + ((v ^ ((h >> 1) & 3)) << 4)) = x;
+      }
+      fence_proxy_async_smem();  // visible to the MMA (async proxy)
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(q_ready);
+    }
+  }
+  pdl_wait();  // the selected positions come from the previous kernel
   // cache rows of the selected positions of this split (-1: padding or invalid); all
   // index loads of a thread are in flight together, then all page-table loads
   {
@@ -190,7 +231,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   if (tid == 0)
     for (int t = 0; t < 2 && t < n_tiles_run; ++t) mbar_arrive_expect_tx(&xch_full[t], kXchBytes);  // tiles 0, 1
   cluster_sync_all();  // both CTAs' barriers exist before any remote traffic
-  const uint32_t tmem = *tmem_base_s;
 
   if (warp < kGatherWarps) {
     // ============================ gather (TMA) =========================================
@@ -326,35 +366,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const int quarter = warp & 3;
     const int h = quarter * 32 + lane;  // head row == TMEM lane
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-    // Q (own dims) into tensor memory as packed bf16 pairs
-    {
-      const bool live = h < H;
-      const uint4* q4 = (const uint4*)(p.q + ((int64_t)tok * H + (live ? h : 0)) * kLatentDim);
-#pragma unroll 1
-      for (int ch = 0; ch < 4; ++ch) {  // latent: 4 x 32 columns (64 dims each)
-        uint32_t w[32];
-#pragma unroll
-        for (int v = 0; v < 8; ++v) {
-          const uint4 x = live ? __ldg(q4 + (256 * c + 64 * ch) / 8 + v) : make_uint4(0, 0, 0, 0);
-          w[4 * v] = x.x;
-          w[4 * v + 1] = x.y;
-          w[4 * v + 2] = x.z;
-          w[4 * v + 3] = x.w;
-        }
-        tmem_st32(tmem + lane_off + kColQl + 32 * ch, w);
-      }
-      // rope: this CTA's 32 dims, row h of the 64-byte-swizzled operand
-#pragma unroll
-      for (int v = 0; v < 4; ++v) {
-        const uint4 x = live ? __ldg(q4 + (512 + 32 * c) / 8 + v) : make_uint4(0, 0, 0, 0);
-        *(uint4*)(qrope + h * 64 + ((v ^ ((h >> 1) & 3)) << 4)) = x;
-      }
-      fence_proxy_async_smem();  // visible to the MMA (async proxy)
-      tmem_st_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(q_ready);
-    }
     const uint32_t warp_rows = (uint32_t)(quarter * 32) * (kTok * 2);  // this warp's 4 KB slice
     const uint32_t xch_peer0 = map_to_rank(smem_u32(xch) + warp_rows, peer);
     const uint32_t stg_local = smem_u32(stg) + warp_rows;
@@ -724,8 +735,7 @@ cudaError_t launch_sfa_tc(const SfaParams& p, cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(sfa_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
   if (e != cudaSuccess) return e;
   dim3 grid(2 * p.n_splits, p.tv.n_tokens);
-  sfa_tc_kernel<<<grid, kThreads, kSmem, s>>>(kvmap, ropemap, p);
-  return cudaGetLastError();
+  return launch_pdl(sfa_tc_kernel, grid, dim3(kThreads), kSmem, s, kvmap, ropemap, p);
 }
 
 }  // namespace dsa

@@ -98,6 +98,8 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads) top
   const int row = blockIdx.y;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int K = p.top_k;
+  pdl_trigger();
+  pdl_wait();  // scores and histograms of the score kernel
 
   int b, n;
   resolve_token(p.tv, row, &b, &n, nullptr);  // the score pass reports bad metadata
@@ -321,8 +323,7 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads) top
 cudaError_t launch_topk(const TopkParams& p, int32_t max_visible, cudaStream_t s) {
   (void)max_visible;
   dim3 grid(kCluster, p.tv.n_tokens);
-  topk_cluster_kernel<<<grid, kThreads, 0, s>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(topk_cluster_kernel, grid, dim3(kThreads), 0, s, p);
 }
 
 }  // namespace dsa
