@@ -152,7 +152,7 @@ def _traffic(kernel, workload, units):
     if not os.path.exists(p):
         return None
     d = json.load(open(p)).get(kernel)
-    if not d or d.get("src_sha") != _src_sha(kernel):
+    if not d or d.get("src_sha") != _src_sha(kernel) or d.get("workload") != workload:
         return None
     # bytes per unit (key token or gathered row) from the capture, scaled to this launch
     return d["bytes_per_unit"] * units
