@@ -20,7 +20,10 @@
  *     The library allocates no memory, keeps no state between calls and may be called
  *     concurrently on different streams with different workspaces.
  *   - Pointers marked "device" must be device (or managed) memory of the current CUDA
- *     device; "host" pointers are read synchronously during the call.
+ *     device; "host" pointers are read synchronously during the call.  The index and
+ *     latent caches, their scales, the attention query and its output must start on a
+ *     16-byte boundary (they are moved in 16-byte or larger units); otherwise the call
+ *     returns DSA_ERR_INVALID_ARG.
  *   - Execution: kernels are enqueued on `stream` (a cudaStream_t; NULL = legacy default
  *     stream).  Argument checks run on the host before any launch; a failed check
  *     returns an error status and enqueues nothing.
@@ -217,9 +220,10 @@ dsa_status_t dsa_fused_decode(const dsa_indexer_args_t* iargs,
  * dsa_indexer_topk, but its scratch (the error word and the f32 score rows) lives in a
  * fixed 8 MiB array inside the library, one per device, held from the library's first
  * use on that device until the process exits.  It allocates nothing.
- *   - Limit: 256 + n_tokens * (ceil(max visible / 64) * 64 * 4 + 16384) bytes must fit
- *     in 8 MiB (e.g. 32 decode tokens over 32768 positions, or 8 over 131072); larger
- *     requests return DSA_ERR_WORKSPACE before any launch.
+ *   - Limit: 256 + n_tokens * (ceil(max visible / 64) * 64 * 4 + 16384 + 32 * dim + 64) bytes
+ *     (each part rounded up to 256) must fit in 8 MiB (e.g. 32 decode tokens over 32768
+ *     positions, or 8 over 131072); larger requests return DSA_ERR_WORKSPACE before any
+ *     launch.
  *   - The first call on a device looks up the array's device address (set-up, once per
  *     device, under a lock); make that first call before any stream capture.
  *   - Every call on a device shares the one array and it keeps the last call's

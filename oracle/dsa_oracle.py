@@ -221,6 +221,23 @@ def _lsb_exponent(x: np.ndarray) -> np.ndarray:
     return np.where(sig == 0, np.inf, e0 + tz)
 
 
+def collapsed_query_certificate(wl, token: int) -> float:
+    """max over dims d of Q_d / (2^24 A_d) for the head-collapsed query q~_d = sum_h w_h q_hd.
+
+    With the identity activation the score is also sum_d q~_d k_td.  Q_d = sum_h
+    |w_h q_hd| bounds every partial sum of q~_d and A_d is the coarsest power of two
+    dividing all its terms; a value < 1 means q~ is reached exactly in float32 (any
+    order), after which every product q~_d k_td and sum of them is a partial sum of the
+    score's terms, exact under exactness_certificate.
+    """
+    q = dequant_index_query(wl, token)                   # [H, d], scales included
+    w = wl.head_w[token].astype(np.float64)              # [H]
+    Q = (np.abs(q) * np.abs(w)[:, None]).sum(axis=0)     # [d]
+    a = (_lsb_exponent(q) + _lsb_exponent(w)[:, None]).min(axis=0)
+    ratio = np.where(np.isfinite(a), Q / np.ldexp(1.0, 24) / np.exp2(np.where(np.isfinite(a), a, 0)), 0.0)
+    return float(ratio.max())
+
+
 def exactness_certificate(wl, token: int) -> float:
     """max over visible t of S_t / (2^24 G_t) for the score I[t].
 

@@ -31,6 +31,7 @@ dsa_status_t cuda_fail(cudaError_t e, const char* what) {
 
 constexpr size_t kAlign = 256;
 size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+bool aligned16(const void* ptr) { return ((uintptr_t)ptr & 15u) == 0; }
 
 int num_sms() {
   int dev = 0, n = 0;
@@ -101,6 +102,8 @@ dsa_status_t check_indexer(const dsa_indexer_args_t* a, const dsa_index_cache_t*
   if (a->act != DSA_ACT_IDENTITY && a->act != DSA_ACT_RELU) return fail(DSA_ERR_INVALID_ARG, "unknown activation");
   if (a->q_dtype != c->dtype || a->q_scale_kind != c->scale_kind)
     return fail(DSA_ERR_UNSUPPORTED, "query and cache must share dtype and scale kind");
+  if (!aligned16(c->data) || (c->scale && !aligned16(c->scale)))
+    return fail(DSA_ERR_INVALID_ARG, "index cache data and scales must be 16-byte aligned");
   if (c->dtype == DSA_BF16) {
     if (c->scale_kind != DSA_SCALE_NONE) return fail(DSA_ERR_UNSUPPORTED, "bf16 index cache takes no scales");
   } else if (c->dtype == DSA_E4M3) {
@@ -119,8 +122,10 @@ dsa_status_t check_sfa(const dsa_sfa_args_t* a, const dsa_latent_cache_t* c) {
   if (a->n_heads < 1 || a->n_heads > kMaxSfaHeads)
     return fail(DSA_ERR_UNSUPPORTED, "sfa n_heads must be in [1, %d] (got %d)", kMaxSfaHeads, a->n_heads);
   if (!std::isfinite(a->softmax_scale)) return fail(DSA_ERR_INVALID_ARG, "softmax_scale must be finite");
+  if (!aligned16(a->q)) return fail(DSA_ERR_INVALID_ARG, "sfa q must be 16-byte aligned");
   if (c) {
     if (!c->data) return fail(DSA_ERR_INVALID_ARG, "latent cache data is NULL");
+    if (!aligned16(c->data)) return fail(DSA_ERR_INVALID_ARG, "latent cache data must be 16-byte aligned");
     if (c->dim != kLatentDim || c->v_dim != kValueDim)
       return fail(DSA_ERR_UNSUPPORTED, "latent rows must be 576 wide with a 512-wide value (got %d/%d)", c->dim, c->v_dim);
   }
@@ -145,18 +150,21 @@ __global__ void __launch_bounds__(256) clear_kernel(uint4* p, size_t n16) {
 struct IndexerPlan {
   int32_t max_visible;
   int64_t score_stride;
-  size_t score_bytes;  // the per-row key histograms, then the f32 score rows
-  size_t hist_bytes;
+  size_t score_bytes;  // the per-row key histograms, the collapsed query, the f32 score rows
+  size_t hist_bytes, qt_bytes;
 };
 
-IndexerPlan plan_indexer(int32_t max_visible, int32_t n_tokens) {
+IndexerPlan plan_indexer(int32_t max_visible, int32_t n_tokens, int32_t dim) {
   IndexerPlan p;
   p.max_visible = max_visible;
   p.score_stride = ((int64_t)max_visible + 63) / 64 * 64;
   if (p.score_stride == 0) p.score_stride = 64;
   const size_t rows = align_up((size_t)n_tokens * p.score_stride * sizeof(float));
   p.hist_bytes = align_up((size_t)n_tokens * kTopkBins * sizeof(uint32_t));
-  p.score_bytes = p.hist_bytes + rows;
+  // collapsed query: f32 [T, dim] or, split for the tensor cores, bf16 [T, 16, dim] + f32 [T, 16]
+  p.qt_bytes = align_up((size_t)n_tokens * kSplitQueryHeads * dim * sizeof(uint16_t)) +
+               align_up((size_t)n_tokens * kSplitQueryHeads * sizeof(float));
+  p.score_bytes = p.hist_bytes + p.qt_bytes + rows;
   return p;
 }
 
@@ -230,7 +238,11 @@ dsa_status_t run_indexer(const dsa_indexer_args_t* a, const dsa_index_cache_t* c
                          int32_t* out_idx, float* out_score, uint32_t* err, uint8_t* region, void* clear,
                          size_t clear_bytes, cudaStream_t s, Tracer& tr) {
   uint32_t* hist = (uint32_t*)region;
-  float* scores = (float*)(region + ip.hist_bytes);
+  float* qt = (float*)(region + ip.hist_bytes);
+  uint16_t* qsplit = (uint16_t*)(region + ip.hist_bytes);
+  float* wsplit = (float*)(region + ip.hist_bytes +
+                           align_up((size_t)tk->n_tokens * kSplitQueryHeads * c->dim * sizeof(uint16_t)));
+  float* scores = (float*)(region + ip.hist_bytes + ip.qt_bytes);
   ScoreParams sp;
   sp.tv = token_view(pg, tk, ip.max_visible);
   sp.q = a->q;
@@ -246,14 +258,37 @@ dsa_status_t run_indexer(const dsa_indexer_args_t* a, const dsa_index_cache_t* c
   sp.dim = c->dim;
   sp.act = (int)a->act;
   sp.max_page_blocks = (ip.max_visible + kPage - 1) / kPage;
+  sp.q_dep = 0;
   tr.begin();
   cudaError_t me = launch_clear(clear, clear_bytes, s);
   tr.end("hist_clear");
   if (me != cudaSuccess) return cuda_fail(me, "clearing the key histograms");
   if (sp.max_page_blocks > 0) {
+    // e4m3 with per-token scales and the identity activation: the head sum folds into
+    // the query and each key is one streamed dot product.  Otherwise the per-head
+    // contraction on the tensor cores (CUDA cores for shapes they do not take).  (The
+    // folded query split into bf16 terms serves query rows that share keys; one row per
+    // sequence gains nothing from it.)
+    const bool identity = a->act == DSA_ACT_IDENTITY;
+    const bool split = false;
+    const bool stream = !split && identity && c->dtype == DSA_E4M3 && c->scale_kind == DSA_SCALE_PER_TOKEN_F32 &&
+                        score_stream_supported(a->act, c->dim);
     const bool tc = score_tc_supported(c->dtype, c->dim, a->n_heads);
     tr.begin();
-    cudaError_t e = tc ? launch_score_tc(sp, c->dtype, c->scale_kind, s) : launch_score(sp, c->dtype, c->scale_kind, s);
+    cudaError_t e = cudaSuccess;
+    if (split) {
+      e = launch_qsplit(sp, qsplit, wsplit, s);
+      ScoreParams sp2 = sp;
+      sp2.q = qsplit;
+      sp2.head_w = wsplit;
+      sp2.n_heads = kSplitQueryHeads;
+      sp2.q_dep = 1;
+      if (e == cudaSuccess) e = launch_score_tc(sp2, c->dtype, c->scale_kind, s);
+    } else {
+      e = stream ? launch_score_stream(sp, c->dtype, c->scale_kind, qt, s)
+          : tc   ? launch_score_tc(sp, c->dtype, c->scale_kind, s)
+                 : launch_score(sp, c->dtype, c->scale_kind, s);
+    }
     tr.end("indexer_score");
     if (e != cudaSuccess) return cuda_fail(e, "indexer score launch");
   }
@@ -324,7 +359,7 @@ size_t dsa_indexer_workspace_size(const dsa_indexer_args_t* args, const dsa_inde
                                   const dsa_page_table_t* pages, const dsa_tokens_t* tokens) {
   int32_t mv = 0;
   if (check_indexer(args, cache) != DSA_OK || check_pages_tokens(pages, tokens, &mv) != DSA_OK) return 0;
-  return kAlign + plan_indexer(mv, tokens->n_tokens).score_bytes;
+  return kAlign + plan_indexer(mv, tokens->n_tokens, cache->dim).score_bytes;
 }
 
 dsa_status_t dsa_indexer_topk(const dsa_indexer_args_t* args, const dsa_index_cache_t* cache,
@@ -336,7 +371,7 @@ dsa_status_t dsa_indexer_topk(const dsa_indexer_args_t* args, const dsa_index_ca
   int32_t mv = 0;
   if ((st = check_pages_tokens(pages, tokens, &mv)) != DSA_OK) return st;
   if (!out_idx) return fail(DSA_ERR_INVALID_ARG, "out_idx is NULL");
-  IndexerPlan ip = plan_indexer(mv, tokens->n_tokens);
+  IndexerPlan ip = plan_indexer(mv, tokens->n_tokens, cache->dim);
   if ((st = check_ws(ws, ws_bytes, kAlign + ip.score_bytes)) != DSA_OK) return st;
   Tracer tr(trace, (cudaStream_t)stream);
   uint8_t* region = (uint8_t*)ws + kAlign;
@@ -365,6 +400,7 @@ dsa_status_t dsa_sparse_attn(const dsa_sfa_args_t* args, const dsa_latent_cache_
   int32_t mv = 0;
   if ((st = check_pages_tokens(pages, tokens, &mv)) != DSA_OK) return st;
   if (!idx || !out) return fail(DSA_ERR_INVALID_ARG, "idx and out are required");
+  if (!aligned16(out)) return fail(DSA_ERR_INVALID_ARG, "out must be 16-byte aligned");
   if (top_k < 1 || top_k > kMaxTopK) return fail(DSA_ERR_UNSUPPORTED, "top_k must be in [1, %d]", kMaxTopK);
   SfaPlan sp = plan_sfa(tokens->n_tokens, args->n_heads, top_k);
   if ((st = check_ws(ws, ws_bytes, kAlign + sp.cnt_bytes + sp.region_bytes())) != DSA_OK) return st;
@@ -383,7 +419,7 @@ size_t dsa_fused_workspace_size(const dsa_indexer_args_t* iargs, const dsa_index
   if (check_indexer(iargs, icache) != DSA_OK || check_sfa(sargs, nullptr) != DSA_OK ||
       check_pages_tokens(pages, tokens, &mv) != DSA_OK)
     return 0;
-  IndexerPlan ip = plan_indexer(mv, tokens->n_tokens);
+  IndexerPlan ip = plan_indexer(mv, tokens->n_tokens, icache->dim);
   SfaPlan sp = plan_sfa(tokens->n_tokens, sargs->n_heads, iargs->top_k);
   const size_t sfa_b = sp.region_bytes();
   return kAlign + sp.cnt_bytes + (ip.score_bytes > sfa_b ? ip.score_bytes : sfa_b);  // the passes reuse one region
@@ -400,7 +436,8 @@ dsa_status_t dsa_fused_decode(const dsa_indexer_args_t* iargs, const dsa_index_c
   int32_t mv = 0;
   if ((st = check_pages_tokens(pages, tokens, &mv)) != DSA_OK) return st;
   if (!out_idx || !out) return fail(DSA_ERR_INVALID_ARG, "out_idx and out are required");
-  IndexerPlan ip = plan_indexer(mv, tokens->n_tokens);
+  if (!aligned16(out)) return fail(DSA_ERR_INVALID_ARG, "out must be 16-byte aligned");
+  IndexerPlan ip = plan_indexer(mv, tokens->n_tokens, icache->dim);
   SfaPlan sp = plan_sfa(tokens->n_tokens, sargs->n_heads, iargs->top_k);
   const size_t sfa_b = sp.region_bytes();
   if ((st = check_ws(ws, ws_bytes, kAlign + sp.cnt_bytes + (ip.score_bytes > sfa_b ? ip.score_bytes : sfa_b))) !=
@@ -491,7 +528,7 @@ extern "C" dsa_status_t dsa_indexer_topk_noalloc(const dsa_indexer_args_t* args,
   int32_t mv = 0;
   if ((st = check_pages_tokens(pages, tokens, &mv)) != DSA_OK) return st;
   if (!out_idx) return fail(DSA_ERR_INVALID_ARG, "out_idx is NULL");
-  IndexerPlan ip = plan_indexer(mv, tokens->n_tokens);
+  IndexerPlan ip = plan_indexer(mv, tokens->n_tokens, cache->dim);
   const size_t need = kAlign + ip.score_bytes;
   if (need > kNoAllocScratchBytes)
     return fail(DSA_ERR_WORKSPACE,

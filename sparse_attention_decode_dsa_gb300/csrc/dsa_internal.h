@@ -40,6 +40,7 @@ struct ScoreParams {
   int64_t score_stride;
   uint32_t* err;
   int32_t n_heads, dim, act, max_page_blocks;
+  int32_t q_dep;           // 1: q is written by the preceding kernel (wait before reading it)
 };
 
 struct TopkParams {
@@ -76,6 +77,10 @@ bool make_tma_2d_sw128(CUtensorMap* m, const void* base, uint64_t rows, int elem
 // Same with 64-byte swizzle and a 64-byte box inner extent (one-row boxes, no L2
 // promotion): for gathering 64-byte pieces of scattered rows.
 bool make_tma_2d_sw64_rows(CUtensorMap* m, const void* base, uint64_t rows, int elem, int row_elems);
+// 2-D map without swizzle, box = box_inner elements x box_rows rows (rows land densely,
+// row-major, in shared memory); elem = 1, 2 or 4 bytes.
+bool make_tma_2d_plain(CUtensorMap* m, const void* base, uint64_t rows, int elem, int row_elems, int box_inner,
+                       int box_rows);
 
 // Launch with programmatic stream serialization: the kernel may start while the previous
 // kernel in the stream is finishing; it calls pdl_wait() before touching what that
@@ -100,6 +105,13 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 cudaError_t launch_score(const ScoreParams& p, dsa_dtype_t dt, dsa_scale_t sk, cudaStream_t s);
 bool score_tc_supported(dsa_dtype_t dt, int dim, int n_heads);
 cudaError_t launch_score_tc(const ScoreParams& p, dsa_dtype_t dt, dsa_scale_t sk, cudaStream_t s);
+bool score_stream_supported(dsa_act_t act, int dim);
+// q~ scratch: [n_tokens, dim] f32 in the workspace
+cudaError_t launch_score_stream(const ScoreParams& p, dsa_dtype_t dt, dsa_scale_t sk, float* qt, cudaStream_t s);
+// bf16, identity activation: the head-collapsed query split into 3 bf16 terms, as 16
+// heads [n_tokens, 16, dim] with weights [n_tokens, 16] (for the tensor-core kernel)
+constexpr int kSplitQueryHeads = 16;
+cudaError_t launch_qsplit(const ScoreParams& p, uint16_t* qs, float* ws, cudaStream_t s);
 cudaError_t launch_topk(const TopkParams& p, int32_t max_visible, cudaStream_t s);
 cudaError_t launch_sfa_tc(const SfaParams& p, cudaStream_t s);
 cudaError_t launch_clear(void* p, size_t bytes, cudaStream_t s);  // bytes: multiple of 16

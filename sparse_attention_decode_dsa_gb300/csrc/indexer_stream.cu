@@ -1,0 +1,286 @@
+// Lightning Indexer, scoring pass, for the identity per-head activation.
+//
+// "Adapting and Optimizing Inference for a New Model Architecture on Ascend", section
+// 3.1: scores = query x paged keys^T, weighted per head and summed over heads.  With
+// the identity activation the head sum moves inside the dot product:
+//     I[t] = sum_h w_h (q_h . k_t) = (sum_h w_h q_h) . k_t = q~ . k_t,
+// and the quantisation scales fold the same way (a per-token query scale multiplies q~,
+// a per-token key scale the dot product; MXFP8 group scales of the query go into q~
+// group by group, those of the key multiply each group's partial sum).  So the pass is
+// one small kernel that forms q~ per query token and one that streams the paged
+// K-index cache once, a dot product of length d per key: bound by HBM, not by the
+// 64-head contraction.  With integer-valued inputs and power-of-two weights and scales
+// every product and partial sum is exact in f32 (the oracle's tests check the bound on
+// every workload), so the scores equal the per-head definition bit for bit.
+//
+// Keys are read straight from the paged cache ("Day0 Inference Optimization on Ascend
+// CANN", section 2), with the MXFP8 group of 32 of section 3 for the quantised mode.
+#include <cuda_fp8.h>
+
+#include "sm100.cuh"
+
+namespace dsa {
+
+namespace {
+
+constexpr int kQtThreads = 128;
+
+// q~[row][d] = (per-token query scale) * sum_h w_h * (query group scale of h, MX) * q[h][d].
+template <int D, int KIND>  // KIND 0: bf16; 1: e4m3 + per-token f32; 2: e4m3 + E8M0/32
+__global__ void __launch_bounds__(kQtThreads) qtilde_kernel(ScoreParams p, float* qt) {
+  pdl_trigger();
+  pdl_wait();  // q~ lives in workspace that the previous pass may still use
+  const int row = blockIdx.x;
+  const int H = p.n_heads;
+  for (int d = threadIdx.x; d < D; d += kQtThreads) {
+    float acc = 0.f;
+    for (int h0 = 0; h0 < H; h0 += 16) {  // fixed order; 16 heads' loads in flight
+      float q[16], w[16];
+#pragma unroll
+      for (int u = 0; u < 16; ++u) {
+        const int h = h0 + u;
+        const int64_t off = ((int64_t)row * H + (h < H ? h : 0)) * D + d;
+        q[u] = KIND == 0 ? bf16_to_f32(__ldg((const uint16_t*)p.q + off)) : e4m3_to_f32(__ldg((const uint8_t*)p.q + off));
+        w[u] = h < H ? __ldg(p.head_w + (int64_t)row * H + h) : 0.f;
+        if (KIND == 2 && h < H)
+          w[u] *= e8m0_to_f32(__ldg((const uint8_t*)p.q_scale + ((int64_t)row * H + h) * (D / 32) + d / 32));
+      }
+#pragma unroll
+      for (int u = 0; u < 16; ++u) acc = fmaf(w[u], q[u], acc);
+    }
+    if (KIND == 1) acc *= ((const float*)p.q_scale)[row];
+    qt[(int64_t)row * D + d] = acc;
+  }
+}
+
+// bf16 keys on the tensor cores: q~ split exactly into three bf16 terms
+// q~ = hi + mid + lo (each rounding leaves a residual that is exact in f32 and needs at
+// most 8 fewer significant bits, so three terms hold all 24 bits of an f32) and handed
+// to the per-head tensor-core score kernel as 16 "heads" (the three terms, 13 zero rows)
+// with weights (1, 1, 1, 0, ...): the same kernel, a quarter of its MMA and epilogue work.
+// 512 threads per query token: thread (quarter j, dim d) sums 16 heads; the four quarter
+// sums are added in order.
+constexpr int kSplitHeads = 16;
+constexpr int kSplitThreads = 512;
+
+template <int D>
+__global__ void __launch_bounds__(kSplitThreads) qsplit_kernel(ScoreParams p, uint16_t* qs, float* ws) {
+  pdl_trigger();
+  pdl_wait();  // the split query lives in workspace that the previous pass may still use
+  const int row = blockIdx.x;
+  const int H = p.n_heads;
+  __shared__ float part[4][D];
+  for (int e = threadIdx.x; e < 4 * D; e += kSplitThreads) {
+    const int j = e / D, d = e % D;
+    float acc = 0.f;
+    float q[16], w[16];
+#pragma unroll
+    for (int u = 0; u < 16; ++u) {
+      const int h = 16 * j + u;
+      q[u] = h < H ? bf16_to_f32(__ldg((const uint16_t*)p.q + ((int64_t)row * H + h) * D + d)) : 0.f;
+      w[u] = h < H ? __ldg(p.head_w + (int64_t)row * H + h) : 0.f;
+    }
+#pragma unroll
+    for (int u = 0; u < 16; ++u) acc = fmaf(w[u], q[u], acc);
+    part[j][d] = acc;
+  }
+  __syncthreads();
+  for (int d = threadIdx.x; d < D; d += kSplitThreads) {
+    const float qt = ((part[0][d] + part[1][d]) + part[2][d]) + part[3][d];
+    const uint16_t hi = f32_to_bf16_rne(qt);
+    const float r1 = qt - bf16_to_f32(hi);
+    const uint16_t mid = f32_to_bf16_rne(r1);
+    const uint16_t lo = f32_to_bf16_rne(r1 - bf16_to_f32(mid));
+    uint16_t* o = qs + (int64_t)row * kSplitHeads * D + d;
+    o[0] = hi;
+    o[D] = mid;
+    o[2 * D] = lo;
+#pragma unroll
+    for (int h = 3; h < kSplitHeads; ++h) o[h * D] = 0;
+  }
+  if (threadIdx.x < kSplitHeads) ws[(int64_t)row * kSplitHeads + threadIdx.x] = threadIdx.x < 3 ? 1.f : 0.f;
+}
+
+// 16 bytes of a key row -> 8 (bf16) or 16 (e4m3) f32 values, exactly.
+template <int KIND>
+__device__ __forceinline__ void decode16(const uint4& raw, float* out) {
+  const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+  if (KIND == 0) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      out[2 * i] = __uint_as_float(w[i] << 16);
+      out[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w[i] & 0xFFFFu), __NV_E4M3);
+      const __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w[i] >> 16), __NV_E4M3);
+      const float2 a = __half22float2(__half2(lo));
+      const float2 c = __half22float2(__half2(hi));
+      out[4 * i] = a.x;
+      out[4 * i + 1] = a.y;
+      out[4 * i + 2] = c.x;
+      out[4 * i + 3] = c.y;
+    }
+  }
+}
+
+// One CTA per (group of pages, query token); warp w takes pages blockIdx.x * 8 + w,
+// then every gridDim.x * 8-th.  A key row is spread over LPK lanes, 16 bytes each; each
+// lane keeps its slice of q~ in registers.  The warp walks its pages in steps of KPL * U
+// keys (U 16-byte loads per lane) and issues step s + 1 before it computes step s (two
+// register buffers), the page id of the next page one page ahead, so its loads stay in
+// flight while it computes.  The CTA counts its keys' top-12-bit bins in shared memory
+// (a row's scores crowd into a few dozen bins, which global atomics would serialise on)
+// and adds the non-zero bins to the row's histogram at the end.
+constexpr int kStreamThreads = 256;
+constexpr int kStreamWarps = kStreamThreads / 32;
+constexpr int kPagesPerWarp = 4;
+
+template <int D, int KIND>
+__global__ void __launch_bounds__(kStreamThreads) score_stream_kernel(ScoreParams p, const float* qt) {
+  constexpr int ELEM = KIND == 0 ? 2 : 1;
+  constexpr int EPL = 16 / ELEM;   // elements per lane
+  constexpr int LPK = D / EPL;     // lanes per key
+  constexpr int KPL = 32 / LPK;    // keys per warp load
+  constexpr int U = 8;             // loads per lane per step
+  constexpr int GPP = kPage / (KPL * U);  // steps per page
+  constexpr int G = D / 32;        // MX groups per key
+  static_assert(kPage % (KPL * U) == 0, "whole pages per step");
+  const int row = blockIdx.y;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  pdl_trigger();
+  pdl_wait();  // q~ of the previous kernel; scores and histograms share workspace
+  int b, n_vis;
+  resolve_token(p.tv, row, &b, &n_vis, (threadIdx.x == 0 && blockIdx.x == 0) ? p.err : nullptr);
+  const int npages = (n_vis + kPage - 1) / kPage;
+  const int pj0 = blockIdx.x * kStreamWarps + warp, stride = gridDim.x * kStreamWarps;
+  if (blockIdx.x * kStreamWarps >= npages) return;  // (uniform over the CTA)
+  __shared__ uint32_t hist_s[kTopkBins];
+  for (int i = threadIdx.x; i < kTopkBins; i += kStreamThreads) hist_s[i] = 0u;
+  __syncthreads();
+  const int c = lane % LPK, kk = lane / LPK;
+  float qr[EPL];
+#pragma unroll
+  for (int e = 0; e < EPL; e += 4) {
+    const float4 v = __ldg((const float4*)(qt + (int64_t)row * D + c * EPL + e));
+    qr[e] = v.x;
+    qr[e + 1] = v.y;
+    qr[e + 2] = v.z;
+    qr[e + 3] = v.w;
+  }
+  float* srow = p.scores + (int64_t)row * p.score_stride;
+  uint32_t* hrow = p.hist + (int64_t)row * kTopkBins;
+  uint32_t* hrow_s = hist_s;
+
+  // issue cursor: page number m_i (page pj0 + m_i * stride, id pg_i; the next page's id
+  // pg_n already requested), step g_i within it
+  // (set below, only for warps that have pages)
+  int m_i = 0, g_i = 0, pg_i = -1, pg_n = -1;
+
+  // Issues the next step into raw (false when the warp's pages are done); records the
+  // step's page (pj, pg) and first key.
+  auto issue = [&](uint4 (&raw)[U], int& pj, int& pg, int& k0) -> bool {
+    pj = pj0 + m_i * stride;
+    if (pj >= npages) return false;
+    pg = pg_i;
+    k0 = g_i * (KPL * U);
+    if (pg >= 0) {
+      const uint8_t* kb = (const uint8_t*)p.k + (int64_t)pg * kPage * D * ELEM + c * 16;
+#pragma unroll
+      for (int u = 0; u < U; ++u) raw[u] = ldg_nc_v4(kb + (int64_t)(k0 + u * KPL + kk) * (D * ELEM));
+    }
+    if (++g_i == GPP) {
+      g_i = 0;
+      ++m_i;
+      pg_i = pg_n;
+      const int pj2 = pj0 + (m_i + 1) * stride;
+      pg_n = pj2 < npages ? physical_page(p.tv, b, pj2, lane == 0 ? p.err : nullptr) : -1;
+    }
+    return true;
+  };
+  // Scores the step held in raw.
+  auto consume = [&](const uint4 (&raw)[U], int pj, int pg, int k0) {
+    if (pg < 0) {  // bad page id (error bit set): its keys rank below every real key
+      for (int key = k0 + lane; key < k0 + KPL * U; key += 32) {
+        const int t = pj * kPage + key;
+        if (t < n_vis) {
+          srow[t] = -INFINITY;
+          atomicAdd(hrow_s + (score_key(-INFINITY) >> 20), 1u);
+        }
+      }
+      return;
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int key = k0 + u * KPL + kk;
+      float kv[EPL];
+      decode16<KIND>(raw[u], kv);
+      float sc = 0.f;
+#pragma unroll
+      for (int e = 0; e < EPL; ++e) sc = fmaf(qr[e], kv[e], sc);
+      if (KIND == 2)  // this lane's elements lie in one group of 32
+        sc *= e8m0_to_f32(((const uint8_t*)p.k_scale)[((int64_t)pg * kPage + key) * G + (c * EPL) / 32]);
+#pragma unroll
+      for (int o = LPK / 2; o; o >>= 1) sc += __shfl_xor_sync(0xffffffffu, sc, o);
+      const int t = pj * kPage + key;
+      if (c == 0 && t < n_vis) {
+        if (KIND == 1) sc *= ((const float*)p.k_scale)[(int64_t)pg * kPage + key];
+        srow[t] = sc;
+        atomicAdd(hrow_s + (score_key(sc) >> 20), 1u);
+      }
+    }
+  };
+
+  if (pj0 < npages) {
+    pg_i = physical_page(p.tv, b, pj0, lane == 0 ? p.err : nullptr);
+    pg_n = pj0 + stride < npages ? physical_page(p.tv, b, pj0 + stride, lane == 0 ? p.err : nullptr) : -1;
+    uint4 ra[U], rb[U];
+    int pja, pga, ka, pjb, pgb, kb_;
+    issue(ra, pja, pga, ka);
+    while (true) {
+      if (!issue(rb, pjb, pgb, kb_)) {
+        consume(ra, pja, pga, ka);
+        break;
+      }
+      consume(ra, pja, pga, ka);
+      if (!issue(ra, pja, pga, ka)) {
+        consume(rb, pjb, pgb, kb_);
+        break;
+      }
+      consume(rb, pjb, pgb, kb_);
+    }
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < kTopkBins; i += kStreamThreads) {
+    const uint32_t v = hist_s[i];
+    if (v) atomicAdd(hrow + i, v);
+  }
+}
+
+template <int D, int KIND>
+cudaError_t launch_stream(const ScoreParams& p, float* qt, cudaStream_t s) {
+  cudaError_t e = launch_pdl(qtilde_kernel<D, KIND>, dim3(p.tv.n_tokens), dim3(kQtThreads), 0, s, p, qt);
+  if (e != cudaSuccess) return e;
+  const int gx = (p.max_page_blocks + kStreamWarps * kPagesPerWarp - 1) / (kStreamWarps * kPagesPerWarp);
+  return launch_pdl(score_stream_kernel<D, KIND>, dim3(gx, p.tv.n_tokens), dim3(kStreamThreads), 0, s, p,
+                    (const float*)qt);
+}
+
+}  // namespace
+
+bool score_stream_supported(dsa_act_t act, int dim) { return act == DSA_ACT_IDENTITY && (dim == 64 || dim == 128); }
+
+cudaError_t launch_qsplit(const ScoreParams& p, uint16_t* qs, float* ws, cudaStream_t s) {
+  return p.dim == 64 ? launch_pdl(qsplit_kernel<64>, dim3(p.tv.n_tokens), dim3(kSplitThreads), 0, s, p, qs, ws)
+                     : launch_pdl(qsplit_kernel<128>, dim3(p.tv.n_tokens), dim3(kSplitThreads), 0, s, p, qs, ws);
+}
+
+cudaError_t launch_score_stream(const ScoreParams& p, dsa_dtype_t dt, dsa_scale_t sk, float* qt, cudaStream_t s) {
+  if (dt == DSA_BF16) return p.dim == 64 ? launch_stream<64, 0>(p, qt, s) : launch_stream<128, 0>(p, qt, s);
+  if (sk == DSA_SCALE_PER_TOKEN_F32) return p.dim == 64 ? launch_stream<64, 1>(p, qt, s) : launch_stream<128, 1>(p, qt, s);
+  return p.dim == 64 ? launch_stream<64, 2>(p, qt, s) : launch_stream<128, 2>(p, qt, s);
+}
+
+}  // namespace dsa

@@ -152,6 +152,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
   if (warp == 0) {
     // ================================ TMA producer ================================
+    // When the query is written by the preceding kernel the producer waits for it (the
+    // K-index loads share its in-order issue); a caller-supplied query is read at once.
+    if (p.q_dep) pdl_wait();
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0;

@@ -10,18 +10,22 @@
 // pass already counted, per row, how many keys fall in each of the 4096 bins of their
 // top 12 bits (kept in the workspace).  A cluster of 8 CTAs shares each row, CTA r
 // owning the r-th eighth of its positions:
-//   1. every CTA finds, from that histogram, the bin holding the K-th largest key;
-//   2. each CTA gathers the keys of that bin (the candidates) from its eighth;
-//   3. the candidates are pooled through distributed shared memory and every CTA finds
-//      the same exact K-th largest key T among them with an MSB-first radix select over
-//      the remaining 20 bits (8 + 8 + 4), and how many keys equal to T to take;
-//   4. each CTA counts its keys > T and == T, learns the counts of the CTAs before it,
-//      and writes, in position order, every key > T and the first (K - #{> T}) keys
-//      == T (warps own contiguous ranges; block scans place them).
+//   1. every CTA finds, from that histogram, the bin holding the K-th largest key (its
+//      own keys are loading meanwhile);
+//   2. each CTA counts its keys above that bin and gathers the keys in it (the
+//      candidates);
+//   3. each CTA writes its count and its candidates into every CTA's pool (distributed
+//      shared memory); after one cluster barrier every CTA finds the same exact K-th
+//      largest key T among all candidates with an MSB-first radix select over the
+//      remaining 20 bits (8 + 8 + 4), and from the pool alone how many keys > T and
+//      == T each CTA holds, hence where its output starts;
+//   4. each CTA writes, in position order, its keys > T and its share of the first
+//      (K - #{> T}) keys == T (warps own contiguous ranges; block scans place them).
 // Keys are read from the score row (in L2) in blocks of 4096 positions held in
-// registers, all loads of a block in flight together.  If the candidates overflow the
-// pool (a row with very many equal top bits), step 3 rescans the whole row instead,
-// with the same result.
+// registers, all loads of a block in flight together.  If a CTA has more candidates
+// than its pool slot (a row with very many equal top bits), steps 3-4 fall back to a
+// radix select that rescans the whole row and exchanges the counts, with the same
+// result.
 #include <cooperative_groups.h>
 
 #include "common.cuh"
@@ -37,8 +41,8 @@ constexpr int kThreads = 256;
 constexpr int kWarpsPerCta = kThreads / 32;
 constexpr int kChunks = 16;                      // 32-position chunks per warp per block
 constexpr int kBlock = kThreads * kChunks;       // positions whose keys sit in registers
-constexpr int kLocalCap = 2048;                  // candidates one CTA may contribute
-constexpr int kCandCap = 8192;                   // candidates pooled over the cluster
+constexpr int kLocalCap = 2048;                  // candidates one CTA may gather
+constexpr int kSlot = 256;                       // candidates one CTA may put in the pool
 
 // Exclusive prefix sum of v over the CTA in thread order, and the CTA total.
 __device__ __forceinline__ int block_excl_sum(int v, int* buf, int* total) {
@@ -116,13 +120,34 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads) top
   }
 
   __shared__ uint32_t cand_local[kLocalCap];
-  __shared__ uint32_t cand[kCandCap];
+  __shared__ uint32_t pool[kCluster][kSlot];  // every CTA's candidates
+  __shared__ int pool_n[kCluster], pool_above[kCluster];
   __shared__ uint32_t hist[256];
   __shared__ int buf[kWarpsPerCta];
-  __shared__ int s_nlocal;
-  __shared__ int cnt[2];  // this CTA's #{key > T}, #{key == T}
+  __shared__ int s_nlocal, s_above_local;
+  __shared__ int cnt[2];  // fallback: this CTA's #{key > T}, #{key == T}
   __shared__ uint32_t s_digit, s_above;
   __shared__ int s_taken_before, s_eq_before;
+
+  // This CTA's positions [lo, hi), visited in blocks of kBlock whose keys sit in
+  // registers: warp w owns kChunks consecutive 32-position chunks of each block.
+  const int chunk = ((n + kCluster - 1) / kCluster + 31) / 32 * 32;
+  const int lo = min(n, rank * chunk), hi = min(n, lo + chunk);
+  const int nblocks = (hi - lo + kBlock - 1) / kBlock;
+  uint32_t kr[kChunks];
+  auto load_block = [&](int blk) {
+    const int base = lo + blk * kBlock + warp * (kChunks * 32) + lane;
+#pragma unroll
+    for (int c = 0; c < kChunks; ++c) {
+      const int i = base + c * 32;
+      kr[c] = i < hi ? score_key(__ldg(srow + i)) : 0u;
+    }
+  };
+  int loaded = -1;
+  if (nblocks > 0) {
+    load_block(0);  // in flight while the histogram is scanned
+    loaded = 0;
+  }
 
   // ---- 1. bin of the K-th largest key among the 4096 top-12-bit bins (all CTAs alike)
   // thread t owns bins 4095-16t .. 4080-16t (high to low)
@@ -136,6 +161,7 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads) top
   }
   if (tid == 0) {
     s_nlocal = 0;
+    s_above_local = 0;
     s_digit = 0;
     s_above = 0;
   }
@@ -154,130 +180,172 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads) top
     }
   }
   __syncthreads();
-  uint32_t prefix = s_digit << 20, mask = 0xFFF00000u;
+  const uint32_t bin = s_digit;
+  uint32_t prefix = bin << 20, mask = 0xFFF00000u;
   remaining -= s_above;
 
-  // This CTA's positions [lo, hi), visited in blocks of kBlock whose keys sit in
-  // registers: warp w owns kChunks consecutive 32-position chunks of each block.
-  const int chunk = ((n + kCluster - 1) / kCluster + 31) / 32 * 32;
-  const int lo = min(n, rank * chunk), hi = min(n, lo + chunk);
-  const int nblocks = (hi - lo + kBlock - 1) / kBlock;
-  uint32_t kr[kChunks];
-  auto load_block = [&](int blk) {
-    const int base = lo + blk * kBlock + warp * (kChunks * 32) + lane;
+  // ---- 2. this CTA's keys above the bin (counted) and in it (gathered) ---------------
+  {
+    int above = 0;
+    for (int blk = 0; blk < nblocks; ++blk) {
+      if (loaded != blk) {
+        load_block(blk);
+        loaded = blk;
+      }
+      const int base = lo + blk * kBlock + warp * (kChunks * 32) + lane;
 #pragma unroll
-    for (int c = 0; c < kChunks; ++c) {
-      const int i = base + c * 32;
-      kr[c] = i < hi ? score_key(__ldg(srow + i)) : 0u;
-    }
-  };
-  int loaded = -1;
-
-  // ---- 2. this CTA's keys of the boundary bin ------------------------------------
-  for (int blk = 0; blk < nblocks; ++blk) {
-    load_block(blk);
-    loaded = blk;
-    const int base = lo + blk * kBlock + warp * (kChunks * 32) + lane;
-#pragma unroll
-    for (int c = 0; c < kChunks; ++c) {
-      const bool in = base + c * 32 < hi && (kr[c] & mask) == prefix;
-      const unsigned bal = __ballot_sync(0xffffffffu, in);
-      if (bal) {
-        int slot = 0;
-        if (lane == 0) slot = atomicAdd(&s_nlocal, __popc(bal));
-        slot = __shfl_sync(0xffffffffu, slot, 0) + __popc(bal & ((1u << lane) - 1u));
-        if (in && slot < kLocalCap) cand_local[slot] = kr[c];
+      for (int c = 0; c < kChunks; ++c) {
+        const bool ok = base + c * 32 < hi;
+        above += __popc(__ballot_sync(0xffffffffu, ok && (kr[c] >> 20) > bin));
+        const bool in = ok && (kr[c] & mask) == prefix;
+        const unsigned bal = __ballot_sync(0xffffffffu, in);
+        if (bal) {
+          int slot = 0;
+          if (lane == 0) slot = atomicAdd(&s_nlocal, __popc(bal));
+          slot = __shfl_sync(0xffffffffu, slot, 0) + __popc(bal & ((1u << lane) - 1u));
+          if (in && slot < kLocalCap) cand_local[slot] = kr[c];
+        }
       }
     }
+    if (lane == 0) atomicAdd(&s_above_local, above);
   }
-  cluster.sync();
+  __syncthreads();
 
-  // ---- 3. pool the candidates; every CTA selects the same exact K-th largest key ----
-  int ncand = 0;
-  bool pooled = true;
-  for (int r = 0; r < kCluster; ++r) {
-    const int nr = *cluster.map_shared_rank(&s_nlocal, r);
-    if (nr > kLocalCap) pooled = false;
-    ncand += nr;
-  }
-  if (ncand > kCandCap) pooled = false;
-  if (pooled) {
-    int off = 0;
+  // ---- 3. pool (every CTA writes its part into every CTA), then one cluster barrier --
+  {
+    const int nl = s_nlocal;
+    const int m = min(nl, kSlot);
     for (int r = 0; r < kCluster; ++r) {
-      const int nr = *cluster.map_shared_rank(&s_nlocal, r);
-      const uint32_t* src = cluster.map_shared_rank(cand_local, r);
-      for (int i = tid; i < nr; i += kThreads) cand[off + i] = src[i];
-      off += nr;
+      uint32_t* dst = cluster.map_shared_rank(&pool[rank][0], r);
+      for (int j = tid; j < m; j += kThreads) dst[j] = cand_local[j];
+    }
+    if (tid < kCluster) {
+      *cluster.map_shared_rank(&pool_n[rank], tid) = nl;
+      *cluster.map_shared_rank(&pool_above[rank], tid) = s_above_local;
     }
   }
-  __syncthreads();
+  cluster.sync();
+  bool fast = true;
+  for (int r = 0; r < kCluster; ++r) fast = fast && pool_n[r] <= kSlot;
+
+  const unsigned lt = (1u << lane) - 1u;
+  int taken0, ties0;  // this CTA's first output slot and #{key == T} before it
+  uint32_t T;
+  if (fast) {
+    // exact K-th largest key among the pooled candidates (all keys of the bin)
 #pragma unroll 1
-  for (int pass = 0; pass < 3; ++pass) {
-    const int shift = pass == 0 ? 12 : (pass == 1 ? 4 : 0);
-    const uint32_t dmask = pass == 2 ? 0xFu : 0xFFu;
-    hist[tid] = 0;
-    __syncthreads();
-    const int cnt_all = pooled ? ncand : n;  // without the pool, rescan the whole row
-    for (int base = 0; base < cnt_all; base += kThreads) {
-      const int i = base + tid;
-      uint32_t k = 0;
-      if (i < cnt_all) k = pooled ? cand[i] : score_key(__ldg(srow + i));
-      const bool in = i < cnt_all && (k & mask) == prefix;
-      const uint32_t dgt = (k >> shift) & dmask;
-      const unsigned act = __ballot_sync(0xffffffffu, in);
-      if (in) {
-        const unsigned peers = __match_any_sync(act, dgt);
-        if (lane == __ffs(peers) - 1) atomicAdd(&hist[dgt], (uint32_t)__popc(peers));
+    for (int pass = 0; pass < 3; ++pass) {
+      const int shift = pass == 0 ? 12 : (pass == 1 ? 4 : 0);
+      const uint32_t dmask = pass == 2 ? 0xFu : 0xFFu;
+      hist[tid] = 0;
+      __syncthreads();
+      for (int r = 0; r < kCluster; ++r)
+        for (int j = tid; j < pool_n[r]; j += kThreads) {
+          const uint32_t k = pool[r][j];
+          if ((k & mask) == prefix) atomicAdd(&hist[(k >> shift) & dmask], 1u);
+        }
+      __syncthreads();
+      if (warp == 0) find_bin256(hist, remaining, &s_digit, &s_above);
+      __syncthreads();
+      prefix |= s_digit << shift;
+      mask |= dmask << shift;
+      remaining -= s_above;
+    }
+    T = prefix;  // take `remaining` of the keys == T
+    // #{> T} and #{== T} of every CTA from the pool; place this CTA after the ones before
+    if (warp == 0) {
+      int gt_r = 0, eq_r = 0;
+      if (lane < kCluster) {
+        gt_r = pool_above[lane];
+        for (int j = 0; j < pool_n[lane]; ++j) {
+          const uint32_t k = pool[lane][j];
+          gt_r += k > T;
+          eq_r += k == T;
+        }
+      }
+      int taken = 0, eq_before = 0;
+      for (int r = 0; r < rank; ++r) {  // the whole warp, in step
+        const int g = __shfl_sync(0xffffffffu, gt_r, r);
+        const int e = __shfl_sync(0xffffffffu, eq_r, r);
+        taken += g + max(0, min((int)remaining - eq_before, e));
+        eq_before += e;
+      }
+      if (lane == 0) {
+        s_taken_before = taken;
+        s_eq_before = eq_before;
       }
     }
     __syncthreads();
-    if (warp == 0) find_bin256(hist, remaining, &s_digit, &s_above);
-    __syncthreads();
-    prefix |= s_digit << shift;
-    mask |= dmask << shift;
-    remaining -= s_above;
-  }
-  const uint32_t T = prefix;  // the K-th largest key; take `remaining` of the keys == T
-
-  // ---- 4. ordered output: count, place this CTA among the cluster, write -----------
-  int gt_c = 0, eq_c = 0;  // this CTA's totals
-  for (int blk = 0; blk < nblocks; ++blk) {
-    if (loaded != blk) {
-      load_block(blk);
-      loaded = blk;
+    taken0 = s_taken_before;
+    ties0 = s_eq_before;
+  } else {
+    // fallback: radix select rescanning the whole row, counts exchanged in the cluster
+#pragma unroll 1
+    for (int pass = 0; pass < 3; ++pass) {
+      const int shift = pass == 0 ? 12 : (pass == 1 ? 4 : 0);
+      const uint32_t dmask = pass == 2 ? 0xFu : 0xFFu;
+      hist[tid] = 0;
+      __syncthreads();
+      for (int base = 0; base < n; base += kThreads) {
+        const int i = base + tid;
+        const uint32_t k = i < n ? score_key(__ldg(srow + i)) : 0u;
+        const bool in = i < n && (k & mask) == prefix;
+        const unsigned act = __ballot_sync(0xffffffffu, in);
+        if (in) {
+          const unsigned peers = __match_any_sync(act, (k >> shift) & dmask);
+          if (lane == __ffs(peers) - 1) atomicAdd(&hist[(k >> shift) & dmask], (uint32_t)__popc(peers));
+        }
+      }
+      __syncthreads();
+      if (warp == 0) find_bin256(hist, remaining, &s_digit, &s_above);
+      __syncthreads();
+      prefix |= s_digit << shift;
+      mask |= dmask << shift;
+      remaining -= s_above;
     }
-    const int base = lo + blk * kBlock + warp * (kChunks * 32) + lane;
+    T = prefix;
+    int gt_c = 0, eq_c = 0;
+    for (int blk = 0; blk < nblocks; ++blk) {
+      if (loaded != blk) {
+        load_block(blk);
+        loaded = blk;
+      }
+      const int base = lo + blk * kBlock + warp * (kChunks * 32) + lane;
 #pragma unroll
-    for (int c = 0; c < kChunks; ++c) {
-      const bool ok = base + c * 32 < hi;
-      gt_c += (ok && kr[c] > T);
-      eq_c += (ok && kr[c] == T);
+      for (int c = 0; c < kChunks; ++c) {
+        const bool ok = base + c * 32 < hi;
+        gt_c += (ok && kr[c] > T);
+        eq_c += (ok && kr[c] == T);
+      }
     }
-  }
-  for (int o = 16; o; o >>= 1) {
-    gt_c += __shfl_xor_sync(0xffffffffu, gt_c, o);
-    eq_c += __shfl_xor_sync(0xffffffffu, eq_c, o);
-  }
-  if (tid == 0) cnt[0] = cnt[1] = 0;
-  __syncthreads();
-  if (lane == 0) {
-    atomicAdd(&cnt[0], gt_c);
-    atomicAdd(&cnt[1], eq_c);
-  }
-  cluster.sync();
-  if (tid == 0) {
-    int taken = 0, eq_before = 0;
-    for (int r = 0; r < rank; ++r) {
-      const int* c = cluster.map_shared_rank(cnt, r);
-      taken += c[0] + max(0, min((int)remaining - eq_before, c[1]));
-      eq_before += c[1];
+    for (int o = 16; o; o >>= 1) {
+      gt_c += __shfl_xor_sync(0xffffffffu, gt_c, o);
+      eq_c += __shfl_xor_sync(0xffffffffu, eq_c, o);
     }
-    s_taken_before = taken;
-    s_eq_before = eq_before;
+    if (tid == 0) cnt[0] = cnt[1] = 0;
+    __syncthreads();
+    if (lane == 0) {
+      atomicAdd(&cnt[0], gt_c);
+      atomicAdd(&cnt[1], eq_c);
+    }
+    cluster.sync();
+    if (tid == 0) {
+      int taken = 0, eq_before = 0;
+      for (int r = 0; r < rank; ++r) {
+        const int* c = cluster.map_shared_rank(cnt, r);
+        taken += c[0] + max(0, min((int)remaining - eq_before, c[1]));
+        eq_before += c[1];
+      }
+      s_taken_before = taken;
+      s_eq_before = eq_before;
+    }
+    cluster.sync();  // no CTA leaves while another may still read its shared memory
+    taken0 = s_taken_before;
+    ties0 = s_eq_before;
   }
-  cluster.sync();  // no CTA leaves while another may still read its shared memory
-  const unsigned lt = (1u << lane) - 1u;
-  int taken = s_taken_before, ties = s_eq_before;  // before the current block
+
+  // ---- 4. ordered output -------------------------------------------------------------
+  int taken = taken0, ties = ties0;  // before the current block
   for (int blk = 0; blk < nblocks; ++blk) {
     if (loaded != blk) {
       load_block(blk);

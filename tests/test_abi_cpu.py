@@ -52,8 +52,10 @@ def test_workspace_size_formula():
     pages, toks, cache, args, keep = _structs(lens=(100, 200))
     n = dsa.lib.dsa_indexer_workspace_size(C.byref(args), C.byref(cache), C.byref(pages), C.byref(toks))
     # error word (256 B) + T rows x ceil(max visible / 64) * 64 f32 scores (256-aligned)
-    # + T rows x 4096 u32 key-histogram bins
-    assert n == 256 + ((2 * 256 * 4 + 255) // 256) * 256 + 2 * 4096 * 4
+    # + T rows x 4096 u32 key-histogram bins + the collapsed query (bf16 [T, 16, dim] and
+    # f32 [T, 16] weights, each 256-aligned)
+    assert n == (256 + ((2 * 256 * 4 + 255) // 256) * 256 + 2 * 4096 * 4
+                 + ((2 * 16 * 128 * 2 + 255) // 256) * 256 + ((2 * 16 * 4 + 255) // 256) * 256)
 
 
 @pytest.mark.parametrize("mutate,status", [
@@ -69,6 +71,7 @@ def test_workspace_size_formula():
     (lambda p, t, c, a: setattr(p, "max_pages_per_seq", 1), dsa.DSA_ERR_INVALID_ARG),
     (lambda p, t, c, a: setattr(a, "head_w", None), dsa.DSA_ERR_INVALID_ARG),
     (lambda p, t, c, a: setattr(a, "act", 7), dsa.DSA_ERR_INVALID_ARG),
+    (lambda p, t, c, a: setattr(c, "data", C.c_void_p(FAKE + 8)), dsa.DSA_ERR_INVALID_ARG),
 ])
 def test_indexer_rejects_bad_arguments(mutate, status):
     pages, toks, cache, args, keep = _structs()
@@ -101,6 +104,13 @@ def test_sfa_rejects_bad_shapes():
     st = dsa.lib.dsa_sparse_attn(C.byref(sargs), C.byref(lat), C.byref(pages), C.byref(toks), C.c_void_p(FAKE),
                                  128, C.c_void_p(FAKE), C.c_void_p(FAKE), 1 << 30, None, None)
     assert st == dsa.DSA_ERR_UNSUPPORTED
+    lat.dim = 576
+    for q, data, out in [(FAKE + 4, FAKE, FAKE), (FAKE, FAKE + 8, FAKE), (FAKE, FAKE, FAKE + 2)]:
+        sargs.q = q
+        lat.data = data
+        st = dsa.lib.dsa_sparse_attn(C.byref(sargs), C.byref(lat), C.byref(pages), C.byref(toks), C.c_void_p(FAKE),
+                                     128, C.c_void_p(out), C.c_void_p(FAKE), 1 << 30, None, None)
+        assert st == dsa.DSA_ERR_INVALID_ARG  # 16-byte alignment
 
 
 def test_product_path_has_no_cpu_fallback():

@@ -296,6 +296,27 @@ def test_certificate_small(spec):
         assert O.exactness_certificate(wl, tok) < 1.0
 
 
+@pytest.mark.parametrize("spec", W.SMALL + [W.TINY_DECODE])
+def test_collapsed_query_certificate_small(spec):
+    """The head-collapsed query q~ = sum_h w_h q_h (the identity-activation form the
+    indexer kernel evaluates) is exact in fp32 on every sampled token."""
+    wl = W.make(spec)
+    for tok in range(0, wl.n_tokens, max(1, wl.n_tokens // 16)):
+        assert O.collapsed_query_certificate(wl, tok) < 1.0
+
+
+def test_collapsed_query_certificate_rejects_wide_weights():
+    """Head weights spread over 2^-30 .. 1 with odd integer queries: q~ needs more than
+    24 significant bits, and the certificate says so."""
+    wl = W.make(W.SMALL_DECODE_BF16)
+    wl.head_w[0] = np.exp2(-np.arange(wl.head_w.shape[1], dtype=np.float64) * 30.0 / wl.head_w.shape[1]).round(30)
+    wl.head_w[0] = np.exp2(np.floor(np.log2(wl.head_w[0])))
+    q = O.dequant_index_query(wl, 0)
+    if not np.any(np.abs(q) % 2 == 1):
+        pytest.skip("needs an odd query element")
+    assert O.collapsed_query_certificate(wl, 0) >= 1.0
+
+
 def test_certificate_rejects_naive_mx_reading():
     """Independent per-token key scales in [2^-4, 2^2], query scales likewise, elements in
     [-8, 8]: the fp32 score is no longer reachable exactly, and the certificate says so."""
@@ -337,6 +358,7 @@ def test_certificate_headline(spec):
     toks = sorted(set(np.linspace(0, wl.n_tokens - 1, 6).astype(int).tolist()))
     for tok in toks:
         assert O.exactness_certificate(wl, tok) < 1.0
+        assert O.collapsed_query_certificate(wl, tok) < 1.0
 
 
 def test_fp8_decode_shares_integers_with_bf16_decode():
