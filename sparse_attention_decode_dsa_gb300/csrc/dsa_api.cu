@@ -170,6 +170,7 @@ IndexerPlan plan_indexer(int32_t max_visible, int32_t n_tokens, int32_t dim) {
 
 struct SfaPlan {
   int32_t n_splits, split_len;
+  bool sib_merge;                      // two splits merged inside their cluster
   size_t cnt_bytes;                    // split counters, right after the error word
   size_t part_o_bytes, part_lse_bytes;  // in the shared region
   size_t region_bytes() const { return part_o_bytes + part_lse_bytes; }
@@ -187,7 +188,8 @@ SfaPlan plan_sfa(int32_t n_tokens, int32_t n_heads, int32_t top_k) {
   p.n_splits = s;
   p.split_len = (tiles + s - 1) / s * 64;
   p.n_splits = (tiles * 64 + p.split_len - 1) / p.split_len;  // drop empty splits
-  if (p.n_splits > 1) {
+  p.sib_merge = p.n_splits == 2;
+  if (p.n_splits > 1 && !p.sib_merge) {
     p.cnt_bytes = align_up((size_t)n_tokens * 2 * sizeof(uint32_t));
     p.part_o_bytes = align_up((size_t)n_tokens * p.n_splits * n_heads * kValueDim * sizeof(float));
     p.part_lse_bytes = align_up((size_t)n_tokens * p.n_splits * 2 * n_heads * sizeof(float));
@@ -320,16 +322,18 @@ dsa_status_t run_sfa(const dsa_sfa_args_t* a, const dsa_latent_cache_t* c, const
   p.kv = (const uint16_t*)c->data;
   p.idx = idx;
   p.out = (uint16_t*)out;
-  p.part_o = sp_.n_splits > 1 ? (float*)region : nullptr;
-  p.part_lse = sp_.n_splits > 1 ? (float*)(region + sp_.part_o_bytes) : nullptr;
-  p.merge_cnt = sp_.n_splits > 1 ? cnt : nullptr;
+  const bool global_merge = sp_.n_splits > 1 && !sp_.sib_merge;
+  p.part_o = global_merge ? (float*)region : nullptr;
+  p.part_lse = global_merge ? (float*)(region + sp_.part_o_bytes) : nullptr;
+  p.merge_cnt = global_merge ? cnt : nullptr;
+  p.sib_merge = sp_.sib_merge ? 1 : 0;
   p.err = err;
   p.n_heads = a->n_heads;
   p.top_k = top_k;
   p.n_splits = sp_.n_splits;
   p.split_len = sp_.split_len;
   p.scale_log2 = a->softmax_scale * 1.4426950408889634f;
-  if (p.n_splits > 1 && !cnt_zeroed) {
+  if (global_merge && !cnt_zeroed) {
     cudaError_t me = launch_clear(cnt, sp_.cnt_bytes, s);
     if (me != cudaSuccess) return cuda_fail(me, "clearing the split counters");
   }

@@ -65,6 +65,7 @@ struct SfaParams {
   uint32_t* merge_cnt;     // [T, 2 halves]: splits done so far; zero before the launch, left zero
   uint32_t* err;
   int32_t n_heads, top_k, n_splits, split_len;
+  int32_t sib_merge;       // two splits, merged inside a cluster of four (no partials in memory)
   float scale_log2;        // softmax_scale * log2(e)
 };
 
@@ -74,9 +75,10 @@ struct SfaParams {
 // consecutive rows; for gathers of scattered rows it fetches bytes nobody asked for).
 bool make_tma_2d_sw128(CUtensorMap* m, const void* base, uint64_t rows, int elem, int row_elems, int box_rows,
                        bool promote_l2 = true);
-// Same with 64-byte swizzle and a 64-byte box inner extent (one-row boxes, no L2
-// promotion): for gathering 64-byte pieces of scattered rows.
-bool make_tma_2d_sw64_rows(CUtensorMap* m, const void* base, uint64_t rows, int elem, int row_elems);
+// Same with 64-byte swizzle and a 64-byte box inner extent, box_rows rows (no L2
+// promotion); one-row boxes serve to gather 64-byte pieces of scattered rows.
+bool make_tma_2d_sw64_rows(CUtensorMap* m, const void* base, uint64_t rows, int elem, int row_elems,
+                           int box_rows = 1);
 // 2-D map without swizzle, box = box_inner elements x box_rows rows (rows land densely,
 // row-major, in shared memory); elem = 1, 2 or 4 bytes.
 bool make_tma_2d_plain(CUtensorMap* m, const void* base, uint64_t rows, int elem, int row_elems, int box_inner,
@@ -98,6 +100,26 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
+}
+// Same, in thread-block clusters of `cluster_x` CTAs along x.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl_cluster(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                               unsigned cluster_x, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = cluster_x;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
 }
 

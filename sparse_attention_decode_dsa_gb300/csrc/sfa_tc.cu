@@ -60,6 +60,8 @@ constexpr int kStageBytes = 4 * kRegion + kRopeRegion;  // 4 latent regions + 1 
 constexpr int kXchBytes = 128 * kTok * 2;        // one fp16 partial-logit tile (128 rows x 128 B)
 constexpr int kMaxSplitLen = kMaxTopK;
 constexpr uint32_t kColO = 0, kColS = 256, kColQl = 384;  // S buffer b: kColS + 64 b
+constexpr int kQRegion = 128 * 128;                // Q latent staging: 4 regions of 128 rows x 128 B
+static_assert(4 * kQRegion <= 2 * kStageBytes, "Q latent staging fits in stage buffers 2-3");
 constexpr int kQropeBytes = 128 * 64;             // Q rope (own 32 dims) [128 rows][64 B], 64-byte swizzle
 constexpr int kSmem = 1024 + kStages * kStageBytes + kQropeBytes + 3 * kXchBytes + kMaxSplitLen * 4 + 512;
 // Split merge: 64-column chunks of other splits' partials stream through the (then idle)
@@ -68,13 +70,21 @@ constexpr int kMergeCols = 64;
 constexpr int kMergeBuf = kMergeCols * kMaxSfaHeads * 4;  // 32 KB
 static_assert(4 * kMergeBuf <= kStages * kStageBytes, "merge ring fits in the stage buffers");
 static_assert(16 * kMaxSfaHeads * 4 <= 2 * kXchBytes, "split weights fit in the exchange buffers");
-constexpr uint32_t kMergeThreads = 5 * 32;                 // gather warp 0 + the four softmax warps
+constexpr uint32_t kMergeThreads = 5 * 32;
+// Sibling merge (two splits in one cluster): outbox and inbox of 128 rows x 128 f32
+// columns plus 128 (m, l) pairs each, in the stage buffers.
+constexpr uint32_t kSibBytes = 128 * 512 + 128 * 8;
+static_assert(2 * kSibBytes <= kStages * kStageBytes, "sibling merge buffers fit in the stage buffers");                 // gather warp 0 + the four softmax warps
 
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
-    sfa_tc_kernel(const __grid_constant__ CUtensorMap kvmap, const __grid_constant__ CUtensorMap ropemap, SfaParams p) {
+// Launched in clusters of two CTAs (the pair), or four (two splits x the pair) when the
+// two splits of a token merge inside the cluster.
+__global__ void __launch_bounds__(kThreads, 1)
+    sfa_tc_kernel(const __grid_constant__ CUtensorMap kvmap, const __grid_constant__ CUtensorMap ropemap,
+                  const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap qropemap, SfaParams p) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const uint32_t c = cluster_rank();
-  const uint32_t peer = c ^ 1u;
+  const uint32_t rank = cluster_rank();  // 2 * (split within the cluster) + c
+  const uint32_t c = rank & 1u;
+  const uint32_t peer = rank ^ 1u;
   const int split = blockIdx.x >> 1, tok = blockIdx.y;
   const int H = p.n_heads;
   pdl_trigger();  // the next kernel may start its set-up; it waits for this one to finish
@@ -98,12 +108,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   uint64_t* xch_full = pv_done + 2;   // [2]: peer partial of tile t in buffer t & 1
   uint64_t* xch_empty = xch_full + 2;  // [2]: the peer is done with our partial of tile t (its P.V ran)
   uint64_t* drain = xch_empty + 2;
-  uint64_t* mfull = drain + 1;   // [4]: split merge, a chunk of another split's partial landed
+  uint64_t* q_tma = drain + 1;    // Q (own dims) landed in shared memory
+  uint64_t* m_ready = q_tma + 1;  // sibling merge: the sibling's inbox is free
+  uint64_t* m_full = m_ready + 1; // sibling merge: the sibling's columns arrived
+  uint64_t* mfull = m_full + 1;   // [4]: split merge, a chunk of another split's partial landed
   uint64_t* mempty = mfull + 4;  // [4]: the softmax warps are done with that chunk buffer
   uint32_t* tmem_base_s = (uint32_t*)(mempty + 4);
   volatile int* abort_flag = (volatile int*)(tmem_base_s + 1);
-  int* fill_row_s = (int*)(abort_flag + 1);  // a selected row that stands in for empty slots
-  volatile int* last_s = (volatile int*)(fill_row_s + 1);  // this CTA merges the splits
+  volatile int* last_s = (volatile int*)(abort_flag + 1);  // this CTA merges the splits
 
   int b, n_vis;
   resolve_token(p.tv, tok, &b, &n_vis, nullptr);
@@ -129,11 +141,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       mbar_init(&xch_empty[i], 1);  // the peer's P.V(t) completion, multicast by its MMA thread
     }
     mbar_init(drain, 1);
+    mbar_init(q_tma, 1);
+    mbar_init(m_ready, 1);
+    mbar_init(m_full, 1);
     for (int i = 0; i < 4; ++i) {
       mbar_init(&mfull[i], 1);
       mbar_init(&mempty[i], 4);
     }
     *abort_flag = 0;
+    // the peer's partial logits of tiles 0 and 1 may arrive as soon as the cluster syncs
+    for (int t = 0; t < 2 && t < n_tiles; ++t) mbar_arrive_expect_tx(&xch_full[t], kXchBytes);
     fence_mbar_init();
   }
   if (warp == kMmaWarp) {
@@ -144,44 +161,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_base_s;
-  if (warp > kMmaWarp) {
-    // Q does not depend on the previous kernel: stage it while that one finishes.
-    const int quarter = warp & 3;
-    const int h = quarter * 32 + lane;  // head row == TMEM lane
-    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-    // Q (own dims) into tensor memory as packed bf16 pairs
-    {
-      const bool live = h < H;
-      const uint4* q4 = (const uint4*)(p.q + ((int64_t)tok * H + (live ? h : 0)) * kLatentDim);
-#pragma unroll 1
-      for (int ch = 0; ch < 4; ++ch) {  // latent: 4 x 32 columns (64 dims each)
-        uint32_t w[32];
+  // Q does not depend on the previous kernel: fetch it while that one finishes.  Its
+  // latent own dims land (TMA, 128-byte swizzle) in stage buffers 2-3, idle until tile
+  // 2's gathers; its rope own dims land directly as the 64-byte-swizzled MMA operand.
+  uint8_t* qstage = stages + 2 * kStageBytes;
+  if (warp == kMmaWarp && lane == 0) {
+    mbar_arrive_expect_tx(q_tma, (uint32_t)H * (4 * 128 + 64));
 #pragma unroll
-        for (int v = 0; v < 8; ++v) {
-          const uint4 x = live ? __ldg(q4 + (256 * c + 64 * ch) / 8 + v) : make_uint4(0, 0, 0, 0);
-          w[4 * v] = x.x;
-          w[4 * v + 1] = x.y;
-          w[4 * v + 2] = x.z;
-          w[4 * v + 3] = x.w;
-        }
-        tmem_st32(tmem + lane_off + kColQl + 32 * ch, w);
-      }
-      // rope: this CTA's 32 dims, row h of the 64-byte-swizzled operand
-#pragma unroll
-      for (int v = 0; v < 4; ++v) {
-        const uint4 x = live ? __ldg(q4 + (512 + 32 * c) / 8 + v) : make_uint4(0, 0, 0, 0);
-        *(uint4*)(qrope + h * 64 + ((v ^ ((h >> 1) & 3)) << 4)) = x;
-      }
-      fence_proxy_async_smem();  // visible to the MMA (async proxy)
-      tmem_st_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(q_ready);
-    }
+    for (int q = 0; q < 4; ++q)
+      tma_load_2d(smem_u32(qstage + q * kQRegion), &qmap, q_tma, 256 * (int)c + 64 * q, tok * H);
+    tma_load_2d(smem_u32(qrope), &qropemap, q_tma, 512 + 32 * (int)c, tok * H);
+    tma_prefetch_desc(&kvmap);
+    tma_prefetch_desc(&ropemap);
   }
-  pdl_wait();  // the selected positions come from the previous kernel
-  // cache rows of the selected positions of this split (-1: padding or invalid); all
-  // index loads of a thread are in flight together, then all page-table loads
+  __syncwarp();
+  cluster_arrive();  // this CTA's barriers exist (the wait comes before any remote traffic)
+  pdl_wait();        // the selected positions come from the previous kernel
+  // Cache row of every selected position of this split (-1: padding or invalid), while
+  // Q is in flight; all index loads of a thread are in flight together, then all
+  // page-table loads.
   {
     constexpr int kPer = (kMaxSplitLen + kThreads - 1) / kThreads;
     int pos[kPer];
@@ -197,7 +195,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
     int pg[kPer];
 #pragma unroll
-    for (int u = 0; u < kPer; ++u) pg[u] = pos[u] >= 0 ? __ldg(p.tv.block_table + (int64_t)b * p.tv.max_pages + (pos[u] >> 6)) : -1;
+    for (int u = 0; u < kPer; ++u)
+      pg[u] = pos[u] >= 0 ? __ldg(p.tv.block_table + (int64_t)b * p.tv.max_pages + (pos[u] >> 6)) : -1;
 #pragma unroll
     for (int u = 0; u < kPer; ++u) {
       const int j = tid + u * kThreads;
@@ -213,24 +212,49 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       rowid[j] = rid;
     }
   }
-  __syncthreads();
-  if (tid == 0) {
-    int fr = -1;
-    for (int j = 0; j < n_tiles * kTok && fr < 0; ++j) fr = rowid[j];
-    *fill_row_s = fr;
-    if (fr >= 0) {
-      tma_prefetch_desc(&kvmap);
-      tma_prefetch_desc(&ropemap);
+  if (warp > kMmaWarp) {
+    // each softmax thread moves its head row h of the latent part into tensor memory
+    // (packed bf16 pairs); rows past the head count are zero, in the rope operand too
+    const int quarter = warp & 3;
+    const int h = quarter * 32 + lane;  // head row == TMEM lane
+    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    const bool live = h < H;
+    bool good = true;
+    if (lane == 0) good = mbar_wait(q_tma, 0, abort_flag, p.err);
+    good = __shfl_sync(0xffffffffu, good, 0);
+#pragma unroll 1
+    for (int q = 0; q < 4; ++q) {
+      uint32_t w[32];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const uint4 x = (live && good) ? *(const uint4*)(qstage + q * kQRegion + h * 128 + ((u ^ (h & 7)) << 4))
+                                       : make_uint4(0, 0, 0, 0);
+        w[4 * u] = x.x;
+        w[4 * u + 1] = x.y;
+        w[4 * u + 2] = x.z;
+        w[4 * u + 3] = x.w;
+      }
+      tmem_st32(tmem + lane_off + kColQl + 32 * q, w);
     }
+    if (!live) {
+#pragma unroll
+      for (int v = 0; v < 4; ++v) *(uint4*)(qrope + h * 64 + (v << 4)) = make_uint4(0, 0, 0, 0);
+    }
+    fence_proxy_async_smem();  // visible to the MMA (async proxy)
+    tmem_st_wait();
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(q_ready);
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  // A split without any selected row attends to nothing: skip the pipeline entirely.
-  const int n_tiles_run = *fill_row_s >= 0 ? n_tiles : 0;
-  if (tid == 0)
-    for (int t = 0; t < 2 && t < n_tiles_run; ++t) mbar_arrive_expect_tx(&xch_full[t], kXchBytes);  // tiles 0, 1
-  cluster_sync_all();  // both CTAs' barriers exist before any remote traffic
+  // a selected row stands in for empty slots; a split without any selected row attends
+  // to nothing and skips the pipeline entirely
+  int fill = -1;
+  for (int j = 0; j < n_tiles * kTok && fill < 0; ++j) fill = rowid[j];
+  const int n_tiles_run = fill >= 0 ? n_tiles : 0;
+  cluster_wait();  // both CTAs' barriers exist before any remote traffic
 
   if (warp < kGatherWarps) {
     // ============================ gather (TMA) =========================================
@@ -247,12 +271,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const uint32_t doff = q < 4 ? q * kRegion + g * 512 : 4 * kRegion + g * 256;
       const CUtensorMap* map = q < 4 ? &kvmap : &ropemap;
       const uint32_t my_bytes = __reduce_add_sync(0xffffffffu, mine ? (q < 4 ? 512u : 256u) : 0u);
-      const int fill = *fill_row_s;
       for (int n = 0; n < n_tiles_run; ++n) {
         const int stage = n % kStages;
         bool good = true;
         if (lane == 0) {
-          good = mbar_wait(&kv_empty[stage], ((n / kStages) & 1) ^ 1, abort_flag, p.err);
+          // stage buffers 2-3 hold Q until the softmax warps have moved it to tensor memory
+          if (n == 2) good = mbar_wait(q_ready, 0, abort_flag, p.err);
+          if (good) good = mbar_wait(&kv_empty[stage], ((n / kStages) & 1) ^ 1, abort_flag, p.err);
           if (good) mbar_arrive_expect_tx(&kv_full[stage], my_bytes);
         }
         if (!__shfl_sync(0xffffffffu, good, 0)) break;
@@ -264,7 +289,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
       }
     }
-    if (p.n_splits > 1 && warp == 0) {
+    if (p.n_splits > 1 && !p.sib_merge && warp == 0) {
       // ---- split merge, producer: the other splits' partials, chunk by chunk -----------
       __syncwarp();
       named_bar_sync(1, kMergeThreads);  // partials published
@@ -302,64 +327,89 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // the other.  QK(t) contracts the 288 own dims: 16 latent steps
     // (A = Q latent columns in tensor memory) and 2 rope steps (A = Q rope in shared
     // memory, B = this CTA's 32 of the 64 gathered rope dims).
-    if (lane == 0) {
+    // The whole warp runs the loop (operands and decisions stay warp-uniform); one
+    // elected lane issues every MMA and commit, so each commit tracks all of them.
+    {
       const uint32_t id_qk = idesc(128, kTok, 1u, 1u);
       const uint32_t id_pv = idesc_bmn(128, 256, 1u, 1u);
       const uint32_t qr = smem_u32(qrope);
-      bool ok = mbar_wait(q_ready, 0, abort_flag, p.err);
+      const bool leader = elect_one();
+      bool ok = true;
+      if (lane == 0) ok = mbar_wait(q_ready, 0, abort_flag, p.err);
+      ok = __shfl_sync(0xffffffffu, ok, 0);
       int next_qk = 0, next_pv = 0;
       long long idle_since = clock64();
       while (ok && next_pv < n_tiles_run) {
         bool progress = false;
         if (next_qk < n_tiles_run) {
           const int t = next_qk, stage = t % kStages, b = t & 1;
-          if (mbar_test(smem_u32(&kv_full[stage]), (t / kStages) & 1) &&
-              (t < 2 || mbar_test(smem_u32(&s_free[b]), ((t - 2) >> 1) & 1))) {
+          bool ready = false;
+          if (lane == 0)
+            ready = mbar_test(smem_u32(&kv_full[stage]), (t / kStages) & 1) &&
+                    (t < 2 || mbar_test(smem_u32(&s_free[b]), ((t - 2) >> 1) & 1));
+          if (__shfl_sync(0xffffffffu, ready, 0)) {
             tc_fence_after();
             const uint32_t sb = smem_u32(stages + stage * kStageBytes);
             const uint32_t d = tmem + kColS + 64 * b;
+            if (leader) {
 #pragma unroll
-            for (int k = 0; k < 16; ++k)
-              mma_f16_ts(d, tmem + kColQl + 8 * k, desc_sw128(sb + (k >> 2) * kRegion + (k & 3) * 32), id_qk, k > 0);
+              for (int k = 0; k < 16; ++k)
+                mma_f16_ts(d, tmem + kColQl + 8 * k, desc_sw128(sb + (k >> 2) * kRegion + (k & 3) * 32), id_qk, k > 0);
 #pragma unroll
-            for (int k = 0; k < 2; ++k)
-              mma_f16(d, desc_sw64(qr + 32 * k), desc_sw64(sb + 4 * kRegion + 32 * k), id_qk, 1u);
-            tc_commit(&s_full[b]);
+              for (int k = 0; k < 2; ++k)
+                mma_f16(d, desc_sw64(qr + 32 * k), desc_sw64(sb + 4 * kRegion + 32 * k), id_qk, 1u);
+              tc_commit(&s_full[b]);
+            }
+            __syncwarp();
             ++next_qk;
             progress = true;
           }
         }
-        if (next_pv < next_qk && mbar_test(smem_u32(&p_full[next_pv & 1]), (next_pv >> 1) & 1)) {
-          const int m = next_pv, stage = m % kStages;
-          tc_fence_after();
-          const uint32_t sb = smem_u32(stages + stage * kStageBytes);
-          const uint32_t pb = smem_u32(xch + (m & 1) * kXchBytes);
+        if (next_pv < next_qk) {
+          bool ready = false;
+          if (lane == 0) ready = mbar_test(smem_u32(&p_full[next_pv & 1]), (next_pv >> 1) & 1);
+          if (__shfl_sync(0xffffffffu, ready, 0)) {
+            const int m = next_pv, stage = m % kStages;
+            tc_fence_after();
+            const uint32_t sb = smem_u32(stages + stage * kStageBytes);
+            const uint32_t pb = smem_u32(xch + (m & 1) * kXchBytes);
+            if (leader) {
 #pragma unroll
-          for (int j = 0; j < kTok / 16; ++j)
-            mma_f16(tmem + kColO, desc_sw128(pb + 32 * j), desc_sw128_mn(sb + j * 2048, kRegion, 1024), id_pv,
-                    (m > 0 || j > 0) ? 1u : 0u);
-          tc_commit(&pv_done[m & 1]);
-          tc_commit(&kv_empty[stage]);
-          tc_commit_mc(&xch_empty[m & 1], (uint16_t)(1u << peer));  // the peer may send tile m + 2
-          ++next_pv;
-          progress = true;
+              for (int j = 0; j < kTok / 16; ++j)
+                mma_f16(tmem + kColO, desc_sw128(pb + 32 * j), desc_sw128_mn(sb + j * 2048, kRegion, 1024), id_pv,
+                        (m > 0 || j > 0) ? 1u : 0u);
+              tc_commit(&pv_done[m & 1]);
+              tc_commit(&kv_empty[stage]);
+              tc_commit_mc(&xch_empty[m & 1], (uint16_t)(1u << peer));  // the peer may send tile m + 2
+            }
+            __syncwarp();
+            ++next_pv;
+            progress = true;
+          }
         }
         if (progress) {
           idle_since = clock64();
-        } else if (*abort_flag) {
-          ok = false;
-        } else if (clock64() - idle_since > kWaitLimitCycles) {
-          atomicOr(p.err, DSA_DEVERR_TIMEOUT);
-          *abort_flag = 1;
-          ok = false;
         } else {
-          __nanosleep(20);
+          bool quit = false;
+          if (lane == 0) {
+            if (*abort_flag) {
+              quit = true;
+            } else if (clock64() - idle_since > kWaitLimitCycles) {
+              atomicOr(p.err, DSA_DEVERR_TIMEOUT);
+              *abort_flag = 1;
+              quit = true;
+            }
+          }
+          if (__shfl_sync(0xffffffffu, quit, 0)) ok = false;
         }
       }
-      tc_commit(drain);
-      const long long t0 = clock64();
-      while (!mbar_try_wait(smem_u32(drain), 0) && clock64() - t0 < kWaitLimitCycles) {
+      if (leader) {
+        tc_commit(drain);
+        const long long t0 = clock64();
+        while (!mbar_try_wait(smem_u32(drain), 0) && clock64() - t0 < kWaitLimitCycles) {
+        }
       }
+      __syncwarp();
     }
   } else {
     // ============================ softmax + epilogue ==================================
@@ -528,47 +578,38 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       return true;
     };
 
-    // Event loop: load-and-send the next tile a as soon as its logits are ready (that
-    // frees its logit buffer and feeds the peer), else finish the oldest tile b once the
-    // peer's part of it has arrived.  At most two own partials are held: sc for tile b,
-    // sn for tile b + 1.
+    // Order: tile a is sent (logits loaded, partial to the peer) before tile b is
+    // finished, at most one tile ahead; the tile ahead is sent early only when its logits
+    // are already there, so finishing b never waits behind the gathers of b + 1.  sc holds
+    // the own partial of tile b once it is sent, sn that of the tile sent last.  Each step
+    // has one copy in the code; its waits are bounded and give up on abort.
     uint32_t sc[kTok / 2], sn[kTok / 2];
-    int a = 0, b = 0;
-    long long idle_since = clock64();
-    while (ok && b < n_tiles_run) {
-      bool s_ready = false, x_ready = false;
-      if (lane == 0) {
-        s_ready = a < n_tiles_run && a <= b + 1 && mbar_test(smem_u32(&s_full[a & 1]), (a >> 1) & 1);
-        x_ready = b < a && mbar_test(smem_u32(&xch_full[b & 1]), (b >> 1) & 1);
-      }
-      s_ready = __shfl_sync(0xffffffffu, s_ready, 0);
-      x_ready = __shfl_sync(0xffffffffu, x_ready, 0);
-      if (s_ready) {
-        ok = a == b ? load_and_send(a, sc) : load_and_send(a, sn);
-        ++a;
-      } else if (x_ready) {
-        ok = finish(b, sc);
-#pragma unroll
-        for (int j = 0; j < kTok / 2; ++j) sc[j] = sn[j];
-        ++b;
-      } else {
-        // nothing ready: back off; the whole warp gives up (lane 0 decides) on abort or
-        // when nothing has moved for the wait limit
-        bool quit = false;
-        if (lane == 0) {
-          if (*abort_flag) {
-            quit = true;
-          } else if (clock64() - idle_since > kWaitLimitCycles) {
-            atomicOr(p.err, DSA_DEVERR_TIMEOUT);
-            *abort_flag = 1;
-            quit = true;
-          }
+    {
+      int a = 0, b = 0;
+      while (ok && b < n_tiles_run) {
+        bool send = false;
+        if (a == b) {
+          send = true;
+        } else if (a == b + 1 && a < n_tiles_run) {
+          if (lane == 0) send = mbar_test(smem_u32(&s_full[a & 1]), (a >> 1) & 1);
+          send = __shfl_sync(0xffffffffu, send, 0);
         }
-        if (__shfl_sync(0xffffffffu, quit, 0)) ok = false;
-        else __nanosleep(20);
-        continue;
+        if (send) {
+          ok = load_and_send(a, sn);
+          if (a == b) {
+#pragma unroll
+            for (int j = 0; j < kTok / 2; ++j) sc[j] = sn[j];
+          }
+          ++a;
+          continue;
+        }
+        ok = finish(b, sc);
+        ++b;
+        if (a > b) {
+#pragma unroll
+          for (int j = 0; j < kTok / 2; ++j) sc[j] = sn[j];
+        }
       }
-      idle_since = clock64();
     }
     // ---- epilogue: O / l -> this CTA's 256 value dims ----------------------------------
     if (ok && n_tiles_run > 0) {
@@ -602,6 +643,96 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             w.w = pack_bf16x2(__uint_as_float(v[8 * q + 6]) * inv, __uint_as_float(v[8 * q + 7]) * inv);
             dst[q] = w;
           }
+        }
+      }
+    } else if (p.sib_merge) {
+      // Two splits in one cluster of four (rank 2 s + c: split s, value half c).  Split s
+      // finalizes value columns [128 s, 128 s + 128) of this half: it hands the other 128
+      // columns of its O (unnormalized) and every row's (m_ref, l) to its sibling (rank
+      // ^ 2) through distributed shared memory and receives the sibling's in exchange.
+      // The (then idle) stage buffers hold the outbox and the inbox: row h's 16-byte chunk
+      // u at slot u ^ (h & 31) (conflict-free), then the 128 (m, l) pairs.
+      const uint32_t sib = rank ^ 2u;
+      const int s_me = (int)(rank >> 1);
+      uint8_t* outbox = stages;
+      uint8_t* inbox = stages + kSibBytes;
+      if (h == 0) {
+        mbar_arrive_expect_tx(m_full, kSibBytes);                // our inbox may fill from now on
+        mbar_arrive_remote(map_to_rank(smem_u32(m_ready), sib));  // tell the sibling
+      }
+      const int send_col = 128 * (1 - s_me);
+#pragma unroll 1
+      for (int q = 0; q < 4; ++q) {
+        uint32_t v[32];
+        if (n_tiles_run > 0 && ok) {
+          tmem_ld32(tmem + lane_off + kColO + send_col + 32 * q, v);
+          tmem_ld_wait();
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) v[j] = 0u;
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          *(uint4*)(outbox + h * 512 + (((8 * q + u) ^ (h & 31)) << 4)) =
+              make_uint4(v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
+      }
+      ((float2*)(outbox + 128 * 512))[h] = make_float2(ok ? m_ref : -INFINITY, ok ? l : 0.f);
+      fence_proxy_async_smem();  // the bulk copies read it (async proxy)
+      __syncwarp();
+      if (lane == 0 && mbar_wait_cluster(m_ready, 0, abort_flag, p.err)) {  // the sibling's inbox is free
+        // this warp's 32 rows and their (m, l) pairs, one bulk copy each
+        const uint32_t rows = (uint32_t)(quarter * 32);
+        const uint32_t sib_full = map_to_rank(smem_u32(m_full), sib);
+        bulk_copy_to_peer(map_to_rank(smem_u32(inbox) + rows * 512, sib), smem_u32(outbox) + rows * 512, 32 * 512,
+                          sib_full);
+        bulk_copy_to_peer(map_to_rank(smem_u32(inbox) + 128 * 512 + rows * 8, sib),
+                          smem_u32(outbox) + 128 * 512 + rows * 8, 32 * 8, sib_full);
+        bulk_commit();
+      }
+      bool good = true;
+      if (lane == 0) good = mbar_wait(m_full, 0, abort_flag, p.err);
+      good = __shfl_sync(0xffffffffu, good, 0);
+      __syncwarp();
+      if (good && ok) {  // (warp-uniform: the tensor-memory loads below take the whole warp)
+        const float2 ms = ((const float2*)(inbox + 128 * 512))[h];  // the sibling's (m, l)
+        const float m0 = s_me == 0 ? m_ref : ms.x, l0 = s_me == 0 ? l : ms.y;
+        const float m1 = s_me == 0 ? ms.x : m_ref, l1 = s_me == 0 ? ms.y : l;
+        const float mx = fmaxf(m0, m1);
+        const float a0 = mx == -INFINITY || m0 == -INFINITY ? 0.f : exp2f(m0 - mx);
+        const float a1 = mx == -INFINITY || m1 == -INFINITY ? 0.f : exp2f(m1 - mx);
+        const float den = l0 * a0 + l1 * a1;
+        const float inv2 = den > 0.f ? 1.f / den : 0.f;
+        const float w0 = a0 * inv2, w1 = a1 * inv2;  // split 0's and split 1's weight
+#pragma unroll 1
+        for (int q = 0; q < 4; ++q) {
+          uint32_t v[32];
+          if (n_tiles_run > 0) {
+            tmem_ld32(tmem + lane_off + kColO + 128 * s_me + 32 * q, v);
+            tmem_ld_wait();
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] = 0u;
+          }
+          if (!live) continue;
+          uint4* dst = (uint4*)(p.out + ((int64_t)tok * H + h) * kValueDim + 256 * (int)c + 128 * s_me + 32 * q);
+          uint32_t packed[16];
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const uint4 r = *(const uint4*)(inbox + h * 512 + (((8 * q + u) ^ (h & 31)) << 4));
+            const uint32_t rr[4] = {r.x, r.y, r.z, r.w};
+            float o[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const float mine = __uint_as_float(v[4 * u + i]), theirs = __uint_as_float(rr[i]);
+              const float x0 = s_me == 0 ? mine : theirs, x1 = s_me == 0 ? theirs : mine;
+              o[i] = fmaf(x1, w1, x0 * w0);  // the same expression in both CTAs
+            }
+            packed[2 * u] = pack_bf16x2(o[0], o[1]);
+            packed[2 * u + 1] = pack_bf16x2(o[2], o[3]);
+          }
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            dst[j] = make_uint4(packed[4 * j], packed[4 * j + 1], packed[4 * j + 2], packed[4 * j + 3]);
         }
       }
     } else {
@@ -729,13 +860,19 @@ cudaError_t launch_sfa_tc(const SfaParams& p, cudaStream_t s) {
   // the latent cache as [pages * 64 rows, 576]: one-row boxes of 64 elements (latent
   // pieces, 128-byte swizzle) and of 32 elements (rope pieces, 64-byte swizzle)
   CUtensorMap kvmap, ropemap;
+  // Q as [tokens * heads, 576]: boxes of one token's heads, 64 elements (latent, 128-byte
+  // swizzle) and 32 elements (rope, 64-byte swizzle) wide
+  CUtensorMap qmap, qropemap;
   if (!make_tma_2d_sw128(&kvmap, p.kv, (uint64_t)p.tv.num_pages * kPage, 2, kLatentDim, 1, false) ||
-      !make_tma_2d_sw64_rows(&ropemap, p.kv, (uint64_t)p.tv.num_pages * kPage, 2, kLatentDim))
+      !make_tma_2d_sw64_rows(&ropemap, p.kv, (uint64_t)p.tv.num_pages * kPage, 2, kLatentDim) ||
+      !make_tma_2d_sw128(&qmap, p.q, (uint64_t)p.tv.n_tokens * p.n_heads, 2, kLatentDim, p.n_heads, false) ||
+      !make_tma_2d_sw64_rows(&qropemap, p.q, (uint64_t)p.tv.n_tokens * p.n_heads, 2, kLatentDim, p.n_heads))
     return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(sfa_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
   if (e != cudaSuccess) return e;
   dim3 grid(2 * p.n_splits, p.tv.n_tokens);
-  return launch_pdl(sfa_tc_kernel, grid, dim3(kThreads), kSmem, s, kvmap, ropemap, p);
+  return launch_pdl_cluster(sfa_tc_kernel, grid, dim3(kThreads), kSmem, s, p.sib_merge ? 4u : 2u, kvmap, ropemap,
+                            qmap, qropemap, p);
 }
 
 }  // namespace dsa
