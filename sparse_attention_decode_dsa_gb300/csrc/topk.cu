@@ -13,11 +13,11 @@
 //   1. every CTA finds, from that histogram, the bin holding the K-th largest key (its
 //      own keys are loading meanwhile);
 //   2. each CTA counts its keys above that bin and gathers the keys in it (the
-//      candidates);
+//      candidates; each warp into its own slice);
 //   3. each CTA writes its count and its candidates into every CTA's pool (distributed
 //      shared memory); after one cluster barrier every CTA finds the same exact K-th
 //      largest key T among all candidates with an MSB-first radix select over the
-//      remaining 20 bits (8 + 8 + 4), and from the pool alone how many keys > T and
+//      remaining 20 bits (10 + 10), and from the pool alone how many keys > T and
 //      == T each CTA holds, hence where its output starts;
 //   4. each CTA writes, in position order, its keys > T and its share of the first
 //      (K - #{> T}) keys == T (warps own contiguous ranges; block scans place them).
@@ -43,6 +43,7 @@ constexpr int kChunks = 16;                      // 32-position chunks per warp 
 constexpr int kBlock = kThreads * kChunks;       // positions whose keys sit in registers
 constexpr int kLocalCap = 2048;                  // candidates one CTA may gather
 constexpr int kSlot = 256;                       // candidates one CTA may put in the pool
+static_assert(kSlot <= kThreads, "one pool entry per thread and CTA");
 
 // Exclusive prefix sum of v over the CTA in thread order, and the CTA total.
 __device__ __forceinline__ int block_excl_sum(int v, int* buf, int* total) {
@@ -96,6 +97,34 @@ __device__ __forceinline__ void find_bin256(const uint32_t* hist, uint32_t remai
   }
 }
 
+// Same over a 1024-bin histogram: lane l owns bins 1023 - 32 l .. 992 - 32 l.
+__device__ __forceinline__ void find_bin1024(const uint32_t* hist, uint32_t remaining, uint32_t* s_digit,
+                                             uint32_t* s_above) {
+  const int lane = threadIdx.x & 31;
+  uint32_t loc = 0;
+#pragma unroll
+  for (int u = 0; u < 32; ++u) loc += hist[1023 - 32 * lane - ((u + lane) & 31)];  // rotated: no bank conflicts
+  uint32_t incl = loc;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  const uint32_t ex = incl - loc;
+  if (ex < remaining && remaining <= incl) {
+    uint32_t cum = ex;
+    for (int u = 0; u < 32; ++u) {
+      const int bin = 1023 - 32 * lane - u;
+      if (cum + hist[bin] >= remaining) {
+        *s_digit = (uint32_t)bin;
+        *s_above = cum;
+        break;
+      }
+      cum += hist[bin];
+    }
+  }
+}
+
 __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads) topk_cluster_kernel(TopkParams p) {
   cg::cluster_group cluster = cg::this_cluster();
   const int rank = (int)cluster.block_rank();
@@ -122,7 +151,10 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads) top
   __shared__ uint32_t cand_local[kLocalCap];
   __shared__ uint32_t pool[kCluster][kSlot];  // every CTA's candidates
   __shared__ int pool_n[kCluster], pool_above[kCluster];
-  __shared__ uint32_t hist[256];
+  __shared__ uint32_t hist[1024];
+  __shared__ int wcnt[kWarpsPerCta];                 // candidates each warp gathered
+  __shared__ int2 wstat[2][kWarpsPerCta];            // output: each warp's #{> T}, #{== T}
+  __shared__ int red[kWarpsPerCta][2 * kCluster];    // per warp: #{> T}, #{== T} of each CTA's pool
   __shared__ int buf[kWarpsPerCta];
   __shared__ int s_nlocal, s_above_local;
   __shared__ int cnt[2];  // fallback: this CTA's #{key > T}, #{key == T}
@@ -154,10 +186,18 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads) top
   const uint32_t* h12 = p.hist + (int64_t)row * kTopkBins;
   uint32_t hb[16];
   uint32_t local = 0;
+  {
+    const uint4* hp = (const uint4*)(h12 + kTopkBins - 16 * (tid + 1));  // this thread's 16 bins, low to high
 #pragma unroll
-  for (int u = 0; u < 16; ++u) {
-    hb[u] = __ldg(h12 + kTopkBins - 1 - 16 * tid - u);
-    local += hb[u];
+    for (int v = 0; v < 4; ++v) {
+      const uint4 x = __ldg(hp + v);
+      hb[15 - 4 * v] = x.x;
+      hb[14 - 4 * v] = x.y;
+      hb[13 - 4 * v] = x.z;
+      hb[12 - 4 * v] = x.w;
+    }
+#pragma unroll
+    for (int u = 0; u < 16; ++u) local += hb[u];
   }
   if (tid == 0) {
     s_nlocal = 0;
@@ -185,8 +225,11 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads) top
   remaining -= s_above;
 
   // ---- 2. this CTA's keys above the bin (counted) and in it (gathered) ---------------
+  // Warp w gathers into its own slice of kLocalCap / 8 slots (no atomics); the slices
+  // are concatenated when the pool is written.
+  constexpr int kWarpCap = kLocalCap / kWarpsPerCta;
   {
-    int above = 0;
+    int above = 0, nw = 0;
     for (int blk = 0; blk < nblocks; ++blk) {
       if (loaded != blk) {
         load_block(blk);
@@ -199,25 +242,34 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads) top
         above += __popc(__ballot_sync(0xffffffffu, ok && (kr[c] >> 20) > bin));
         const bool in = ok && (kr[c] & mask) == prefix;
         const unsigned bal = __ballot_sync(0xffffffffu, in);
-        if (bal) {
-          int slot = 0;
-          if (lane == 0) slot = atomicAdd(&s_nlocal, __popc(bal));
-          slot = __shfl_sync(0xffffffffu, slot, 0) + __popc(bal & ((1u << lane) - 1u));
-          if (in && slot < kLocalCap) cand_local[slot] = kr[c];
-        }
+        const int slot = nw + __popc(bal & ((1u << lane) - 1u));
+        if (in && slot < kWarpCap) cand_local[warp * kWarpCap + slot] = kr[c];
+        nw += __popc(bal);
       }
     }
-    if (lane == 0) atomicAdd(&s_above_local, above);
+    if (lane == 0) {
+      wcnt[warp] = nw;
+      atomicAdd(&s_above_local, above);
+      atomicAdd(&s_nlocal, nw);
+    }
   }
   __syncthreads();
 
   // ---- 3. pool (every CTA writes its part into every CTA), then one cluster barrier --
   {
-    const int nl = s_nlocal;
-    const int m = min(nl, kSlot);
+    int nl = s_nlocal;
+    for (int w = 0; w < kWarpsPerCta; ++w) nl = wcnt[w] > kWarpCap ? kSlot + 1 : nl;  // a full slice: fall back
+    const int m = nl <= kSlot ? nl : 0;  // (an overfull CTA sends the fallback its count only)
+    // entry j of the pool slot: warp slices in order
+    uint32_t v = 0;
+    if (tid < m) {
+      int j = tid, w = 0;
+      while (j >= wcnt[w]) j -= wcnt[w++];
+      v = cand_local[w * kWarpCap + j];
+    }
     for (int r = 0; r < kCluster; ++r) {
       uint32_t* dst = cluster.map_shared_rank(&pool[rank][0], r);
-      for (int j = tid; j < m; j += kThreads) dst[j] = cand_local[j];
+      if (tid < m) dst[tid] = v;
     }
     if (tid < kCluster) {
       *cluster.map_shared_rank(&pool_n[rank], tid) = nl;
@@ -232,35 +284,54 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads) top
   int taken0, ties0;  // this CTA's first output slot and #{key == T} before it
   uint32_t T;
   if (fast) {
-    // exact K-th largest key among the pooled candidates (all keys of the bin)
+    // exact K-th largest key among the pooled candidates (all keys of the bin): MSB-first
+    // radix select over the remaining 20 bits, 10 at a time
 #pragma unroll 1
-    for (int pass = 0; pass < 3; ++pass) {
-      const int shift = pass == 0 ? 12 : (pass == 1 ? 4 : 0);
-      const uint32_t dmask = pass == 2 ? 0xFu : 0xFFu;
-      hist[tid] = 0;
+    for (int pass = 0; pass < 2; ++pass) {
+      const int shift = pass == 0 ? 10 : 0;
+      const uint32_t dmask = 0x3FFu;
+#pragma unroll
+      for (int u = 0; u < 1024 / kThreads; ++u) hist[tid + u * kThreads] = 0;
       __syncthreads();
+#pragma unroll
       for (int r = 0; r < kCluster; ++r)
-        for (int j = tid; j < pool_n[r]; j += kThreads) {
-          const uint32_t k = pool[r][j];
+        if (tid < pool_n[r]) {
+          const uint32_t k = pool[r][tid];
           if ((k & mask) == prefix) atomicAdd(&hist[(k >> shift) & dmask], 1u);
         }
       __syncthreads();
-      if (warp == 0) find_bin256(hist, remaining, &s_digit, &s_above);
+      if (warp == 0) find_bin1024(hist, remaining, &s_digit, &s_above);
       __syncthreads();
       prefix |= s_digit << shift;
       mask |= dmask << shift;
       remaining -= s_above;
     }
     T = prefix;  // take `remaining` of the keys == T
-    // #{> T} and #{== T} of every CTA from the pool; place this CTA after the ones before
+    // #{> T} and #{== T} in every CTA's pool: one pool entry per thread and CTA, counted
+    // by warp ballots, summed over the warps
+    {
+#pragma unroll
+      for (int r = 0; r < kCluster; ++r) {
+        const bool has = tid < pool_n[r];
+        const uint32_t k = has ? pool[r][tid] : 0u;
+        const int g = __popc(__ballot_sync(0xffffffffu, has && k > T));
+        const int e = __popc(__ballot_sync(0xffffffffu, has && k == T));
+        if (lane == 0) {
+          red[warp][r] = g;
+          red[warp][kCluster + r] = e;
+        }
+      }
+    }
+    __syncthreads();
+    // place this CTA after the ones before it (warp 0; lane r < kCluster speaks for CTA r)
     if (warp == 0) {
       int gt_r = 0, eq_r = 0;
       if (lane < kCluster) {
         gt_r = pool_above[lane];
-        for (int j = 0; j < pool_n[lane]; ++j) {
-          const uint32_t k = pool[lane][j];
-          gt_r += k > T;
-          eq_r += k == T;
+#pragma unroll
+        for (int w = 0; w < kWarpsPerCta; ++w) {
+          gt_r += red[w][lane];
+          eq_r += red[w][kCluster + lane];
         }
       }
       int taken = 0, eq_before = 0;
@@ -359,11 +430,22 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads) top
       gt_w += __popc(__ballot_sync(0xffffffffu, ok && kr[c] > T));
       eq_w += __popc(__ballot_sync(0xffffffffu, ok && kr[c] == T));
     }
-    int eq_tot, tk_tot;
-    // every lane of a warp holds the warp's counts; lane 0 alone enters them in the scans
-    const int eq_before = ties + __shfl_sync(0xffffffffu, block_excl_sum(lane == 0 ? eq_w : 0, buf, &eq_tot), 0);
-    const int take_w = gt_w + max(0, min((int)remaining - eq_before, eq_w));
-    int pos = taken + __shfl_sync(0xffffffffu, block_excl_sum(lane == 0 ? take_w : 0, buf, &tk_tot), 0);
+    // every warp publishes its counts (double-buffered over blocks: one barrier each);
+    // each warp then places itself after the warps before it and sums the block
+    if (lane == 0) wstat[blk & 1][warp] = make_int2(gt_w, eq_w);
+    __syncthreads();
+    int eq_before = ties, pos = taken, eq_tot = 0, tk_tot = 0;
+#pragma unroll
+    for (int w = 0; w < kWarpsPerCta; ++w) {
+      const int2 st = wstat[blk & 1][w];
+      const int tk = st.x + max(0, min((int)remaining - (ties + eq_tot), st.y));
+      if (w < warp) {
+        eq_before += st.y;
+        pos += tk;
+      }
+      eq_tot += st.y;
+      tk_tot += tk;
+    }
     int tie = eq_before;
 #pragma unroll
     for (int c = 0; c < kChunks; ++c) {
