@@ -50,7 +50,9 @@ using namespace sm100;
 
 constexpr int kGatherWarps = 3;                  // warps 0-2 gather (TMA), warp 3 issues MMAs,
 constexpr int kMmaWarp = kGatherWarps;           // warps 4-7 run softmax and the epilogue
-constexpr int kThreads = (kGatherWarps + 5) * 32;
+constexpr int kSendWarp0 = kMmaWarp + 1;          // warps 4-7 load and send the partial logits,
+constexpr int kFinWarp0 = kSendWarp0 + 4;         // warps 8-11 finish tiles (softmax, P) and the epilogue
+constexpr int kThreads = (kFinWarp0 + 4) * 32;
 constexpr int kTok = 64;                         // selected positions per tile
 constexpr int kStages = 4;
 constexpr int kRegion = kTok * 128;              // 64 rows x 128 B
@@ -63,14 +65,15 @@ constexpr uint32_t kColO = 0, kColS = 256, kColQl = 384;  // S buffer b: kColS +
 constexpr int kQRegion = 128 * 128;                // Q latent staging: 4 regions of 128 rows x 128 B
 static_assert(4 * kQRegion <= 2 * kStageBytes, "Q latent staging fits in stage buffers 2-3");
 constexpr int kQropeBytes = 128 * 64;             // Q rope (own 32 dims) [128 rows][64 B], 64-byte swizzle
-constexpr int kSmem = 1024 + kStages * kStageBytes + kQropeBytes + 3 * kXchBytes + kMaxSplitLen * 4 + 512;
+constexpr int kSmem = 1024 + kStages * kStageBytes + kQropeBytes + 4 * kXchBytes + kMaxSplitLen * 4 + 512;
+static_assert(kSmem <= 232448, "shared memory budget");
 // Split merge: 64-column chunks of other splits' partials stream through the (then idle)
 // stage buffers, four at a time.
 constexpr int kMergeCols = 64;
 constexpr int kMergeBuf = kMergeCols * kMaxSfaHeads * 4;  // 32 KB
 static_assert(4 * kMergeBuf <= kStages * kStageBytes, "merge ring fits in the stage buffers");
 static_assert(16 * kMaxSfaHeads * 4 <= 2 * kXchBytes, "split weights fit in the exchange buffers");
-constexpr uint32_t kMergeThreads = 5 * 32;
+constexpr uint32_t kMergeThreads = 5 * 32;                 // gather warp 0 + the four finishing warps
 // Sibling merge (two splits in one cluster): outbox and inbox of 128 rows x 128 f32
 // columns plus 128 (m, l) pairs each, in the stage buffers.
 constexpr uint32_t kSibBytes = 128 * 512 + 128 * 8;
@@ -95,8 +98,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* stages = smem;
   uint8_t* qrope = stages + kStages * kStageBytes;            // Q rope operand
   uint8_t* xch = qrope + kQropeBytes;                         // [2][128 rows][64 fp16] peer partials, then P
-  uint8_t* stg = xch + 2 * kXchBytes;                         // [128 rows][64 fp16] own partial, outbound
-  int32_t* rowid = (int32_t*)(stg + kXchBytes);               // cache row of each slot or -1
+  uint8_t* stg = xch + 2 * kXchBytes;                         // [2][128 rows][64 fp16] own partial, outbound
+  int32_t* rowid = (int32_t*)(stg + 2 * kXchBytes);           // cache row of each slot or -1
   uint64_t* bars = (uint64_t*)(rowid + kMaxSplitLen);
   uint64_t* kv_full = bars;
   uint64_t* kv_empty = kv_full + kStages;
@@ -111,7 +114,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* q_tma = drain + 1;    // Q (own dims) landed in shared memory
   uint64_t* m_ready = q_tma + 1;  // sibling merge: the sibling's inbox is free
   uint64_t* m_full = m_ready + 1; // sibling merge: the sibling's columns arrived
-  uint64_t* mfull = m_full + 1;   // [4]: split merge, a chunk of another split's partial landed
+  uint64_t* stg_full = m_full + 1;  // [2]: the senders staged tile t's own partial in stg[t & 1]
+  uint64_t* stg_free = stg_full + 2; // [2]: the finishers have read it
+  uint64_t* mfull = stg_free + 2;   // [4]: split merge, a chunk of another split's partial landed
   uint64_t* mempty = mfull + 4;  // [4]: the softmax warps are done with that chunk buffer
   uint32_t* tmem_base_s = (uint32_t*)(mempty + 4);
   volatile int* abort_flag = (volatile int*)(tmem_base_s + 1);
@@ -144,6 +149,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(q_tma, 1);
     mbar_init(m_ready, 1);
     mbar_init(m_full, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&stg_full[i], 4);
+      mbar_init(&stg_free[i], 4);
+    }
     for (int i = 0; i < 4; ++i) {
       mbar_init(&mfull[i], 1);
       mbar_init(&mempty[i], 4);
@@ -212,8 +221,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       rowid[j] = rid;
     }
   }
-  if (warp > kMmaWarp) {
-    // each softmax thread moves its head row h of the latent part into tensor memory
+  if (warp >= kSendWarp0 && warp < kFinWarp0) {
+    // each sending thread moves its head row h of the latent part into tensor memory
     // (packed bf16 pairs); rows past the head count are zero, in the rope operand too
     const int quarter = warp & 3;
     const int h = quarter * 32 + lane;  // head row == TMEM lane
@@ -411,35 +420,33 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       __syncwarp();
     }
-  } else {
-    // ============================ softmax + epilogue ==================================
+  } else if (warp < kFinWarp0) {
+    // ============================ senders =============================================
+    // Per tile t: load this CTA's partial logits, scale them by softmax_scale * log2(e)
+    // and round them to fp16 (both CTAs sum the same rounded halves, so their softmax is
+    // identical), free the logit buffer for QK(t + 2), stage them in stg[t & 1] for the
+    // finishing warps and send them (one bulk copy per warp) to the peer's receive buffer
+    // t & 1 once the peer is done with tile t - 2 there.  Every wait is bounded.
     const int quarter = warp & 3;
     const int h = quarter * 32 + lane;  // head row == TMEM lane
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
     const uint32_t warp_rows = (uint32_t)(quarter * 32) * (kTok * 2);  // this warp's 4 KB slice
     const uint32_t xch_peer0 = map_to_rank(smem_u32(xch) + warp_rows, peer);
-    const uint32_t stg_local = smem_u32(stg) + warp_rows;
     const uint32_t xfull_peer0 = map_to_rank(smem_u32(&xch_full[0]), peer);
     const uint32_t myrow = (uint32_t)h * (kTok * 2);
     const uint32_t sw = (uint32_t)(h & 7);
-    float m_ref = -INFINITY, l = 0.f;
-    bool ok = true;
-
-    // Loads this CTA's partial logits of tile t, scales them by softmax_scale * log2(e)
-    // and rounds them to fp16 into `dst` (kept: both CTAs sum the same rounded halves,
-    // so their softmax is identical), frees the logit buffer for QK(t + 2), and stores
-    // sends them (staging + one bulk copy per warp) to the peer's receive buffer t & 1
-    // once the peer is done with tile t - 2 there.  Returns false on abort.
-    auto load_and_send = [&](int t, uint32_t (&dst)[kTok / 2]) -> bool {
+    for (int t = 0; t < n_tiles_run; ++t) {
+      const int bb = t & 1;
       bool good = true;
-      if (lane == 0) good = mbar_wait(&s_full[t & 1], (t >> 1) & 1, abort_flag, p.err);
-      if (!__shfl_sync(0xffffffffu, good, 0)) return false;
+      if (lane == 0) good = mbar_wait(&s_full[bb], (t >> 1) & 1, abort_flag, p.err);
+      if (!__shfl_sync(0xffffffffu, good, 0)) break;
       __syncwarp();
       tc_fence_after();
+      uint32_t dst[kTok / 2];
       {
         uint32_t v0[32], v1[32];
-        tmem_ld32(tmem + lane_off + kColS + 64 * (t & 1), v0);
-        tmem_ld32(tmem + lane_off + kColS + 64 * (t & 1) + 32, v1);
+        tmem_ld32(tmem + lane_off + kColS + 64 * bb, v0);
+        tmem_ld32(tmem + lane_off + kColS + 64 * bb + 32, v1);
         tmem_ld_wait();
         const uint64_t sc2 = f2_pack(p.scale_log2, p.scale_log2);
 #pragma unroll
@@ -454,30 +461,46 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
-        mbar_arrive(&s_free[t & 1]);
-        if (t > 0) bulk_wait_read0();  // staging free again
+        mbar_arrive(&s_free[bb]);
+        if (t >= 2) {
+          // stg[bb] is free once the finishers read tile t - 2 there and its copy did
+          good = mbar_wait(&stg_free[bb], ((t >> 1) & 1) ^ 1, abort_flag, p.err);
+          bulk_wait_read1();
+        }
       }
+      if (!__shfl_sync(0xffffffffu, good, 0)) break;
       __syncwarp();
+      uint8_t* sbuf = stg + bb * kXchBytes;
 #pragma unroll
       for (int u = 0; u < kTok / 8; ++u)
-        *(uint4*)(stg + myrow + (((uint32_t)u ^ sw) << 4)) =
+        *(uint4*)(sbuf + myrow + (((uint32_t)u ^ sw) << 4)) =
             make_uint4(dst[4 * u], dst[4 * u + 1], dst[4 * u + 2], dst[4 * u + 3]);
-      fence_proxy_async_smem();
+      fence_proxy_async_smem();  // the bulk copy reads it (async proxy)
       __syncwarp();
       if (lane == 0) {
-        const int bb = t & 1;
+        mbar_arrive(&stg_full[bb]);
         if (t >= 2) good = mbar_wait_cluster(&xch_empty[bb], ((t >> 1) & 1) ^ 1, abort_flag, p.err);
         if (good) {
-          bulk_copy_to_peer(xch_peer0 + bb * kXchBytes, stg_local, 32 * kTok * 2, xfull_peer0 + bb * 8);
+          bulk_copy_to_peer(xch_peer0 + bb * kXchBytes, smem_u32(sbuf) + warp_rows, 32 * kTok * 2,
+                            xfull_peer0 + bb * 8);
           bulk_commit();
         }
       }
-      return __shfl_sync(0xffffffffu, good, 0);
-    };
+      if (!__shfl_sync(0xffffffffu, good, 0)) break;
+    }
+  } else {
+    // ============================ finishers + epilogue ================================
+    const int quarter = warp & 3;
+    const int h = quarter * 32 + lane;  // head row == TMEM lane
+    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    const uint32_t myrow = (uint32_t)h * (kTok * 2);
+    const uint32_t sw = (uint32_t)(h & 7);
+    float m_ref = -INFINITY, l = 0.f;
+    bool ok = true;
 
-    // Finishes tile n from this CTA's rounded partial logits `own`: adds the peer's part,
-    // runs the online softmax and stores P.  Returns false on abort.
-    auto finish = [&](int n, const uint32_t (&own)[kTok / 2]) -> bool {
+    // Finishes tile n: adds this CTA's rounded partial logits (staged by the senders) and
+    // the peer's, runs the online softmax and stores P.  Returns false on abort.
+    auto finish = [&](int n) -> bool {
       bool good = true;
       const int bb = n & 1;
       const int32_t* rt = rowid + n * kTok;
@@ -486,22 +509,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) {
         good = mbar_wait(&xch_full[bb], (n >> 1) & 1, abort_flag, p.err);
         if (good && h == 0 && n + 2 < n_tiles_run) mbar_arrive_expect_tx(&xch_full[bb], kXchBytes);  // tile n + 2
+        if (good) good = mbar_wait(&stg_full[bb], (n >> 1) & 1, abort_flag, p.err);
       }
       if (!__shfl_sync(0xffffffffu, good, 0)) return false;
       __syncwarp();
       const uint8_t* recv = xch + bb * kXchBytes + myrow;
+      const uint8_t* mine = stg + bb * kXchBytes + myrow;
       float s[kTok];  // full scaled logits of tile n: widen the peer's half, add ours
 #pragma unroll
       for (int u = 0; u < kTok / 8; ++u) {
         const uint4 r = *(const uint4*)(recv + (((uint32_t)u ^ sw) << 4));
+        const uint4 o = *(const uint4*)(mine + (((uint32_t)u ^ sw) << 4));
         const uint32_t rr[4] = {r.x, r.y, r.z, r.w};
+        const uint32_t oo[4] = {o.x, o.y, o.z, o.w};
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           f16x2_to_f32(rr[i], s[8 * u + 2 * i], s[8 * u + 2 * i + 1]);
-          add_f16x2_to(own[4 * u + i], s[8 * u + 2 * i], s[8 * u + 2 * i + 1]);
+          add_f16x2_to(oo[i], s[8 * u + 2 * i], s[8 * u + 2 * i + 1]);
         }
       }
       __syncwarp();
+      if (lane == 0) mbar_arrive(&stg_free[bb]);  // the senders may stage tile n + 2 there
       // online softmax (base 2), masked positions get no weight
       if ((vlo & vhi) != 0xffffffffu) {
 #pragma unroll
@@ -578,39 +606,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       return true;
     };
 
-    // Order: tile a is sent (logits loaded, partial to the peer) before tile b is
-    // finished, at most one tile ahead; the tile ahead is sent early only when its logits
-    // are already there, so finishing b never waits behind the gathers of b + 1.  sc holds
-    // the own partial of tile b once it is sent, sn that of the tile sent last.  Each step
-    // has one copy in the code; its waits are bounded and give up on abort.
-    uint32_t sc[kTok / 2], sn[kTok / 2];
-    {
-      int a = 0, b = 0;
-      while (ok && b < n_tiles_run) {
-        bool send = false;
-        if (a == b) {
-          send = true;
-        } else if (a == b + 1 && a < n_tiles_run) {
-          if (lane == 0) send = mbar_test(smem_u32(&s_full[a & 1]), (a >> 1) & 1);
-          send = __shfl_sync(0xffffffffu, send, 0);
-        }
-        if (send) {
-          ok = load_and_send(a, sn);
-          if (a == b) {
-#pragma unroll
-            for (int j = 0; j < kTok / 2; ++j) sc[j] = sn[j];
-          }
-          ++a;
-          continue;
-        }
-        ok = finish(b, sc);
-        ++b;
-        if (a > b) {
-#pragma unroll
-          for (int j = 0; j < kTok / 2; ++j) sc[j] = sn[j];
-        }
-      }
-    }
+    for (int n = 0; ok && n < n_tiles_run; ++n) ok = finish(n);
     // ---- epilogue: O / l -> this CTA's 256 value dims ----------------------------------
     if (ok && n_tiles_run > 0) {
       if (lane == 0) ok = mbar_wait(&pv_done[(n_tiles_run - 1) & 1], ((n_tiles_run - 1) >> 1) & 1, abort_flag, p.err);
@@ -764,7 +760,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // finished last; it then resets the counter for the next call.  Both barriers are
       // passed by warp 0 and all four softmax warps whatever happened before.
       named_bar_sync(1, kMergeThreads);
-      if (warp == kMmaWarp + 1 && lane == 0) {
+      if (warp == kFinWarp0 && lane == 0) {
         const uint32_t prev = atomicAdd(p.merge_cnt + tok * 2 + c, 1u);
         *last_s = prev == (uint32_t)(p.n_splits - 1);
       }
@@ -838,7 +834,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
-        if (warp == kMmaWarp + 1 && lane == 0) p.merge_cnt[tok * 2 + c] = 0u;
+        if (warp == kFinWarp0 && lane == 0) p.merge_cnt[tok * 2 + c] = 0u;
       }
     }
   }

@@ -285,6 +285,8 @@ __device__ __forceinline__ void fence_proxy_async_global() {
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;\n" ::: "memory"); }
 // Waits until every committed bulk copy of this thread has finished reading its source.
 __device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;\n" ::: "memory"); }
+// ... all but the most recent one.
+__device__ __forceinline__ void bulk_wait_read1() { asm volatile("cp.async.bulk.wait_group.read 1;\n" ::: "memory"); }
 
 // ---- paired fp32 arithmetic (one instruction for two lanes of a 64-bit register pair) --
 __device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
