@@ -273,13 +273,26 @@ dsa_status_t run_indexer(const dsa_indexer_args_t* a, const dsa_index_cache_t* c
     // sequence gains nothing from it.)
     const bool identity = a->act == DSA_ACT_IDENTITY;
     const bool split = false;
+    // Query rows that share one sequence (prefill) share their keys: with bf16 keys and
+    // the identity activation, blocks of consecutive rows take each K tile together.
+    bool one_seq = tk->token_seq ? true : pg->batch == 1;
+    if (tk->token_seq)
+      for (int32_t i = 1; i < tk->n_tokens && one_seq; ++i) one_seq = tk->token_seq_host[i] == tk->token_seq_host[0];
+    const bool blocked = identity && c->dtype == DSA_BF16 && c->scale_kind == DSA_SCALE_NONE &&
+                         (c->dim == 64 || c->dim == 128) && one_seq && tk->n_tokens >= 2 * kBlockRows;
     const bool stream = !split && identity && c->dtype == DSA_E4M3 && c->scale_kind == DSA_SCALE_PER_TOKEN_F32 &&
                         score_stream_supported(a->act, c->dim);
     const bool tc = score_tc_supported(c->dtype, c->dim, a->n_heads);
     tr.begin();
     cudaError_t e = cudaSuccess;
-    if (split) {
-      e = launch_qsplit(sp, qsplit, wsplit, s);
+    if (blocked) {
+      e = launch_qsplit(sp, qsplit, nullptr, 3, s);
+      ScoreParams sp2 = sp;
+      sp2.q = qsplit;
+      sp2.q_dep = 1;
+      if (e == cudaSuccess) e = launch_score_tc_blocked(sp2, s);
+    } else if (split) {
+      e = launch_qsplit(sp, qsplit, wsplit, kSplitQueryHeads, s);
       ScoreParams sp2 = sp;
       sp2.q = qsplit;
       sp2.head_w = wsplit;

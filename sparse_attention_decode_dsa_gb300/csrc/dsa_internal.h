@@ -130,10 +130,18 @@ cudaError_t launch_score_tc(const ScoreParams& p, dsa_dtype_t dt, dsa_scale_t sk
 bool score_stream_supported(dsa_act_t act, int dim);
 // q~ scratch: [n_tokens, dim] f32 in the workspace
 cudaError_t launch_score_stream(const ScoreParams& p, dsa_dtype_t dt, dsa_scale_t sk, float* qt, cudaStream_t s);
-// bf16, identity activation: the head-collapsed query split into 3 bf16 terms, as 16
-// heads [n_tokens, 16, dim] with weights [n_tokens, 16] (for the tensor-core kernel)
+// bf16, identity activation: the head-collapsed query split into 3 bf16 terms, laid out
+// as `stride` rows per token [n_tokens, stride, dim] (terms, then zero rows) with weights
+// [n_tokens, stride] (1, 1, 1, 0, ...; skipped when ws is null).  stride 16: 16 "heads"
+// of one token for the per-row tensor-core kernel; stride 3: consecutive tokens' terms
+// back to back, for the row-blocked kernel.
 constexpr int kSplitQueryHeads = 16;
-cudaError_t launch_qsplit(const ScoreParams& p, uint16_t* qs, float* ws, cudaStream_t s);
+cudaError_t launch_qsplit(const ScoreParams& p, uint16_t* qs, float* ws, int stride, cudaStream_t s);
+// The row-blocked tensor-core score kernel: every token belongs to one sequence (host
+// checked); blocks of kBlockRows consecutive rows share each K tile; p.q is the stride-3
+// split query.
+constexpr int kBlockRows = 21;
+cudaError_t launch_score_tc_blocked(const ScoreParams& p, cudaStream_t s);
 cudaError_t launch_topk(const TopkParams& p, int32_t max_visible, cudaStream_t s);
 cudaError_t launch_sfa_tc(const SfaParams& p, cudaStream_t s);
 cudaError_t launch_clear(void* p, size_t bytes, cudaStream_t s);  // bytes: multiple of 16

@@ -56,15 +56,16 @@ __global__ void __launch_bounds__(kQtThreads) qtilde_kernel(ScoreParams p, float
 // bf16 keys on the tensor cores: q~ split exactly into three bf16 terms
 // q~ = hi + mid + lo (each rounding leaves a residual that is exact in f32 and needs at
 // most 8 fewer significant bits, so three terms hold all 24 bits of an f32) and handed
-// to the per-head tensor-core score kernel as 16 "heads" (the three terms, 13 zero rows)
-// with weights (1, 1, 1, 0, ...): the same kernel, a quarter of its MMA and epilogue work.
+// to the tensor-core score kernel, either as 16 "heads" of one token (the three terms,
+// 13 zero rows, weights (1, 1, 1, 0, ...)) or, for rows that share their keys, three rows
+// per token back to back so that one MMA serves 21 consecutive tokens.
 // 512 threads per query token: thread (quarter j, dim d) sums 16 heads; the four quarter
 // sums are added in order.
 constexpr int kSplitHeads = 16;
 constexpr int kSplitThreads = 512;
 
 template <int D>
-__global__ void __launch_bounds__(kSplitThreads) qsplit_kernel(ScoreParams p, uint16_t* qs, float* ws) {
+__global__ void __launch_bounds__(kSplitThreads) qsplit_kernel(ScoreParams p, uint16_t* qs, float* ws, int stride) {
   pdl_trigger();
   pdl_wait();  // the split query lives in workspace that the previous pass may still use
   const int row = blockIdx.x;
@@ -91,14 +92,13 @@ __global__ void __launch_bounds__(kSplitThreads) qsplit_kernel(ScoreParams p, ui
     const float r1 = qt - bf16_to_f32(hi);
     const uint16_t mid = f32_to_bf16_rne(r1);
     const uint16_t lo = f32_to_bf16_rne(r1 - bf16_to_f32(mid));
-    uint16_t* o = qs + (int64_t)row * kSplitHeads * D + d;
+    uint16_t* o = qs + (int64_t)row * stride * D + d;
     o[0] = hi;
     o[D] = mid;
     o[2 * D] = lo;
-#pragma unroll
-    for (int h = 3; h < kSplitHeads; ++h) o[h * D] = 0;
+    for (int h = 3; h < stride; ++h) o[h * D] = 0;
   }
-  if (threadIdx.x < kSplitHeads) ws[(int64_t)row * kSplitHeads + threadIdx.x] = threadIdx.x < 3 ? 1.f : 0.f;
+  if (ws && threadIdx.x < stride) ws[(int64_t)row * stride + threadIdx.x] = threadIdx.x < 3 ? 1.f : 0.f;
 }
 
 // 16 bytes of a key row -> 8 (bf16) or 16 (e4m3) f32 values, exactly.
@@ -272,9 +272,9 @@ cudaError_t launch_stream(const ScoreParams& p, float* qt, cudaStream_t s) {
 
 bool score_stream_supported(dsa_act_t act, int dim) { return act == DSA_ACT_IDENTITY && (dim == 64 || dim == 128); }
 
-cudaError_t launch_qsplit(const ScoreParams& p, uint16_t* qs, float* ws, cudaStream_t s) {
-  return p.dim == 64 ? launch_pdl(qsplit_kernel<64>, dim3(p.tv.n_tokens), dim3(kSplitThreads), 0, s, p, qs, ws)
-                     : launch_pdl(qsplit_kernel<128>, dim3(p.tv.n_tokens), dim3(kSplitThreads), 0, s, p, qs, ws);
+cudaError_t launch_qsplit(const ScoreParams& p, uint16_t* qs, float* ws, int stride, cudaStream_t s) {
+  return p.dim == 64 ? launch_pdl(qsplit_kernel<64>, dim3(p.tv.n_tokens), dim3(kSplitThreads), 0, s, p, qs, ws, stride)
+                     : launch_pdl(qsplit_kernel<128>, dim3(p.tv.n_tokens), dim3(kSplitThreads), 0, s, p, qs, ws, stride);
 }
 
 cudaError_t launch_score_stream(const ScoreParams& p, dsa_dtype_t dt, dsa_scale_t sk, float* qt, cudaStream_t s) {

@@ -54,7 +54,7 @@ struct Cfg {
   static constexpr int kTmemCols = kNumAcc * kAccCols;
   static constexpr uint32_t kFmt = KIND == 0 ? 1u : 0u;    // bf16 / e4m3
   static constexpr int kSmem = 1024 /*align*/ + kStages * kStageBytes + 2 * kQSlotBytes + 4096 /*bars*/ +
-                               3 * (kMaxRowsPerLaunch + 1) * 4 + 4 * kEpiGroups * (64 + 64 * 4 + 4) * 4;
+                               4 * (kMaxRowsPerLaunch + 1) * 4 + 4 * kEpiGroups * (64 + 64 * 4 + 4) * 4;
 };
 
 struct TcArgs {
@@ -63,7 +63,10 @@ struct TcArgs {
   int32_t nrows;  // rows in this launch
 };
 
-template <int KIND, int D>
+// BLK: row-blocked (bf16, identity activation, one sequence): an item is a block of
+// kBlockRows consecutive rows and one tile; the MMA's N = 64 columns are the blocks' rows'
+// three split-query terms (p.q: [rows, 3, D]).
+template <int KIND, int D, bool BLK>
 __global__ void __launch_bounds__(kTcThreads, 1)
     score_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap qmap,
                     const TcArgs a) {
@@ -89,10 +92,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   uint64_t* drain = q_empty + 2;
   uint32_t* tmem_base_s = (uint32_t*)(drain + 1);
   volatile int* abort_flag = (volatile int*)(tmem_base_s + 1);
-  int* prefix = (int*)(bars + 512);                 // [nrows + 1] item prefix
+  int* prefix = (int*)(bars + 512);                 // [units + 1] item prefix (unit: a row, or a block)
   int* rowb = prefix + kMaxRowsPerLaunch + 1;       // batch row of each query row
-  int* rown = rowb + kMaxRowsPerLaunch + 1;         // visible count of each query row
-  float* epi = (float*)(rown + kMaxRowsPerLaunch + 1);  // per epilogue warp: w[64], qs[64*4], qtok
+  int* rown = rowb + kMaxRowsPerLaunch + 1;         // visible count of each unit
+  int* rn = rown + kMaxRowsPerLaunch + 1;           // visible count of each query row (blocks)
+  float* epi = (float*)(rn + kMaxRowsPerLaunch + 1);  // per epilogue warp: w[64], qs[64*4], qtok
 
   // ---- set-up: barriers, TMEM, per-row metadata and this CTA's item range ----------
   if (tid == 0) {
@@ -119,33 +123,46 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     tmem_relinquish();
   }
   // visible counts and tiles of every row, then an exclusive scan (one warp)
+  const int nunits = BLK ? (a.nrows + kBlockRows - 1) / kBlockRows : a.nrows;
   for (int r = tid; r < a.nrows; r += kTcThreads) {
     int b, n;
     resolve_token(p.tv, a.row0 + r, &b, &n, p.err);
     rowb[r] = b;
-    rown[r] = n;
-    prefix[r + 1] = (n + kTileTok - 1) / kTileTok;
+    rn[r] = n;
+    if (!BLK) {
+      rown[r] = n;
+      prefix[r + 1] = (n + kTileTok - 1) / kTileTok;
+    }
+  }
+  if (BLK) {
+    __syncthreads();
+    for (int u = tid; u < nunits; u += kTcThreads) {  // a block sees its rows' widest window
+      int m = 0;
+      for (int r = u * kBlockRows; r < a.nrows && r < (u + 1) * kBlockRows; ++r) m = max(m, rn[r]);
+      rown[u] = m;
+      prefix[u + 1] = (m + kTileTok - 1) / kTileTok;
+    }
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   if (warp == 0) {
     int carry = 0;
-    for (int base = 0; base < a.nrows; base += 32) {
+    for (int base = 0; base < nunits; base += 32) {
       const int r = base + lane;
-      int v = r < a.nrows ? prefix[r + 1] : 0;
+      int v = r < nunits ? prefix[r + 1] : 0;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
         const int u = __shfl_up_sync(0xffffffffu, v, o);
         if (lane >= o) v += u;
       }
-      if (r < a.nrows) prefix[r + 1] = carry + v;
+      if (r < nunits) prefix[r + 1] = carry + v;
       carry += __shfl_sync(0xffffffffu, v, 31);
     }
     if (lane == 0) prefix[0] = 0;
   }
   __syncthreads();
-  const int total = prefix[a.nrows];
+  const int total = prefix[nunits];
   const int it_begin = (int)((int64_t)total * blockIdx.x / gridDim.x);
   const int it_end = (int)((int64_t)total * (blockIdx.x + 1) / gridDim.x);
   const uint32_t tmem_base = *tmem_base_s;
@@ -169,12 +186,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           mbar_arrive_expect_tx(&q_full[slot], C::kRegions * H * 128);
           const uint32_t qdst = smem_u32(qslots + slot * C::kQSlotBytes);
           for (int g = 0; g < C::kRegions; ++g)
-            tma_load_2d(qdst + g * C::kRegionQBytes, &qmap, &q_full[slot], g * C::kBoxInner, (a.row0 + r) * H);
+            tma_load_2d(qdst + g * C::kRegionQBytes, &qmap, &q_full[slot], g * C::kBoxInner,
+                        BLK ? 3 * (a.row0 + r * kBlockRows) : (a.row0 + r) * H);
           ++qcount;
         }
         if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.err)) break;
         const int tile = it - prefix[r];
-        const int b = rowb[r];
+        const int b = rowb[BLK ? r * kBlockRows : r];
         const int npages = (rown[r] + kPage - 1) / kPage;
         int pg[2] = {-1, -1};
         uint32_t bytes = 0;
@@ -272,6 +290,47 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int grp = (warp - 2) / 4;
     const int quarter = warp & 3;
     const int i = quarter * 32 + lane;
+    if constexpr (BLK) {
+      // token i of the tile against every row of the block: column 3 j + e is term e of
+      // row j, the row's score their sum; each row masks its own causal window
+      int r = 0;
+      for (int it = it_begin; it < it_end; ++it) {
+        while (prefix[r + 1] <= it) ++r;
+        const int n = it - it_begin;
+        if (n % kEpiGroups != grp) continue;
+        const int acc = n % C::kNumAcc;
+        const uint32_t acc_phase = (uint32_t)(n / C::kNumAcc) & 1u;
+        const int t = (it - prefix[r]) * kTileTok + i;
+        const int r0 = r * kBlockRows;
+        const int nb = min(kBlockRows, a.nrows - r0);
+        const int pg = t < rown[r] ? physical_page(p.tv, rowb[r0], t >> 6, nullptr) : -1;
+        bool ok = true;
+        if (lane == 0) ok = mbar_wait(&acc_full[acc], acc_phase, abort_flag, p.err);
+        if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+        __syncwarp();
+        tc_fence_after();
+        const uint32_t tbase = tmem_base + ((uint32_t)(quarter * 32) << 16) + acc * C::kAccCols;
+        uint32_t v0[32], v1[32];
+        tmem_ld32(tbase, v0);
+        tmem_ld32(tbase + 32, v1);
+        tmem_ld_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&acc_empty[acc]);
+#pragma unroll
+        for (int j = 0; j < kBlockRows; ++j) {
+          if (j < nb && t < rn[r0 + j]) {
+            const float c0 = __uint_as_float(3 * j < 32 ? v0[(3 * j) & 31] : v1[(3 * j) & 31]);
+            const float c1 = __uint_as_float(3 * j + 1 < 32 ? v0[(3 * j + 1) & 31] : v1[(3 * j + 1) & 31]);
+            const float c2 = __uint_as_float(3 * j + 2 < 32 ? v0[(3 * j + 2) & 31] : v1[(3 * j + 2) & 31]);
+            const float v = pg >= 0 ? (c0 + c1) + c2 : -INFINITY;
+            const int64_t grow = a.row0 + r0 + j;
+            p.scores[grow * p.score_stride + t] = v;
+            atomicAdd(p.hist + grow * kTopkBins + (score_key(v) >> 20), 1u);
+          }
+        }
+      }
+    } else {
     float* w_s = epi + (warp - 2) * (64 + 64 * 4 + 4);
     float* qs_s = w_s + 64;             // [h][g] query group scales (MX)
     int r = 0, cur_row = -1;
@@ -378,6 +437,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         atomicAdd(p.hist + (int64_t)grow * kTopkBins + (score_key(v) >> 20), 1u);
       }
     }
+    }  // per-row epilogue
   }
 
   // ---- tear-down ---------------------------------------------------------------------
@@ -390,26 +450,29 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 }
 
 // ---- host side: launch ---------------------------------------------------------------
-template <int KIND, int D>
+template <int KIND, int D, bool BLK = false>
 cudaError_t launch_tc(const ScoreParams& p, cudaStream_t s) {
   using C = Cfg<KIND, D>;
   static_assert(C::kSmem <= 232448, "shared memory budget");
   CUtensorMap kmap, qmap;
   if (!make_tma_2d_sw128(&kmap, p.k, (uint64_t)p.tv.num_pages * kPage, C::kElem, D, kPage)) return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(score_tc_kernel<KIND, D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaError_t e = cudaFuncSetAttribute(score_tc_kernel<KIND, D, BLK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        C::kSmem);
   if (e != cudaSuccess) return e;
   int dev = 0, sms = 0;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  if (!make_tma_2d_sw128(&qmap, p.q, (uint64_t)p.tv.n_tokens * p.n_heads, C::kElem, D, p.n_heads))
+  // the query: [tokens * heads, D], boxes of one token's heads; blocked: [tokens * 3, D],
+  // boxes of 64 rows (a block's 21 tokens x 3 terms, and one spare row)
+  if (!make_tma_2d_sw128(&qmap, p.q, (uint64_t)p.tv.n_tokens * (BLK ? 3 : p.n_heads), C::kElem, D,
+                         BLK ? 64 : p.n_heads))
     return cudaErrorInvalidValue;
   for (int row0 = 0; row0 < p.tv.n_tokens; row0 += kMaxRowsPerLaunch) {
     TcArgs a;
     a.p = p;
     a.row0 = row0;
     a.nrows = p.tv.n_tokens - row0 < kMaxRowsPerLaunch ? p.tv.n_tokens - row0 : kMaxRowsPerLaunch;
-    e = launch_pdl(score_tc_kernel<KIND, D>, dim3(sms), dim3(kTcThreads), C::kSmem, s, kmap, qmap, a);
+    e = launch_pdl(score_tc_kernel<KIND, D, BLK>, dim3(sms), dim3(kTcThreads), C::kSmem, s, kmap, qmap, a);
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;
@@ -421,6 +484,12 @@ bool score_tc_supported(dsa_dtype_t dt, int dim, int n_heads) {
   if (n_heads < 1 || n_heads > 64) return false;
   if (dt == DSA_BF16) return dim == 64 || dim == 128;
   return dim == 128;
+}
+
+cudaError_t launch_score_tc_blocked(const ScoreParams& p, cudaStream_t s) {
+  ScoreParams b = p;
+  b.n_heads = 64;  // N: 21 rows x 3 terms + 1
+  return p.dim == 64 ? launch_tc<0, 64, true>(b, s) : launch_tc<0, 128, true>(b, s);
 }
 
 cudaError_t launch_score_tc(const ScoreParams& p, dsa_dtype_t dt, dsa_scale_t sk, cudaStream_t s) {
