@@ -8,8 +8,9 @@
 //
 // Scores are compared through an order-preserving 32-bit key (score_key).  The scoring
 // pass already counted, per row, how many keys fall in each of the 4096 bins of their
-// top 12 bits (kept in the workspace).  A cluster of 8 CTAs shares each row, CTA r
-// owning the r-th eighth of its positions:
+// top 12 bits (kept in the workspace).  A cluster of C CTAs (1, 2, 4 or 8: the fewest
+// that keep a CTA's share of the longest row within 4096 keys) shares each row, CTA r
+// owning the r-th C-th of its positions:
 //   1. every CTA finds, from that histogram, the bin holding the K-th largest key (its
 //      own keys are loading meanwhile);
 //   2. each CTA counts its keys above that bin and gathers the keys in it (the
@@ -36,14 +37,12 @@ namespace dsa {
 
 namespace {
 
-constexpr int kCluster = 8;                      // CTAs per row
 constexpr int kThreads = 256;
 constexpr int kWarpsPerCta = kThreads / 32;
 constexpr int kChunks = 16;                      // 32-position chunks per warp per block
 constexpr int kBlock = kThreads * kChunks;       // positions whose keys sit in registers
 constexpr int kLocalCap = 2048;                  // candidates one CTA may gather
-constexpr int kSlot = 256;                       // candidates one CTA may put in the pool
-static_assert(kSlot <= kThreads, "one pool entry per thread and CTA");
+constexpr int kPoolTotal = 2048;                 // pooled candidates of a row (kSlot per CTA)
 
 // Exclusive prefix sum of v over the CTA in thread order, and the CTA total.
 __device__ __forceinline__ int block_excl_sum(int v, int* buf, int* total) {
@@ -125,7 +124,9 @@ __device__ __forceinline__ void find_bin1024(const uint32_t* hist, uint32_t rema
   }
 }
 
+template <int kCluster>  // CTAs per row
 __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads) topk_cluster_kernel(TopkParams p) {
+  constexpr int kSlot = kPoolTotal / kCluster;  // candidates one CTA may put in the pool
   cg::cluster_group cluster = cg::this_cluster();
   const int rank = (int)cluster.block_rank();
   const int row = blockIdx.y;
@@ -261,15 +262,24 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads) top
     for (int w = 0; w < kWarpsPerCta; ++w) nl = wcnt[w] > kWarpCap ? kSlot + 1 : nl;  // a full slice: fall back
     const int m = nl <= kSlot ? nl : 0;  // (an overfull CTA sends the fallback its count only)
     // entry j of the pool slot: warp slices in order
-    uint32_t v = 0;
-    if (tid < m) {
-      int j = tid, w = 0;
-      while (j >= wcnt[w]) j -= wcnt[w++];
-      v = cand_local[w * kWarpCap + j];
-    }
-    for (int r = 0; r < kCluster; ++r) {
-      uint32_t* dst = cluster.map_shared_rank(&pool[rank][0], r);
-      if (tid < m) dst[tid] = v;
+    if constexpr (kSlot <= kThreads) {
+      uint32_t v = 0;
+      if (tid < m) {
+        int j = tid, w = 0;
+        while (j >= wcnt[w]) j -= wcnt[w++];
+        v = cand_local[w * kWarpCap + j];
+      }
+      for (int r = 0; r < kCluster; ++r) {
+        uint32_t* dst = cluster.map_shared_rank(&pool[rank][0], r);
+        if (tid < m) dst[tid] = v;
+      }
+    } else {
+      for (int j0 = tid; j0 < m; j0 += kThreads) {
+        int j = j0, w = 0;
+        while (j >= wcnt[w]) j -= wcnt[w++];
+        const uint32_t v = cand_local[w * kWarpCap + j];
+        for (int r = 0; r < kCluster; ++r) *cluster.map_shared_rank(&pool[rank][j0], r) = v;
+      }
     }
     if (tid < kCluster) {
       *cluster.map_shared_rank(&pool_n[rank], tid) = nl;
@@ -293,12 +303,20 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads) top
 #pragma unroll
       for (int u = 0; u < 1024 / kThreads; ++u) hist[tid + u * kThreads] = 0;
       __syncthreads();
+      if constexpr (kSlot <= kThreads) {  // one pool entry per thread and CTA
 #pragma unroll
-      for (int r = 0; r < kCluster; ++r)
-        if (tid < pool_n[r]) {
-          const uint32_t k = pool[r][tid];
-          if ((k & mask) == prefix) atomicAdd(&hist[(k >> shift) & dmask], 1u);
-        }
+        for (int r = 0; r < kCluster; ++r)
+          if (tid < pool_n[r]) {
+            const uint32_t k = pool[r][tid];
+            if ((k & mask) == prefix) atomicAdd(&hist[(k >> shift) & dmask], 1u);
+          }
+      } else {
+        for (int r = 0; r < kCluster; ++r)
+          for (int j = tid; j < pool_n[r]; j += kThreads) {
+            const uint32_t k = pool[r][j];
+            if ((k & mask) == prefix) atomicAdd(&hist[(k >> shift) & dmask], 1u);
+          }
+      }
       __syncthreads();
       if (warp == 0) find_bin1024(hist, remaining, &s_digit, &s_above);
       __syncthreads();
@@ -307,15 +325,28 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads) top
       remaining -= s_above;
     }
     T = prefix;  // take `remaining` of the keys == T
-    // #{> T} and #{== T} in every CTA's pool: one pool entry per thread and CTA, counted
-    // by warp ballots, summed over the warps
+    // #{> T} and #{== T} in every CTA's pool: counted per thread, summed over each warp
+    // and then over the warps
     {
 #pragma unroll
       for (int r = 0; r < kCluster; ++r) {
-        const bool has = tid < pool_n[r];
-        const uint32_t k = has ? pool[r][tid] : 0u;
-        const int g = __popc(__ballot_sync(0xffffffffu, has && k > T));
-        const int e = __popc(__ballot_sync(0xffffffffu, has && k == T));
+        int g, e;
+        if constexpr (kSlot <= kThreads) {
+          const bool has = tid < pool_n[r];
+          const uint32_t k = has ? pool[r][tid] : 0u;
+          g = __popc(__ballot_sync(0xffffffffu, has && k > T));
+          e = __popc(__ballot_sync(0xffffffffu, has && k == T));
+        } else {
+          g = 0;
+          e = 0;
+          for (int j = tid; j < pool_n[r]; j += kThreads) {
+            const uint32_t k = pool[r][j];
+            g += k > T;
+            e += k == T;
+          }
+          g = __reduce_add_sync(0xffffffffu, g);
+          e = __reduce_add_sync(0xffffffffu, e);
+        }
         if (lane == 0) {
           red[warp][r] = g;
           red[warp][kCluster + r] = e;
@@ -471,9 +502,15 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads) top
 }  // namespace
 
 cudaError_t launch_topk(const TopkParams& p, int32_t max_visible, cudaStream_t s) {
-  (void)max_visible;
-  dim3 grid(kCluster, p.tv.n_tokens);
-  return launch_pdl(topk_cluster_kernel, grid, dim3(kThreads), 0, s, p);
+  // the fewest CTAs per row that keep each CTA's share of the longest row within one
+  // block of keys held in registers (more for longer rows, at most 8)
+  const int cl = max_visible <= kBlock ? 1 : max_visible <= 2 * kBlock ? 2 : max_visible <= 4 * kBlock ? 4 : 8;
+  switch (cl) {
+    case 1: return launch_pdl(topk_cluster_kernel<1>, dim3(1, p.tv.n_tokens), dim3(kThreads), 0, s, p);
+    case 2: return launch_pdl(topk_cluster_kernel<2>, dim3(2, p.tv.n_tokens), dim3(kThreads), 0, s, p);
+    case 4: return launch_pdl(topk_cluster_kernel<4>, dim3(4, p.tv.n_tokens), dim3(kThreads), 0, s, p);
+    default: return launch_pdl(topk_cluster_kernel<8>, dim3(8, p.tv.n_tokens), dim3(kThreads), 0, s, p);
+  }
 }
 
 }  // namespace dsa
