@@ -133,8 +133,13 @@ EMPTY_AND_SHORT = Spec(
     name="empty_and_short", mode="decode", batch=4, seq_lens=(0, 1, 2, 63), pool_pages=8,
     idx_heads=64, idx_dim=128, topk=64, sfa_heads=128, seed=7007)
 
+SMALL_MID = Spec(
+    name="small_mid", mode="decode", batch=3, seq_lens=(9000, 12345, 300), pool_pages=400,
+    idx_heads=64, idx_dim=128, topk=512, sfa_heads=128, seed=7008,
+    description="longest row between 8K and 16K keys (the selection's four-CTA clusters)")
+
 SMALL = [SMALL_DECODE_BF16, SMALL_DECODE_FP8, SMALL_DECODE_MX, SMALL_TIES, SMALL_PREFILL,
-         SMALL_H8, EMPTY_AND_SHORT]
+         SMALL_H8, EMPTY_AND_SHORT, SMALL_MID]
 
 ALL = {s.name: s for s in HEADLINE + SMALL}
 
