@@ -266,11 +266,9 @@ dsa_status_t run_indexer(const dsa_indexer_args_t* a, const dsa_index_cache_t* c
   tr.end("hist_clear");
   if (me != cudaSuccess) return cuda_fail(me, "clearing the key histograms");
   if (sp.max_page_blocks > 0) {
-    // e4m3 with per-token scales and the identity activation: the head sum folds into
-    // the query and each key is one streamed dot product.  Otherwise the per-head
-    // contraction on the tensor cores (CUDA cores for shapes they do not take).  (The
-    // folded query split into bf16 terms serves query rows that share keys; one row per
-    // sequence gains nothing from it.)
+    // Otherwise the per-head contraction on the tensor cores (CUDA cores for shapes they
+    // do not take).  (The folded query split into bf16 terms serves query rows that share
+    // keys; one row per sequence gains nothing from it.)
     const bool identity = a->act == DSA_ACT_IDENTITY;
     const bool split = false;
     // Query rows that share one sequence (prefill) share their keys: with bf16 keys and
@@ -280,8 +278,12 @@ dsa_status_t run_indexer(const dsa_indexer_args_t* a, const dsa_index_cache_t* c
       for (int32_t i = 1; i < tk->n_tokens && one_seq; ++i) one_seq = tk->token_seq_host[i] == tk->token_seq_host[0];
     const bool blocked = identity && c->dtype == DSA_BF16 && c->scale_kind == DSA_SCALE_NONE &&
                          (c->dim == 64 || c->dim == 128) && one_seq && tk->n_tokens >= 2 * kBlockRows;
-    const bool stream = !split && identity && c->dtype == DSA_E4M3 && c->scale_kind == DSA_SCALE_PER_TOKEN_F32 &&
-                        score_stream_supported(a->act, c->dim);
+    // e4m3 keys (per-token scales, d = 128) with the identity activation: the head
+    // sum folds into the query, and each key is one dot product taken from the TMA-staged
+    // tile on the CUDA cores.
+    const bool fold = score_fold_supported(c->dtype, c->scale_kind, a->act, c->dim);
+    const bool stream = !split && !fold && identity && c->dtype == DSA_E4M3 &&
+                        c->scale_kind == DSA_SCALE_PER_TOKEN_F32 && score_stream_supported(a->act, c->dim);
     const bool tc = score_tc_supported(c->dtype, c->dim, a->n_heads);
     tr.begin();
     cudaError_t e = cudaSuccess;
@@ -291,6 +293,9 @@ dsa_status_t run_indexer(const dsa_indexer_args_t* a, const dsa_index_cache_t* c
       sp2.q = qsplit;
       sp2.q_dep = 1;
       if (e == cudaSuccess) e = launch_score_tc_blocked(sp2, s);
+    } else if (fold) {
+      e = launch_qtilde(sp, c->dtype, c->scale_kind, qt, s);
+      if (e == cudaSuccess) e = launch_score_fold(sp, c->scale_kind, qt, s);
     } else if (split) {
       e = launch_qsplit(sp, qsplit, wsplit, kSplitQueryHeads, s);
       ScoreParams sp2 = sp;

@@ -41,6 +41,7 @@ struct ScoreParams {
   uint32_t* err;
   int32_t n_heads, dim, act, max_page_blocks;
   int32_t q_dep;           // 1: q is written by the preceding kernel (wait before reading it)
+  const float* qt;         // q~ [T, dim] f32 (the folded-query kernel only)
 };
 
 struct TopkParams {
@@ -130,6 +131,12 @@ cudaError_t launch_score_tc(const ScoreParams& p, dsa_dtype_t dt, dsa_scale_t sk
 bool score_stream_supported(dsa_act_t act, int dim);
 // q~ scratch: [n_tokens, dim] f32 in the workspace
 cudaError_t launch_score_stream(const ScoreParams& p, dsa_dtype_t dt, dsa_scale_t sk, float* qt, cudaStream_t s);
+// q~ alone (f32 [n_tokens, dim], query scales folded in)
+cudaError_t launch_qtilde(const ScoreParams& p, dsa_dtype_t dt, dsa_scale_t sk, float* qt, cudaStream_t s);
+// e4m3 keys, identity activation, d = 128: the TMA page ring of the tensor-core kernel,
+// each key's dot product with q~ (key scales applied) on the CUDA cores from shared memory
+bool score_fold_supported(dsa_dtype_t dt, dsa_scale_t sk, dsa_act_t act, int dim);
+cudaError_t launch_score_fold(const ScoreParams& p, dsa_scale_t sk, const float* qt, cudaStream_t s);
 // bf16, identity activation: the head-collapsed query split into 3 bf16 terms, laid out
 // as `stride` rows per token [n_tokens, stride, dim] (terms, then zero rows) with weights
 // [n_tokens, stride] (1, 1, 1, 0, ...; skipped when ws is null).  stride 16: 16 "heads"

@@ -272,6 +272,15 @@ cudaError_t launch_stream(const ScoreParams& p, float* qt, cudaStream_t s) {
 
 bool score_stream_supported(dsa_act_t act, int dim) { return act == DSA_ACT_IDENTITY && (dim == 64 || dim == 128); }
 
+cudaError_t launch_qtilde(const ScoreParams& p, dsa_dtype_t dt, dsa_scale_t sk, float* qt, cudaStream_t s) {
+  const dim3 g(p.tv.n_tokens), b(kQtThreads);
+  if (dt == DSA_BF16)
+    return p.dim == 64 ? launch_pdl(qtilde_kernel<64, 0>, g, b, 0, s, p, qt) : launch_pdl(qtilde_kernel<128, 0>, g, b, 0, s, p, qt);
+  if (sk == DSA_SCALE_PER_TOKEN_F32)
+    return p.dim == 64 ? launch_pdl(qtilde_kernel<64, 1>, g, b, 0, s, p, qt) : launch_pdl(qtilde_kernel<128, 1>, g, b, 0, s, p, qt);
+  return p.dim == 64 ? launch_pdl(qtilde_kernel<64, 2>, g, b, 0, s, p, qt) : launch_pdl(qtilde_kernel<128, 2>, g, b, 0, s, p, qt);
+}
+
 cudaError_t launch_qsplit(const ScoreParams& p, uint16_t* qs, float* ws, int stride, cudaStream_t s) {
   return p.dim == 64 ? launch_pdl(qsplit_kernel<64>, dim3(p.tv.n_tokens), dim3(kSplitThreads), 0, s, p, qs, ws, stride)
                      : launch_pdl(qsplit_kernel<128>, dim3(p.tv.n_tokens), dim3(kSplitThreads), 0, s, p, qs, ws, stride);

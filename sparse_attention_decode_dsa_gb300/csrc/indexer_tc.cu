@@ -43,7 +43,7 @@ struct Cfg {
   static constexpr int kRegions = kRowBytes / 128;         // 128-byte swizzle columns per row
   static constexpr int kBoxInner = 128 / kElem;            // elements in one 128-byte piece
   static constexpr int kStageBytes = kTileTok * kRowBytes;
-  static constexpr int kStages = KIND == 0 ? 4 : 6;
+  static constexpr int kStages = KIND == 0 ? 4 : 10;
   static constexpr int kRegionStageBytes = kTileTok * 128;  // 16 KB
   static constexpr int kRegionQBytes = 64 * 128;           // 8 KB (up to 64 heads)
   static constexpr int kQSlotBytes = kRegions * kRegionQBytes;
@@ -63,10 +63,28 @@ struct TcArgs {
   int32_t nrows;  // rows in this launch
 };
 
+// 16 e4m3 values -> f32, exactly.
+__device__ __forceinline__ void e4m3x16_to_f32(const uint4& raw, float* out) {
+  const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w[i] & 0xFFFFu), __NV_E4M3);
+    const __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w[i] >> 16), __NV_E4M3);
+    const float2 a = __half22float2(__half2(lo));
+    const float2 c = __half22float2(__half2(hi));
+    out[4 * i] = a.x;
+    out[4 * i + 1] = a.y;
+    out[4 * i + 2] = c.x;
+    out[4 * i + 3] = c.y;
+  }
+}
+
 // BLK: row-blocked (bf16, identity activation, one sequence): an item is a block of
 // kBlockRows consecutive rows and one tile; the MMA's N = 64 columns are the blocks' rows'
 // three split-query terms (p.q: [rows, 3, D]).
-template <int KIND, int D, bool BLK>
+// FOLD: e4m3 keys, identity activation: no tensor cores; the epilogue warps take each
+// key's dot product with the folded query q~ (p.qt) straight from the staged tile.
+template <int KIND, int D, bool BLK, bool FOLD = false>
 __global__ void __launch_bounds__(kTcThreads, 1)
     score_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap qmap,
                     const TcArgs a) {
@@ -102,7 +120,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   if (tid == 0) {
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
+      mbar_init(&empty[s], FOLD ? 4 : 1);  // the MMA's commit, or the four consuming warps
     }
     for (int i = 0; i < C::kNumAcc; ++i) {
       mbar_init(&acc_full[i], 1);
@@ -118,7 +136,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     tma_prefetch_desc(&kmap);
     tma_prefetch_desc(&qmap);
   }
-  if (warp == 1) {
+  if (warp == 1 && !FOLD) {
     tmem_alloc(tmem_base_s, C::kTmemCols);
     tmem_relinquish();
   }
@@ -165,7 +183,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const int total = prefix[nunits];
   const int it_begin = (int)((int64_t)total * blockIdx.x / gridDim.x);
   const int it_end = (int)((int64_t)total * (blockIdx.x + 1) / gridDim.x);
-  const uint32_t tmem_base = *tmem_base_s;
+  const uint32_t tmem_base = FOLD ? 0u : *tmem_base_s;
 
   if (warp == 0) {
     // ================================ TMA producer ================================
@@ -179,7 +197,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       int r = 0, cur_row = -1, qcount = 0;
       for (int it = it_begin; it < it_end; ++it) {
         while (prefix[r + 1] <= it) ++r;
-        if (r != cur_row) {
+        if (!FOLD && r != cur_row) {
           cur_row = r;
           const int slot = qcount & 1;
           if (!mbar_wait(&q_empty[slot], ((qcount >> 1) & 1) ^ 1, abort_flag, p.err)) break;
@@ -230,7 +248,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
   } else if (warp == 1) {
     // ================================ MMA issuer ==================================
-    if (lane == 0) {
+    if (lane == 0 && !FOLD) {
       const uint32_t idesc_v = idesc(128, N, C::kFmt, C::kFmt);
       int stage = 0, acc = 0;
       uint32_t phase = 0, acc_phase = 0;  // acc cycles through kNumAcc buffers
@@ -328,6 +346,73 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             p.scores[grow * p.score_stride + t] = v;
             atomicAdd(p.hist + grow * kTopkBins + (score_key(v) >> 20), 1u);
           }
+        }
+      }
+    } else if constexpr (FOLD) {
+      // token i of the tile: its key (one 128-byte swizzled row of e4m3) against q~, the
+      // key's scale per token or per 32-element group applied to the partial sums
+      static_assert(KIND != 0 && D == 128, "folded scoring: e4m3 keys of 128 elements");
+      float* qt_s = epi + (warp - 2) * (64 + 64 * 4 + 4);  // this warp's copy of q~
+      int r = 0, cur_row = -1;
+      for (int it = it_begin; it < it_end; ++it) {
+        while (prefix[r + 1] <= it) ++r;
+        const int n = it - it_begin;
+        if (n % kEpiGroups != grp) continue;
+        const int grow = a.row0 + r;
+        if (r != cur_row) {
+          cur_row = r;
+          __syncwarp();
+          for (int d = lane; d < D; d += 32) qt_s[d] = p.qt[(int64_t)grow * D + d];
+          __syncwarp();
+        }
+        const int stage = n % C::kStages;
+        const uint32_t par = (uint32_t)(n / C::kStages) & 1u;
+        const int t = (it - prefix[r]) * kTileTok + i;
+        const bool valid = t < rown[r];
+        const int pg = valid ? physical_page(p.tv, rowb[r], t >> 6, nullptr) : -1;
+        float ks[4] = {1.f, 1.f, 1.f, 1.f};
+        if (pg >= 0) {
+          const int64_t krow = (int64_t)pg * kPage + (t & 63);
+          if (KIND == 1) {
+            ks[0] = ((const float*)p.k_scale)[krow];
+          } else {
+            const uint32_t k4 = *(const uint32_t*)((const uint8_t*)p.k_scale + krow * 4);
+#pragma unroll
+            for (int g = 0; g < 4; ++g) ks[g] = e8m0_to_f32((k4 >> (8 * g)) & 0xFF);
+          }
+        }
+        bool ok = true;
+        if (lane == 0) ok = mbar_wait(&full[stage], par, abort_flag, p.err);
+        if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+        __syncwarp();
+        const uint8_t* krow_s = stages + stage * C::kStageBytes + i * 128;
+        float acc = 0.f;
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {  // 32-element groups, two 16-byte chunks each
+          float ag = 0.f;
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            const int u = 2 * g + hh;
+            float f[16];
+            e4m3x16_to_f32(*(const uint4*)(krow_s + ((u ^ (i & 7)) << 4)), f);
+            const float4* q4 = (const float4*)(qt_s + 16 * u);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float4 qq = q4[e];
+              ag = fmaf(f[4 * e], qq.x, ag);
+              ag = fmaf(f[4 * e + 1], qq.y, ag);
+              ag = fmaf(f[4 * e + 2], qq.z, ag);
+              ag = fmaf(f[4 * e + 3], qq.w, ag);
+            }
+          }
+          acc += KIND == 2 ? ag * ks[g] : ag;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[stage]);  // this warp has read its 32 keys
+        if (valid) {
+          const float v = pg >= 0 ? (KIND == 1 ? acc * ks[0] : acc) : -INFINITY;
+          p.scores[(int64_t)grow * p.score_stride + t] = v;
+          atomicAdd(p.hist + (int64_t)grow * kTopkBins + (score_key(v) >> 20), 1u);
         }
       }
     } else {
@@ -443,20 +528,20 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   // ---- tear-down ---------------------------------------------------------------------
   tc_fence_before();
   __syncthreads();
-  if (warp == 1) {
+  if (warp == 1 && !FOLD) {
     tc_fence_after();
     tmem_dealloc(tmem_base, C::kTmemCols);
   }
 }
 
 // ---- host side: launch ---------------------------------------------------------------
-template <int KIND, int D, bool BLK = false>
+template <int KIND, int D, bool BLK = false, bool FOLD = false>
 cudaError_t launch_tc(const ScoreParams& p, cudaStream_t s) {
   using C = Cfg<KIND, D>;
   static_assert(C::kSmem <= 232448, "shared memory budget");
   CUtensorMap kmap, qmap;
   if (!make_tma_2d_sw128(&kmap, p.k, (uint64_t)p.tv.num_pages * kPage, C::kElem, D, kPage)) return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(score_tc_kernel<KIND, D, BLK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaError_t e = cudaFuncSetAttribute(score_tc_kernel<KIND, D, BLK, FOLD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        C::kSmem);
   if (e != cudaSuccess) return e;
   int dev = 0, sms = 0;
@@ -472,7 +557,7 @@ cudaError_t launch_tc(const ScoreParams& p, cudaStream_t s) {
     a.p = p;
     a.row0 = row0;
     a.nrows = p.tv.n_tokens - row0 < kMaxRowsPerLaunch ? p.tv.n_tokens - row0 : kMaxRowsPerLaunch;
-    e = launch_pdl(score_tc_kernel<KIND, D, BLK>, dim3(sms), dim3(kTcThreads), C::kSmem, s, kmap, qmap, a);
+    e = launch_pdl(score_tc_kernel<KIND, D, BLK, FOLD>, dim3(sms), dim3(kTcThreads), C::kSmem, s, kmap, qmap, a);
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;
@@ -484,6 +569,17 @@ bool score_tc_supported(dsa_dtype_t dt, int dim, int n_heads) {
   if (n_heads < 1 || n_heads > 64) return false;
   if (dt == DSA_BF16) return dim == 64 || dim == 128;
   return dim == 128;
+}
+
+bool score_fold_supported(dsa_dtype_t dt, dsa_scale_t sk, dsa_act_t act, int dim) {
+  // (MX keys measured slower this way than through the per-head tensor-core kernel)
+  return dt == DSA_E4M3 && sk == DSA_SCALE_PER_TOKEN_F32 && act == DSA_ACT_IDENTITY && dim == 128;
+}
+
+cudaError_t launch_score_fold(const ScoreParams& p, dsa_scale_t sk, const float* qt, cudaStream_t s) {
+  ScoreParams f = p;
+  f.qt = qt;
+  return sk == DSA_SCALE_PER_TOKEN_F32 ? launch_tc<1, 128, false, true>(f, s) : launch_tc<2, 128, false, true>(f, s);
 }
 
 cudaError_t launch_score_tc_blocked(const ScoreParams& p, cudaStream_t s) {
