@@ -121,6 +121,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* tmem_base_s = (uint32_t*)(mempty + 4);
   volatile int* abort_flag = (volatile int*)(tmem_base_s + 1);
   volatile int* last_s = (volatile int*)(abort_flag + 1);  // this CTA merges the splits
+  int* last_valid_s = (int*)(last_s + 1);                   // last slot holding a selected row
 
   int b, n_vis;
   resolve_token(p.tv, tok, &b, &n_vis, nullptr);
@@ -158,6 +159,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&mempty[i], 4);
     }
     *abort_flag = 0;
+    *last_valid_s = -1;
     // the peer's partial logits of tiles 0 and 1 may arrive as soon as the cluster syncs
     for (int t = 0; t < 2 && t < n_tiles; ++t) mbar_arrive_expect_tx(&xch_full[t], kXchBytes);
     fence_mbar_init();
@@ -206,6 +208,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
     for (int u = 0; u < kPer; ++u)
       pg[u] = pos[u] >= 0 ? __ldg(p.tv.block_table + (int64_t)b * p.tv.max_pages + (pos[u] >> 6)) : -1;
+    int mylast = -1;
 #pragma unroll
     for (int u = 0; u < kPer; ++u) {
       const int j = tid + u * kThreads;
@@ -216,10 +219,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (c == 0) atomicOr(p.err, DSA_DEVERR_PAGE_ID);
         } else {
           rid = pg[u] * kPage + (pos[u] & 63);
+          mylast = j;
         }
       }
       rowid[j] = rid;
     }
+    if (mylast >= 0) atomicMax(last_valid_s, mylast);
   }
   if (warp >= kSendWarp0 && warp < kFinWarp0) {
     // each sending thread moves its head row h of the latent part into tensor memory
@@ -258,11 +263,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  // a selected row stands in for empty slots; a split without any selected row attends
-  // to nothing and skips the pipeline entirely
+  // a selected row stands in for empty slots; tiles past the last selected row (the
+  // padding of rows shorter than K) are skipped, and a split without any selected row
+  // attends to nothing
   int fill = -1;
   for (int j = 0; j < n_tiles * kTok && fill < 0; ++j) fill = rowid[j];
-  const int n_tiles_run = fill >= 0 ? n_tiles : 0;
+  const int last_valid = *last_valid_s;
+  const int n_tiles_run = last_valid >= 0 ? last_valid / kTok + 1 : 0;
   cluster_wait();  // both CTAs' barriers exist before any remote traffic
 
   if (warp < kGatherWarps) {
