@@ -321,6 +321,32 @@ def main():
     ms_per_step = total_ms / args.steps
     value = world * T * args.steps / (total_ms * 1e-3)
 
+    # ---- the same step replayed from a CUDA graph (host launch cost taken out) ----------
+    graph = None
+    try:
+        g = torch.cuda.CUDAGraph()
+        cap = torch.cuda.Stream(dev)
+        cap.wait_stream(stream)
+        with torch.cuda.graph(g, stream=cap):
+            dsa.fused_decode(plan, out_idx, out, ws, stream=cap)
+        torch.cuda.synchronize()
+        for _ in range(max(3, args.warmup)):
+            g.replay()
+        torch.cuda.synchronize()
+        g_b = torch.cuda.Event(enable_timing=True)
+        g_e = torch.cuda.Event(enable_timing=True)
+        g_b.record()
+        for _ in range(args.steps):
+            g.replay()
+        g_e.record()
+        torch.cuda.synchronize()
+        g_ms = g_b.elapsed_time(g_e) / args.steps
+        graph = {"us_per_step": 1e3 * g_ms, "value": world * T / (g_ms * 1e-3), "unit": UNIT,
+                 "note": "one dsa_fused_decode captured once, replayed back to back"}
+        assert dsa.read_device_error(ws) == 0
+    except Exception as ex:  # report, do not fail the bench line
+        graph = {"unavailable": f"{type(ex).__name__}: {ex}"[:200]}
+
     # ---- end to end through host buffers ----------------------------------------------
     # A serving loop: step i's inputs go up (pinned host -> device) on a copy stream while
     # step i - 1 computes, and step i's indices and outputs come back on another stream
@@ -403,6 +429,7 @@ def main():
             "gpu_launches": launches,
             "step_algorithmic_bytes": work["step"]["bytes"],
             "step_frac_hbm": work["step"]["bytes"] / (ms_per_step * 1e-3) / 1e9 / hbm_gbs,
+            "graph_replay": graph,
             "e2e": {"value": e2e_val, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "steps": e2e_steps, "ms_per_step": e2e_ms / e2e_steps},
             "cpu_baseline": cpu,
