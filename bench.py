@@ -317,6 +317,14 @@ def main():
                 "traffic": traffic, "algorithmic_bytes": dom_work["bytes"],
                 "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs, burst copy)" if peak_src == "measured" else "fallback 6.8 TB/s",
                 "frac_of_8TBps_nominal": dom_work["bytes"] / avg_s / 1e9 / 8000.0}
+    if spec.mode == "prefill" and dom_work["flops"] > 0:
+        # prefill is bound by the tensor cores: the kernel's algorithmic flops against the
+        # measured sustained bf16 rate (it runs for milliseconds inside the step)
+        ach = dom_work["flops"] / avg_s / 1e12
+        roofline = {"kernel": dom, "bound": "tensor", "achieved": ach, "peak": bf16_tf_sust, "unit": "TFLOP/s",
+                    "frac": ach / bf16_tf_sust, "traffic": traffic, "algorithmic_flops": dom_work["flops"],
+                    "peak_source": f"{peak_src} (MEASURED_PEAKS.json bf16_tflops_sustained)" if peak_src == "measured"
+                    else "fallback 1.7 PFLOP/s sustained"}
 
     ms_per_step = total_ms / args.steps
     value = world * T * args.steps / (total_ms * 1e-3)
