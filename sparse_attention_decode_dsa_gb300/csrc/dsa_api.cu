@@ -161,7 +161,9 @@ IndexerPlan plan_indexer(int32_t max_visible, int32_t n_tokens, int32_t dim) {
   if (p.score_stride == 0) p.score_stride = 64;
   const size_t rows = align_up((size_t)n_tokens * p.score_stride * sizeof(float));
   p.hist_bytes = align_up((size_t)n_tokens * kTopkBins * sizeof(uint32_t));
-  // collapsed query: f32 [T, dim] or, split for the tensor cores, bf16 [T, 16, dim] + f32 [T, 16]
+  // collapsed-query scratch: f32 [T, dim] (folded query) or bf16 [T, 3, dim] (its split for
+  // the row-blocked tensor-core path), sized as bf16 [T, 16, dim] + f32 [T, 16] (the
+  // workspace formula the boundary documents)
   p.qt_bytes = align_up((size_t)n_tokens * kSplitQueryHeads * dim * sizeof(uint16_t)) +
                align_up((size_t)n_tokens * kSplitQueryHeads * sizeof(float));
   p.score_bytes = p.hist_bytes + p.qt_bytes + rows;
@@ -241,9 +243,7 @@ dsa_status_t run_indexer(const dsa_indexer_args_t* a, const dsa_index_cache_t* c
                          size_t clear_bytes, cudaStream_t s, Tracer& tr) {
   uint32_t* hist = (uint32_t*)region;
   float* qt = (float*)(region + ip.hist_bytes);
-  uint16_t* qsplit = (uint16_t*)(region + ip.hist_bytes);
-  float* wsplit = (float*)(region + ip.hist_bytes +
-                           align_up((size_t)tk->n_tokens * kSplitQueryHeads * c->dim * sizeof(uint16_t)));
+  uint16_t* qsplit = (uint16_t*)(region + ip.hist_bytes);  // (same scratch: the blocked path's split query)
   float* scores = (float*)(region + ip.hist_bytes + ip.qt_bytes);
   ScoreParams sp;
   sp.tv = token_view(pg, tk, ip.max_visible);
@@ -267,10 +267,8 @@ dsa_status_t run_indexer(const dsa_indexer_args_t* a, const dsa_index_cache_t* c
   if (me != cudaSuccess) return cuda_fail(me, "clearing the key histograms");
   if (sp.max_page_blocks > 0) {
     // Otherwise the per-head contraction on the tensor cores (CUDA cores for shapes they
-    // do not take).  (The folded query split into bf16 terms serves query rows that share
-    // keys; one row per sequence gains nothing from it.)
+    // do not take).
     const bool identity = a->act == DSA_ACT_IDENTITY;
-    const bool split = false;
     // Query rows that share one sequence (prefill) share their keys: with bf16 keys and
     // the identity activation, blocks of consecutive rows take each K tile together.
     bool one_seq = tk->token_seq ? true : pg->batch == 1;
@@ -282,7 +280,7 @@ dsa_status_t run_indexer(const dsa_indexer_args_t* a, const dsa_index_cache_t* c
     // sum folds into the query, and each key is one dot product taken from the TMA-staged
     // tile on the CUDA cores.
     const bool fold = score_fold_supported(c->dtype, c->scale_kind, a->act, c->dim);
-    const bool stream = !split && !fold && identity && c->dtype == DSA_E4M3 &&
+    const bool stream = !fold && identity && c->dtype == DSA_E4M3 &&
                         c->scale_kind == DSA_SCALE_PER_TOKEN_F32 && score_stream_supported(a->act, c->dim);
     const bool tc = score_tc_supported(c->dtype, c->dim, a->n_heads);
     tr.begin();
@@ -296,14 +294,6 @@ dsa_status_t run_indexer(const dsa_indexer_args_t* a, const dsa_index_cache_t* c
     } else if (fold) {
       e = launch_qtilde(sp, c->dtype, c->scale_kind, qt, s);
       if (e == cudaSuccess) e = launch_score_fold(sp, c->scale_kind, qt, s);
-    } else if (split) {
-      e = launch_qsplit(sp, qsplit, wsplit, kSplitQueryHeads, s);
-      ScoreParams sp2 = sp;
-      sp2.q = qsplit;
-      sp2.head_w = wsplit;
-      sp2.n_heads = kSplitQueryHeads;
-      sp2.q_dep = 1;
-      if (e == cudaSuccess) e = launch_score_tc(sp2, c->dtype, c->scale_kind, s);
     } else {
       e = stream ? launch_score_stream(sp, c->dtype, c->scale_kind, qt, s)
           : tc   ? launch_score_tc(sp, c->dtype, c->scale_kind, s)

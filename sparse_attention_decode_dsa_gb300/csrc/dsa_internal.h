@@ -80,10 +80,6 @@ bool make_tma_2d_sw128(CUtensorMap* m, const void* base, uint64_t rows, int elem
 // promotion); one-row boxes serve to gather 64-byte pieces of scattered rows.
 bool make_tma_2d_sw64_rows(CUtensorMap* m, const void* base, uint64_t rows, int elem, int row_elems,
                            int box_rows = 1);
-// 2-D map without swizzle, box = box_inner elements x box_rows rows (rows land densely,
-// row-major, in shared memory); elem = 1, 2 or 4 bytes.
-bool make_tma_2d_plain(CUtensorMap* m, const void* base, uint64_t rows, int elem, int row_elems, int box_inner,
-                       int box_rows);
 
 // Launch with programmatic stream serialization: the kernel may start while the previous
 // kernel in the stream is finishing; it calls pdl_wait() before touching what that
@@ -139,9 +135,9 @@ bool score_fold_supported(dsa_dtype_t dt, dsa_scale_t sk, dsa_act_t act, int dim
 cudaError_t launch_score_fold(const ScoreParams& p, dsa_scale_t sk, const float* qt, cudaStream_t s);
 // bf16, identity activation: the head-collapsed query split into 3 bf16 terms, laid out
 // as `stride` rows per token [n_tokens, stride, dim] (terms, then zero rows) with weights
-// [n_tokens, stride] (1, 1, 1, 0, ...; skipped when ws is null).  stride 16: 16 "heads"
-// of one token for the per-row tensor-core kernel; stride 3: consecutive tokens' terms
-// back to back, for the row-blocked kernel.
+// [n_tokens, stride] (1, 1, 1, 0, ...; skipped when ws is null).  The row-blocked kernel
+// takes stride 3 (consecutive tokens' terms back to back).  The workspace reserves
+// kSplitQueryHeads rows per token for it.
 constexpr int kSplitQueryHeads = 16;
 cudaError_t launch_qsplit(const ScoreParams& p, uint16_t* qs, float* ws, int stride, cudaStream_t s);
 // The row-blocked tensor-core score kernel: every token belongs to one sequence (host

@@ -23,21 +23,23 @@
 //   * Online softmax per head row (thread = row, no shuffles), base 2; the reference
 //     maximum only moves when a tile's maximum exceeds it by 8 (2^8 headroom), and O is
 //     then rescaled in tensor memory.
-//   * P (bf16) goes to tensor memory; O[128 x 256] += P . V with V read MN-major from
+//   * P (bf16) goes to shared memory; O[128 x 256] += P . V with V read MN-major from
 //     the same shared-memory rows the logits used.
-// Warp roles: warps 0-2 gather rows with TMA gather4 into a 4-stage ring of swizzled
-// rows, each lane issuing its own gathers (a gather's cost is in its issue); warp 3 (one thread) issues each MMA as soon as its
-// inputs are ready; warps 4-7 run softmax and the epilogue, loading and sending a tile's
-// partial logits as soon as they are ready and finishing a tile as soon as the peer's
-// part has arrived, so the exchange overlaps the softmax.  Tensor memory (512 columns): O [0,256), two logit buffers
+// Warp roles (twelve warps): warps 0-2 gather rows with TMA gather4 into a 4-stage ring
+// of swizzled rows, each lane issuing its own gathers (a gather's cost is in its issue);
+// warp 3 (converged, one elected lane) issues each MMA as soon as its inputs are ready;
+// warps 4-7 (senders) load each tile's partial logits, stage the rounded values for the
+// finishing warps and send them to the peer; warps 8-11 (finishers) add the peer's part,
+// run the softmax, store P and run the epilogue.  Sending tile n + 1 and finishing tile n
+// thus run at the same time.  Tensor memory (512 columns): O [0,256), two logit buffers
 // S0 [256,320) and S1 [320,384), Q latent [384,512).  Tile n uses logit buffer n & 1;
 // its P (bf16) is written over the peer's partial logits of tile n in the receive
 // buffer n & 1 (same 128-byte-swizzled rows, each thread its own row), and P.V(n)'s
 // completion hands that buffer back to the peer.  So QK(n + 1), the softmax of tile n
-// and P.V(n - 1) proceed at the same time; QK(n) only waits for the softmax to have
-// read S(n - 2).  Q's rope dims are an MMA operand in shared memory.  Every wait is bounded.  Shared memory per stage:
-// 4 latent regions of 64 rows x 128 B (128-byte swizzle) + 1 rope region of 64 rows
-// x 64 B (64-byte swizzle).
+// and P.V(n - 1) proceed at the same time; QK(n) only waits for the senders to have
+// read S(n - 2).  Q's rope dims are an MMA operand in shared memory.  Every wait is
+// bounded.  Shared memory per stage: 4 latent regions of 64 rows x 128 B (128-byte
+// swizzle) + 1 rope region of 64 rows x 64 B (64-byte swizzle).
 #include <cuda_fp16.h>
 
 #include "sm100.cuh"
@@ -48,7 +50,7 @@ namespace {
 
 using namespace sm100;
 
-constexpr int kGatherWarps = 3;                  // warps 0-2 gather (TMA), warp 3 issues MMAs,
+constexpr int kGatherWarps = 3;                  // warps 0-2 gather (TMA), warp 3 issues MMAs
 constexpr int kMmaWarp = kGatherWarps;           // warps 4-7 run softmax and the epilogue
 constexpr int kSendWarp0 = kMmaWarp + 1;          // warps 4-7 load and send the partial logits,
 constexpr int kFinWarp0 = kSendWarp0 + 4;         // warps 8-11 finish tiles (softmax, P) and the epilogue

@@ -91,31 +91,11 @@ __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t count) {
   asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(count) : "memory");
 }
 
-// Pulls the 128-byte line holding `ptr` into L2 (no registers written, nothing to wait on).
-__device__ __forceinline__ void prefetch_l2(const void* ptr) {
-  asm volatile("prefetch.global.L2 [%0];\n" ::"l"(ptr));
-}
 // One lane of the (converged) warp: the lowest active one.
 __device__ __forceinline__ bool elect_one() {
   uint32_t r;
   asm volatile("{\n .reg .pred p;\n elect.sync _|p, 0xffffffff;\n selp.u32 %0, 1, 0, p;\n}\n" : "=r"(r));
   return r != 0;
-}
-// 16-byte asynchronous copy global -> shared through the load/store path (no register
-// staging); the whole 128-byte line is brought into L2.
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global.L2::128B [%0], [%1], 16;\n" ::"r"(dst), "l"(src) : "memory");
-}
-// One arrival on `bar` once every cp.async this thread issued before has landed (the
-// barrier's expected count includes it).
-__device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* bar) {
-  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];\n" ::"r"(smem_u32(bar)) : "memory");
-}
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;\n" ::: "memory"); }
-// Bulk prefetch of [ptr, ptr + bytes) into L2 (16-byte aligned address, bytes a multiple
-// of 16); completes on its own, nothing waits for it.
-__device__ __forceinline__ void bulk_prefetch_l2(const void* ptr, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;\n" ::"l"(ptr), "r"(bytes) : "memory");
 }
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];\n" ::"l"(map) : "memory");
@@ -218,20 +198,6 @@ __device__ __forceinline__ uint32_t map_to_rank(uint32_t saddr, uint32_t rank) {
   uint32_t r;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;\n" : "=r"(r) : "r"(saddr), "r"(rank));
   return r;
-}
-// 16-byte store into a peer CTA's shared memory, counted in bytes on the peer's mbarrier.
-__device__ __forceinline__ void st_async_v4(uint32_t raddr, const float4& v, uint32_t rbar) {
-  asm volatile(
-      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];\n" ::"r"(raddr),
-      "r"(__float_as_uint(v.x)), "r"(__float_as_uint(v.y)), "r"(__float_as_uint(v.z)), "r"(__float_as_uint(v.w)),
-      "r"(rbar)
-      : "memory");
-}
-// Plain 16-byte store into a peer CTA's shared memory (address from map_to_rank).
-__device__ __forceinline__ void st_cluster_v4(uint32_t raddr, const float4& v) {
-  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};\n" ::"r"(raddr), "f"(v.x), "f"(v.y), "f"(v.z),
-               "f"(v.w)
-               : "memory");
 }
 // As mbar_wait, with cluster-scope acquire: writes a peer CTA released before its
 // arrival on this barrier are visible afterwards.
@@ -350,11 +316,6 @@ __device__ __forceinline__ float fast_exp2(float x) {
 // Arrival on an mbarrier of a peer CTA (address from map_to_rank).
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t rbar) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];\n" ::"r"(rbar) : "memory");
-}
-// Same without release ordering: for signals that publish no data of this thread (or
-// whose loads have provably completed, e.g. consumed by already issued instructions).
-__device__ __forceinline__ void mbar_arrive_remote_relaxed(uint32_t rbar) {
-  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];\n" ::"r"(rbar) : "memory");
 }
 // Makes this thread's generic-proxy shared-memory writes visible to the async proxy
 // (tensor-core operand reads).

@@ -39,22 +39,6 @@ bool make_tma_2d_sw128(CUtensorMap* m, const void* base, uint64_t rows, int elem
   return r == CUDA_SUCCESS;
 }
 
-bool make_tma_2d_plain(CUtensorMap* m, const void* base, uint64_t rows, int elem, int row_elems, int box_inner,
-                       int box_rows) {
-  auto enc = get_encode();
-  if (!enc) return false;
-  const CUtensorMapDataType dt = elem == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
-                                 : elem == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
-                                             : CU_TENSOR_MAP_DATA_TYPE_UINT8;
-  cuuint64_t dims[2] = {(cuuint64_t)row_elems, (cuuint64_t)rows};
-  cuuint64_t strides[1] = {(cuuint64_t)row_elems * elem};
-  cuuint32_t box[2] = {(cuuint32_t)box_inner, (cuuint32_t)box_rows};
-  cuuint32_t estr[2] = {1, 1};
-  CUresult r = enc(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                   CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
-}
-
 bool make_tma_2d_sw64_rows(CUtensorMap* m, const void* base, uint64_t rows, int elem, int row_elems, int box_rows) {
   auto enc = get_encode();
   if (!enc) return false;
