@@ -125,7 +125,7 @@ __device__ __forceinline__ void find_bin1024(const uint32_t* hist, uint32_t rema
 }
 
 template <int kCluster>  // CTAs per row
-__global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads) topk_cluster_kernel(TopkParams p) {
+__global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 3) topk_cluster_kernel(TopkParams p) {
   constexpr int kSlot = kPoolTotal / kCluster;  // candidates one CTA may put in the pool
   cg::cluster_group cluster = cg::this_cluster();
   const int rank = (int)cluster.block_rank();
