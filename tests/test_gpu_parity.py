@@ -176,3 +176,33 @@ def test_repeated_calls_are_deterministic(dsa):
     a = _run_fused(dsa, plan, wl.n_tokens, spec.topk, spec.sfa_heads)
     b = _run_fused(dsa, plan, wl.n_tokens, spec.topk, spec.sfa_heads)
     assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+
+
+@pytest.mark.parametrize("spec", [W.SMALL_DECODE_BF16, W.SMALL_PREFILL, W.SMALL_DECODE_FP8],
+                         ids=lambda s: s.name)
+def test_cuda_graph_replay_matches_eager(dsa, spec):
+    """The fused call captured into a CUDA graph and replayed gives the eager call's
+    indices and outputs bit for bit (the library launches only kernels and holds no
+    host-side state a replay could miss); the workspace is reused across replays."""
+    wl = W.make(spec)
+    plan = dsa.Plan(_device(wl))
+    T, K, H = wl.n_tokens, spec.topk, spec.sfa_heads
+    want = _run_fused(dsa, plan, T, K, H)
+    out_idx = torch.empty((T, K), dtype=torch.int32, device="cuda")
+    out = torch.empty((T, H, 512), dtype=torch.bfloat16, device="cuda")
+    ws = dsa.alloc_workspace(plan.ws_fused())
+    dsa.fused_decode(plan, out_idx, out, ws)  # first call on the device outside the capture
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    cap = torch.cuda.Stream()
+    cap.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.graph(g, stream=cap):
+        dsa.fused_decode(plan, out_idx, out, ws, stream=cap)
+    for _ in range(3):
+        out_idx.fill_(-7)
+        out.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert dsa.read_device_error(ws) == 0
+        assert np.array_equal(out_idx.cpu().numpy(), want[0])
+        assert np.array_equal(out.float().cpu().numpy().astype(np.float64), want[1])
