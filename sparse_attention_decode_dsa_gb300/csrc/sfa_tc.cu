@@ -53,8 +53,9 @@ using namespace sm100;
 constexpr int kGatherWarps = 3;                  // warps 0-2 gather (TMA), warp 3 issues MMAs
 constexpr int kMmaWarp = kGatherWarps;           // warps 4-7 run softmax and the epilogue
 constexpr int kSendWarp0 = kMmaWarp + 1;          // warps 4-7 load and send the partial logits,
-constexpr int kFinWarp0 = kSendWarp0 + 4;         // warps 8-11 finish tiles (softmax, P) and the epilogue
-constexpr int kThreads = (kFinWarp0 + 4) * 32;
+constexpr int kFinWarp0 = kSendWarp0 + 4;         // warps 8-11 finish key columns 0-31 of each tile and run
+constexpr int kFinWarpB0 = kFinWarp0 + 4;         // the epilogue; warps 12-15 finish columns 32-63
+constexpr int kThreads = (kFinWarpB0 + 4) * 32;
 constexpr int kTok = 64;                         // selected positions per tile
 constexpr int kStages = 4;
 constexpr int kRegion = kTok * 128;              // 64 rows x 128 B
@@ -67,7 +68,8 @@ constexpr uint32_t kColO = 0, kColS = 256, kColQl = 384;  // S buffer b: kColS +
 constexpr int kQRegion = 128 * 128;                // Q latent staging: 4 regions of 128 rows x 128 B
 static_assert(4 * kQRegion <= 2 * kStageBytes, "Q latent staging fits in stage buffers 2-3");
 constexpr int kQropeBytes = 128 * 64;             // Q rope (own 32 dims) [128 rows][64 B], 64-byte swizzle
-constexpr int kSmem = 1024 + kStages * kStageBytes + kQropeBytes + 4 * kXchBytes + kMaxSplitLen * 4 + 512;
+constexpr int kMaxXBytes = 2 * 2 * 128 * 4;       // finisher pairs' row maxima [tile parity][half][row]
+constexpr int kSmem = 1024 + kStages * kStageBytes + kQropeBytes + 3 * kXchBytes + kMaxXBytes + kMaxSplitLen * 4 + 512;
 static_assert(kSmem <= 232448, "shared memory budget");
 // Split merge: 64-column chunks of other splits' partials stream through the (then idle)
 // stage buffers, four at a time.
@@ -100,8 +102,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* stages = smem;
   uint8_t* qrope = stages + kStages * kStageBytes;            // Q rope operand
   uint8_t* xch = qrope + kQropeBytes;                         // [2][128 rows][64 fp16] peer partials, then P
-  uint8_t* stg = xch + 2 * kXchBytes;                         // [2][128 rows][64 fp16] own partial, outbound
-  int32_t* rowid = (int32_t*)(stg + 2 * kXchBytes);           // cache row of each slot or -1
+  uint8_t* stg = xch + 2 * kXchBytes;                         // [128 rows][64 fp16] own partial, outbound
+  float* maxx = (float*)(stg + kXchBytes);                    // [2][2][128] finisher pairs' row maxima
+  int32_t* rowid = (int32_t*)((uint8_t*)maxx + kMaxXBytes);   // cache row of each slot or -1
   uint64_t* bars = (uint64_t*)(rowid + kMaxSplitLen);
   uint64_t* kv_full = bars;
   uint64_t* kv_empty = kv_full + kStages;
@@ -116,9 +119,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* q_tma = drain + 1;    // Q (own dims) landed in shared memory
   uint64_t* m_ready = q_tma + 1;  // sibling merge: the sibling's inbox is free
   uint64_t* m_full = m_ready + 1; // sibling merge: the sibling's columns arrived
-  uint64_t* stg_full = m_full + 1;  // [2]: the senders staged tile t's own partial in stg[t & 1]
-  uint64_t* stg_free = stg_full + 2; // [2]: the finishers have read it
-  uint64_t* mfull = stg_free + 2;   // [4]: split merge, a chunk of another split's partial landed
+  uint64_t* mfull = m_full + 1;   // [4]: split merge, a chunk of another split's partial landed
   uint64_t* mempty = mfull + 4;  // [4]: the softmax warps are done with that chunk buffer
   uint32_t* tmem_base_s = (uint32_t*)(mempty + 4);
   volatile int* abort_flag = (volatile int*)(tmem_base_s + 1);
@@ -140,8 +141,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(q_ready, 4);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s_full[i], 1);
-      mbar_init(&s_free[i], 4);
-      mbar_init(&p_full[i], 4);
+      mbar_init(&s_free[i], 12);  // the four senders and the eight finishers have read the logits
+      mbar_init(&p_full[i], 8);   // both halves of every row of P stored
       mbar_init(&pv_done[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
@@ -152,10 +153,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(q_tma, 1);
     mbar_init(m_ready, 1);
     mbar_init(m_full, 1);
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&stg_full[i], 4);
-      mbar_init(&stg_free[i], 4);
-    }
     for (int i = 0; i < 4; ++i) {
       mbar_init(&mfull[i], 1);
       mbar_init(&mempty[i], 4);
@@ -433,9 +430,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ============================ senders =============================================
     // Per tile t: load this CTA's partial logits, scale them by softmax_scale * log2(e)
     // and round them to fp16 (both CTAs sum the same rounded halves, so their softmax is
-    // identical), free the logit buffer for QK(t + 2), stage them in stg[t & 1] for the
-    // finishing warps and send them (one bulk copy per warp) to the peer's receive buffer
-    // t & 1 once the peer is done with tile t - 2 there.  Every wait is bounded.
+    // identical), stage them and send them (one bulk copy per warp) to the peer's receive
+    // buffer t & 1 once the peer is done with tile t - 2 there.  (The finishing warps
+    // derive the same rounded values from the logits themselves.)  Every wait is bounded.
     const int quarter = warp & 3;
     const int h = quarter * 32 + lane;  // head row == TMEM lane
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
@@ -471,15 +468,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) {
         mbar_arrive(&s_free[bb]);
-        if (t >= 2) {
-          // stg[bb] is free once the finishers read tile t - 2 there and its copy did
-          good = mbar_wait(&stg_free[bb], ((t >> 1) & 1) ^ 1, abort_flag, p.err);
-          bulk_wait_read1();
-        }
+        if (t > 0) bulk_wait_read0();  // the staging is free once the copy of tile t - 1 read it
       }
-      if (!__shfl_sync(0xffffffffu, good, 0)) break;
       __syncwarp();
-      uint8_t* sbuf = stg + bb * kXchBytes;
+      uint8_t* sbuf = stg;
 #pragma unroll
       for (int u = 0; u < kTok / 8; ++u)
         *(uint4*)(sbuf + myrow + (((uint32_t)u ^ sw) << 4)) =
@@ -487,7 +479,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       fence_proxy_async_smem();  // the bulk copy reads it (async proxy)
       __syncwarp();
       if (lane == 0) {
-        mbar_arrive(&stg_full[bb]);
         if (t >= 2) good = mbar_wait_cluster(&xch_empty[bb], ((t >> 1) & 1) ^ 1, abort_flag, p.err);
         if (good) {
           bulk_copy_to_peer(xch_peer0 + bb * kXchBytes, smem_u32(sbuf) + warp_rows, 32 * kTok * 2,
@@ -507,54 +498,65 @@ __global__ void __launch_bounds__(kThreads, 1)
     float m_ref = -INFINITY, l = 0.f;
     bool ok = true;
 
-    // Finishes tile n: adds this CTA's rounded partial logits (staged by the senders) and
-    // the peer's, runs the online softmax and stores P.  Returns false on abort.
-    auto finish = [&](int n) -> bool {
-      bool good = true;
+    // Finishing: the two warps of a row quarter take key columns [32 hf, 32 hf + 32) of
+    // each tile (hf = 0: warps 8-11, hf = 1: warps 12-15).  Each rounds its own half of
+    // the logits exactly as the senders do, adds the peer's half, and the pair meets once
+    // per tile to share the row maxima (so both keep the same reference maximum); each
+    // keeps its half of the row sum, stores its half of P and rescales half of O.  Both
+    // warps run every tile and reach the pair's barrier whatever happened, so a wait that
+    // gives up never strands the partner; a failed wait skips the work.
+    const int hf = warp >= kFinWarpB0 ? 1 : 0;
+    const uint64_t sc2 = f2_pack(p.scale_log2, p.scale_log2);
+    bool good = true;
+    for (int n = 0; n < n_tiles_run; ++n) {
       const int bb = n & 1;
-      const int32_t* rt = rowid + n * kTok;
-      const uint32_t vlo = __ballot_sync(0xffffffffu, rt[lane] >= 0);
-      const uint32_t vhi = __ballot_sync(0xffffffffu, rt[32 + lane] >= 0);
-      if (lane == 0) {
+      const uint32_t vmask = __ballot_sync(0xffffffffu, rowid[n * kTok + 32 * hf + lane] >= 0);
+      if (lane == 0 && good) {
         good = mbar_wait(&xch_full[bb], (n >> 1) & 1, abort_flag, p.err);
-        if (good && h == 0 && n + 2 < n_tiles_run) mbar_arrive_expect_tx(&xch_full[bb], kXchBytes);  // tile n + 2
-        if (good) good = mbar_wait(&stg_full[bb], (n >> 1) & 1, abort_flag, p.err);
+        if (good && hf == 0 && h == 0 && n + 2 < n_tiles_run)  // one thread re-arms it for tile n + 2
+          mbar_arrive_expect_tx(&xch_full[bb], kXchBytes);
+        if (good) good = mbar_wait(&s_full[bb], (n >> 1) & 1, abort_flag, p.err);
       }
-      if (!__shfl_sync(0xffffffffu, good, 0)) return false;
+      good = __shfl_sync(0xffffffffu, good, 0);
       __syncwarp();
-      const uint8_t* recv = xch + bb * kXchBytes + myrow;
-      const uint8_t* mine = stg + bb * kXchBytes + myrow;
-      float s[kTok];  // full scaled logits of tile n: widen the peer's half, add ours
+      float s[32];  // scaled logits of this warp's half of tile n
+      float lmax = -INFINITY;
+      if (good) {
+        tc_fence_after();
+        uint32_t v[32];
+        tmem_ld32(tmem + lane_off + kColS + 64 * bb + 32 * hf, v);
+        tmem_ld_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&s_free[bb]);
+        const uint8_t* recv = xch + bb * kXchBytes + myrow;
 #pragma unroll
-      for (int u = 0; u < kTok / 8; ++u) {
-        const uint4 r = *(const uint4*)(recv + (((uint32_t)u ^ sw) << 4));
-        const uint4 o = *(const uint4*)(mine + (((uint32_t)u ^ sw) << 4));
-        const uint32_t rr[4] = {r.x, r.y, r.z, r.w};
-        const uint32_t oo[4] = {o.x, o.y, o.z, o.w};
+        for (int u = 0; u < 4; ++u) {
+          const uint4 r = *(const uint4*)(recv + ((((uint32_t)(4 * hf + u)) ^ sw) << 4));
+          const uint32_t rr[4] = {r.x, r.y, r.z, r.w};
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          f16x2_to_f32(rr[i], s[8 * u + 2 * i], s[8 * u + 2 * i + 1]);
-          add_f16x2_to(oo[i], s[8 * u + 2 * i], s[8 * u + 2 * i + 1]);
+          for (int e = 0; e < 4; ++e) {
+            const int jj = 8 * u + 2 * e;
+            float a0, a1;
+            f2_unpack(f2_mul(f2_pack(__uint_as_float(v[jj]), __uint_as_float(v[jj + 1])), sc2), a0, a1);
+            f16x2_to_f32(rr[e], s[jj], s[jj + 1]);
+            add_f16x2_to(cvt_f16x2(a0, a1), s[jj], s[jj + 1]);  // the same rounded half the peer got
+          }
         }
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&stg_free[bb]);  // the senders may stage tile n + 2 there
-      // online softmax (base 2), masked positions get no weight
-      if ((vlo & vhi) != 0xffffffffu) {
+        if (vmask != 0xffffffffu) {
 #pragma unroll
-        for (int j = 0; j < kTok; ++j) {
-          const bool v = ((j < 32 ? vlo : vhi) >> (j & 31)) & 1u;
-          s[j] = v ? s[j] : -INFINITY;
+          for (int jj = 0; jj < 32; ++jj) s[jj] = ((vmask >> jj) & 1u) ? s[jj] : -INFINITY;
         }
+        float mx[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) mx[e] = max3f(s[e], s[8 + e], fmaxf(s[16 + e], s[24 + e]));
+        lmax = max3f(max3f(mx[0], mx[1], mx[2]), max3f(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
       }
-      float mx[8];  // independent partial maxima, three inputs per step
-#pragma unroll
-      for (int i = 0; i < 8; ++i) mx[i] = s[i];
-#pragma unroll
-      for (int j = 8; j < kTok; j += 16)
-#pragma unroll
-        for (int i = 0; i < 8; ++i) mx[i] = j + 8 + i < kTok ? max3f(mx[i], s[j + i], s[j + 8 + i]) : fmaxf(mx[i], s[j + i]);
-      const float tmax = max3f(max3f(mx[0], mx[1], mx[2]), max3f(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
+      maxx[(bb * 2 + hf) * 128 + h] = lmax;
+      named_bar_sync(2 + quarter, 64);
+      const float pmax = maxx[(bb * 2 + (hf ^ 1)) * 128 + h];
+      if (!good) continue;
+      const float tmax = fmaxf(lmax, pmax);
       float alpha = 1.f;
       bool rescale = false;
       if (tmax != -INFINITY && (m_ref == -INFINITY || tmax > m_ref + 8.f)) {
@@ -567,55 +569,63 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float msub = m_ref == -INFINITY ? 0.f : m_ref;  // nothing visible yet: all weights 0
       const uint64_t negm = f2_pack(-msub, -msub);
       uint64_t ps[4] = {0ull, 0ull, 0ull, 0ull};  // paired partial sums
-      uint32_t pw[kTok / 2];
+      uint32_t pw[16];
 #pragma unroll
-      for (int j = 0; j < kTok / 2; ++j) {
+      for (int jj = 0; jj < 16; ++jj) {
         float x0, x1;
-        f2_unpack(f2_add(f2_pack(s[2 * j], s[2 * j + 1]), negm), x0, x1);
+        f2_unpack(f2_add(f2_pack(s[2 * jj], s[2 * jj + 1]), negm), x0, x1);
         x0 = fast_exp2(x0);  // 2^-inf = 0 for masked positions
         x1 = fast_exp2(x1);
-        ps[j & 3] = f2_add(ps[j & 3], f2_pack(x0, x1));
-        pw[j] = cvt_bf16x2(x0, x1);
+        ps[jj & 3] = f2_add(ps[jj & 3], f2_pack(x0, x1));
+        pw[jj] = cvt_bf16x2(x0, x1);
       }
       float r0, r1, r2, r3;
       f2_unpack(f2_add(ps[0], ps[1]), r0, r1);
       f2_unpack(f2_add(ps[2], ps[3]), r2, r3);
-      const float rs = (r0 + r2) + (r1 + r3);
-      l = l * alpha + rs;
-      if (__any_sync(0xffffffffu, rescale)) {  // rare: move O to the new reference maximum
+      l = l * alpha + ((r0 + r2) + (r1 + r3));
+      if (__any_sync(0xffffffffu, rescale)) {  // rare: move O (this warp's half of it) to the new reference
         if (n > 0) {  // ... once P.V(n - 1), the last one issued, has updated it
-          if (lane == 0) good = mbar_wait(&pv_done[(n - 1) & 1], ((n - 1) >> 1) & 1, abort_flag, p.err);
-          if (!__shfl_sync(0xffffffffu, good, 0)) return false;
+          bool g2 = true;
+          if (lane == 0) g2 = mbar_wait(&pv_done[(n - 1) & 1], ((n - 1) >> 1) & 1, abort_flag, p.err);
+          good = __shfl_sync(0xffffffffu, g2, 0);
           __syncwarp();
           tc_fence_after();
         }
+        if (good) {
 #pragma unroll 1
-        for (int ch = 0; ch < 8; ++ch) {
-          uint32_t v[32];
-          tmem_ld32(tmem + lane_off + kColO + 32 * ch, v);
-          tmem_ld_wait();
+          for (int ch = 4 * hf; ch < 4 * hf + 4; ++ch) {
+            uint32_t v[32];
+            tmem_ld32(tmem + lane_off + kColO + 32 * ch, v);
+            tmem_ld_wait();
 #pragma unroll
-          for (int j = 0; j < 32; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) * alpha);
-          tmem_st32(tmem + lane_off + kColO + 32 * ch, v);
+            for (int jj = 0; jj < 32; ++jj) v[jj] = __float_as_uint(__uint_as_float(v[jj]) * alpha);
+            tmem_st32(tmem + lane_off + kColO + 32 * ch, v);
+          }
         }
       }
-      {  // row h of P(n) over the peer's row h of tile n (read above): 128-byte swizzle,
-         // the K-major A operand of P.V
+      if (!good) continue;
+      {  // this warp's half of row h of P(n), over the peer's data in the receive buffer
         uint8_t* prow = xch + bb * kXchBytes + myrow;
 #pragma unroll
-        for (int u = 0; u < 8; ++u)
-          *(uint4*)(prow + (((uint32_t)u ^ (uint32_t)(h & 7)) << 4)) =
+        for (int u = 0; u < 4; ++u)
+          *(uint4*)(prow + ((((uint32_t)(4 * hf + u)) ^ sw) << 4)) =
               make_uint4(pw[4 * u], pw[4 * u + 1], pw[4 * u + 2], pw[4 * u + 3]);
       }
       fence_proxy_async_smem();  // visible to the MMA (async proxy)
       tmem_st_wait();            // (rescaled O)
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&p_full[n & 1]);
-      return true;
-    };
-
-    for (int n = 0; ok && n < n_tiles_run; ++n) ok = finish(n);
+      if (lane == 0) mbar_arrive(&p_full[bb]);
+    }
+    // the row sums' halves meet; warps 12-15 are done after this
+    {
+      float* lx = maxx + ((n_tiles_run & 1) * 2 + 1) * 128;  // a slot the last tile did not use
+      if (hf) lx[h] = l;
+      named_bar_sync(2 + quarter, 64);
+      if (!hf) l += lx[h];
+    }
+    ok = good && !*abort_flag;
+    if (!hf) {
     // ---- epilogue: O / l -> this CTA's 256 value dims ----------------------------------
     if (ok && n_tiles_run > 0) {
       if (lane == 0) ok = mbar_wait(&pv_done[(n_tiles_run - 1) & 1], ((n_tiles_run - 1) >> 1) & 1, abort_flag, p.err);
@@ -846,6 +856,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (warp == kFinWarp0 && lane == 0) p.merge_cnt[tok * 2 + c] = 0u;
       }
     }
+    }  // the first finishing warp of each row quarter
   }
 
   // ---- tear-down ---------------------------------------------------------------------
