@@ -80,7 +80,7 @@ static_assert(16 * kMaxSfaHeads * 4 <= 2 * kXchBytes, "split weights fit in the 
 constexpr uint32_t kMergeThreads = 5 * 32;                 // gather warp 0 + the four finishing warps
 // Sibling merge (two splits in one cluster): outbox and inbox of 128 rows x 128 f32
 // columns plus 128 (m, l) pairs each, in the stage buffers.
-constexpr uint32_t kSibBytes = 128 * 512 + 128 * 8;
+constexpr uint32_t kSibBytes = 128 * 256 + 128 * 8;  // 128 rows x 128 fp16 columns, then (m, l) per row
 static_assert(2 * kSibBytes <= kStages * kStageBytes, "sibling merge buffers fit in the stage buffers");                 // gather warp 0 + the four softmax warps
 
 // Launched in clusters of two CTAs (the pair), or four (two splits x the pair) when the
@@ -665,8 +665,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       // finalizes value columns [128 s, 128 s + 128) of this half: it hands the other 128
       // columns of its O (unnormalized) and every row's (m_ref, l) to its sibling (rank
       // ^ 2) through distributed shared memory and receives the sibling's in exchange.
-      // The (then idle) stage buffers hold the outbox and the inbox: row h's 16-byte chunk
-      // u at slot u ^ (h & 31) (conflict-free), then the 128 (m, l) pairs.
+      // The columns travel normalized (O / l, rounded to fp16: relative 2^-11, below the
+      // bf16 rounding of the output) with (m_ref, l) in f32.  The (then idle) stage
+      // buffers hold the outbox and the inbox: row h's 16-byte chunk u (8 columns) at
+      // slot u ^ (h & 15) (conflict-free), then the 128 (m, l) pairs.
       const uint32_t sib = rank ^ 2u;
       const int s_me = (int)(rank >> 1);
       uint8_t* outbox = stages;
@@ -687,21 +689,24 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int j = 0; j < 32; ++j) v[j] = 0u;
         }
 #pragma unroll
-        for (int u = 0; u < 8; ++u)
-          *(uint4*)(outbox + h * 512 + (((8 * q + u) ^ (h & 31)) << 4)) =
-              make_uint4(v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
+        for (int u = 0; u < 4; ++u) {
+          const float* f = (const float*)v + 8 * u;
+          *(uint4*)(outbox + h * 256 + (((4 * q + u) ^ (h & 15)) << 4)) =
+              make_uint4(cvt_f16x2(f[0] * inv, f[1] * inv), cvt_f16x2(f[2] * inv, f[3] * inv),
+                         cvt_f16x2(f[4] * inv, f[5] * inv), cvt_f16x2(f[6] * inv, f[7] * inv));
+        }
       }
-      ((float2*)(outbox + 128 * 512))[h] = make_float2(ok ? m_ref : -INFINITY, ok ? l : 0.f);
+      ((float2*)(outbox + 128 * 256))[h] = make_float2(ok ? m_ref : -INFINITY, ok ? l : 0.f);
       fence_proxy_async_smem();  // the bulk copies read it (async proxy)
       __syncwarp();
       if (lane == 0 && mbar_wait_cluster(m_ready, 0, abort_flag, p.err)) {  // the sibling's inbox is free
         // this warp's 32 rows and their (m, l) pairs, one bulk copy each
         const uint32_t rows = (uint32_t)(quarter * 32);
         const uint32_t sib_full = map_to_rank(smem_u32(m_full), sib);
-        bulk_copy_to_peer(map_to_rank(smem_u32(inbox) + rows * 512, sib), smem_u32(outbox) + rows * 512, 32 * 512,
+        bulk_copy_to_peer(map_to_rank(smem_u32(inbox) + rows * 256, sib), smem_u32(outbox) + rows * 256, 32 * 256,
                           sib_full);
-        bulk_copy_to_peer(map_to_rank(smem_u32(inbox) + 128 * 512 + rows * 8, sib),
-                          smem_u32(outbox) + 128 * 512 + rows * 8, 32 * 8, sib_full);
+        bulk_copy_to_peer(map_to_rank(smem_u32(inbox) + 128 * 256 + rows * 8, sib),
+                          smem_u32(outbox) + 128 * 256 + rows * 8, 32 * 8, sib_full);
         bulk_commit();
       }
       bool good = true;
@@ -709,7 +714,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       good = __shfl_sync(0xffffffffu, good, 0);
       __syncwarp();
       if (good && ok) {  // (warp-uniform: the tensor-memory loads below take the whole warp)
-        const float2 ms = ((const float2*)(inbox + 128 * 512))[h];  // the sibling's (m, l)
+        const float2 ms = ((const float2*)(inbox + 128 * 256))[h];  // the sibling's (m, l)
         const float m0 = s_me == 0 ? m_ref : ms.x, l0 = s_me == 0 ? l : ms.y;
         const float m1 = s_me == 0 ? ms.x : m_ref, l1 = s_me == 0 ? ms.y : l;
         const float mx = fmaxf(m0, m1);
@@ -718,6 +723,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float den = l0 * a0 + l1 * a1;
         const float inv2 = den > 0.f ? 1.f / den : 0.f;
         const float w0 = a0 * inv2, w1 = a1 * inv2;  // split 0's and split 1's weight
+        const float w_me = s_me == 0 ? w0 : w1;                          // on this CTA's O
+        const float w_sib = s_me == 0 ? w1 * l1 : w0 * l0;               // on the sibling's O / l
 #pragma unroll 1
         for (int q = 0; q < 4; ++q) {
           uint32_t v[32];
@@ -732,18 +739,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint4* dst = (uint4*)(p.out + ((int64_t)tok * H + h) * kValueDim + 256 * (int)c + 128 * s_me + 32 * q);
           uint32_t packed[16];
 #pragma unroll
-          for (int u = 0; u < 8; ++u) {
-            const uint4 r = *(const uint4*)(inbox + h * 512 + (((8 * q + u) ^ (h & 31)) << 4));
+          for (int u = 0; u < 4; ++u) {  // 8 columns per chunk
+            const uint4 r = *(const uint4*)(inbox + h * 256 + (((4 * q + u) ^ (h & 15)) << 4));
             const uint32_t rr[4] = {r.x, r.y, r.z, r.w};
-            float o[4];
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-              const float mine = __uint_as_float(v[4 * u + i]), theirs = __uint_as_float(rr[i]);
-              const float x0 = s_me == 0 ? mine : theirs, x1 = s_me == 0 ? theirs : mine;
-              o[i] = fmaf(x1, w1, x0 * w0);  // the same expression in both CTAs
+              float y0, y1;
+              f16x2_to_f32(rr[i], y0, y1);
+              const float o0 = fmaf(y0, w_sib, __uint_as_float(v[8 * u + 2 * i]) * w_me);
+              const float o1 = fmaf(y1, w_sib, __uint_as_float(v[8 * u + 2 * i + 1]) * w_me);
+              packed[4 * u + i] = pack_bf16x2(o0, o1);
             }
-            packed[2 * u] = pack_bf16x2(o[0], o[1]);
-            packed[2 * u + 1] = pack_bf16x2(o[2], o[3]);
           }
 #pragma unroll
           for (int j = 0; j < 4; ++j)
