@@ -25,13 +25,15 @@
 //     then rescaled in tensor memory.
 //   * P (bf16) goes to shared memory; O[128 x 256] += P . V with V read MN-major from
 //     the same shared-memory rows the logits used.
-// Warp roles (twelve warps): warps 0-2 gather rows with TMA gather4 into a 4-stage ring
+// Warp roles (sixteen warps): warps 0-2 gather rows with TMA gather4 into a 4-stage ring
 // of swizzled rows, each lane issuing its own gathers (a gather's cost is in its issue);
 // warp 3 (converged, one elected lane) issues each MMA as soon as its inputs are ready;
-// warps 4-7 (senders) load each tile's partial logits, stage the rounded values for the
-// finishing warps and send them to the peer; warps 8-11 (finishers) add the peer's part,
-// run the softmax, store P and run the epilogue.  Sending tile n + 1 and finishing tile n
-// thus run at the same time.  Tensor memory (512 columns): O [0,256), two logit buffers
+// warps 4-7 (senders) load each tile's partial logits, round them and send them to the
+// peer; warps 8-11 and 12-15 (finishers) take key columns 0-31 and 32-63 of each tile:
+// each rounds its own half of the logits as the senders do, adds the peer's part, meets
+// its partner warp (same 32 head rows) to share the row maxima, runs its half of the
+// softmax and stores its half of P; warps 8-11 then run the epilogue.  Sending tile
+// n + 1 and finishing tile n thus run at the same time.  Tensor memory (512 columns): O [0,256), two logit buffers
 // S0 [256,320) and S1 [320,384), Q latent [384,512).  Tile n uses logit buffer n & 1;
 // its P (bf16) is written over the peer's partial logits of tile n in the receive
 // buffer n & 1 (same 128-byte-swizzled rows, each thread its own row), and P.V(n)'s
@@ -51,10 +53,11 @@ namespace {
 using namespace sm100;
 
 constexpr int kGatherWarps = 3;                  // warps 0-2 gather (TMA), warp 3 issues MMAs
-constexpr int kMmaWarp = kGatherWarps;           // warps 4-7 run softmax and the epilogue
-constexpr int kSendWarp0 = kMmaWarp + 1;          // warps 4-7 load and send the partial logits,
+constexpr int kMmaWarp = kGatherWarps;
+constexpr int kSendWarp0 = kMmaWarp + 1;          // warps 4-7 load and send the partial logits
 constexpr int kFinWarp0 = kSendWarp0 + 4;         // warps 8-11 finish key columns 0-31 of each tile and run
-constexpr int kFinWarpB0 = kFinWarp0 + 4;         // the epilogue; warps 12-15 finish columns 32-63
+                                                  // the epilogue
+constexpr int kFinWarpB0 = kFinWarp0 + 4;         // warps 12-15 finish key columns 32-63
 constexpr int kThreads = (kFinWarpB0 + 4) * 32;
 constexpr int kTok = 64;                         // selected positions per tile
 constexpr int kStages = 4;
@@ -81,7 +84,7 @@ constexpr uint32_t kMergeThreads = 5 * 32;                 // gather warp 0 + th
 // Sibling merge (two splits in one cluster): outbox and inbox of 128 rows x 128 f32
 // columns plus 128 (m, l) pairs each, in the stage buffers.
 constexpr uint32_t kSibBytes = 128 * 256 + 128 * 8;  // 128 rows x 128 fp16 columns, then (m, l) per row
-static_assert(2 * kSibBytes <= kStages * kStageBytes, "sibling merge buffers fit in the stage buffers");                 // gather warp 0 + the four softmax warps
+static_assert(2 * kSibBytes <= kStages * kStageBytes, "sibling merge buffers fit in the stage buffers");
 
 // Launched in clusters of two CTAs (the pair), or four (two splits x the pair) when the
 // two splits of a token merge inside the cluster.
@@ -120,7 +123,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* m_ready = q_tma + 1;  // sibling merge: the sibling's inbox is free
   uint64_t* m_full = m_ready + 1; // sibling merge: the sibling's columns arrived
   uint64_t* mfull = m_full + 1;   // [4]: split merge, a chunk of another split's partial landed
-  uint64_t* mempty = mfull + 4;  // [4]: the softmax warps are done with that chunk buffer
+  uint64_t* mempty = mfull + 4;  // [4]: the merging warps (8-11) are done with that chunk buffer
   uint32_t* tmem_base_s = (uint32_t*)(mempty + 4);
   volatile int* abort_flag = (volatile int*)(tmem_base_s + 1);
   volatile int* last_s = (volatile int*)(abort_flag + 1);  // this CTA merges the splits
@@ -290,7 +293,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int stage = n % kStages;
         bool good = true;
         if (lane == 0) {
-          // stage buffers 2-3 hold Q until the softmax warps have moved it to tensor memory
+          // stage buffers 2-3 hold Q until the sending warps have moved it to tensor memory
           if (n == 2) good = mbar_wait(q_ready, 0, abort_flag, p.err);
           if (good) good = mbar_wait(&kv_empty[stage], ((n / kStages) & 1) ^ 1, abort_flag, p.err);
           if (good) mbar_arrive_expect_tx(&kv_full[stage], my_bytes);
@@ -783,7 +786,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // order and with the same arithmetic for its own part (from tensor memory) as for
       // the others (streamed in by warp 0), so the result does not depend on which CTA
       // finished last; it then resets the counter for the next call.  Both barriers are
-      // passed by warp 0 and all four softmax warps whatever happened before.
+      // passed by warp 0 and warps 8-11 whatever happened before.
       named_bar_sync(1, kMergeThreads);
       if (warp == kFinWarp0 && lane == 0) {
         const uint32_t prev = atomicAdd(p.merge_cnt + tok * 2 + c, 1u);
