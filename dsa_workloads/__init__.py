@@ -138,8 +138,17 @@ SMALL_MID = Spec(
     idx_heads=64, idx_dim=128, topk=512, sfa_heads=128, seed=7008,
     description="longest row between 8K and 16K keys (the selection's four-CTA clusters)")
 
+SMALL_SIB = Spec(
+    name="small_sib", mode="decode", batch=32,
+    seq_lens=(1, 2, 63, 64, 65, 100, 255, 256, 257, 300, 384, 511, 512, 513, 600, 700, 777, 900,
+              1000, 1024, 1200, 1500, 1800, 2000, 2048, 2100, 2500, 2800, 3000, 3100, 3500, 4000),
+    pool_pages=640, idx_heads=64, idx_dim=128, topk=512, sfa_heads=128, seed=7009,
+    description="32 rows, so each token's 512 selected rows run as two splits of four 64-row "
+                "tiles merged inside their cluster; rows up to 256 long leave the second split "
+                "empty, rows of 257-511 leave it partly padded")
+
 SMALL = [SMALL_DECODE_BF16, SMALL_DECODE_FP8, SMALL_DECODE_MX, SMALL_TIES, SMALL_PREFILL,
-         SMALL_H8, EMPTY_AND_SHORT, SMALL_MID]
+         SMALL_H8, EMPTY_AND_SHORT, SMALL_MID, SMALL_SIB]
 
 ALL = {s.name: s for s in HEADLINE + SMALL}
 
