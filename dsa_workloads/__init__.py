@@ -48,7 +48,8 @@ _S_LAYOUT, _S_LENS, _S_QI, _S_QSCALE, _S_W, _S_KI, _S_KSCALE, _S_KV, _S_QS, _S_K
 class Spec:
     """Shape and value recipe of one synthetic workload."""
     name: str
-    mode: str                      # "decode" (one query token per sequence) or "prefill"
+    mode: str                      # "decode" (one query token per sequence), "multi" (several
+                                   # per sequence at its last positions) or "prefill"
     batch: int
     seq_lens: tuple = ()           # explicit lengths; empty => drawn (see len_loguniform)
     len_loguniform: tuple = ()     # (lo, hi): L_b = floor(exp(U(ln lo, ln hi)))
@@ -64,6 +65,7 @@ class Spec:
     sfa_heads: int = 128
     seed: int = 0
     prefill_tokens: int = 0        # prefill: query tokens 0..T-1 of sequence 0
+    tokens_per_seq: int = 1        # multi: query tokens at positions L_b - m .. L_b - 1
     int_seed: Optional[int] = None  # seed for the integer / latent streams (defaults to seed)
     description: str = ""
 
@@ -147,8 +149,14 @@ SMALL_SIB = Spec(
                 "tiles merged inside their cluster; rows up to 256 long leave the second split "
                 "empty, rows of 257-511 leave it partly padded")
 
+SMALL_MULTI = Spec(
+    name="small_multi", mode="multi", batch=4, seq_lens=(70, 300, 1000, 2500), tokens_per_seq=4,
+    pool_pages=80, idx_heads=64, idx_dim=128, topk=256, sfa_heads=128, seed=7010,
+    description="multi-token decode: 4 query tokens per sequence at its last 4 positions "
+                "(a speculative draft), each seeing the prefix up to itself")
+
 SMALL = [SMALL_DECODE_BF16, SMALL_DECODE_FP8, SMALL_DECODE_MX, SMALL_TIES, SMALL_PREFILL,
-         SMALL_H8, EMPTY_AND_SHORT, SMALL_MID, SMALL_SIB]
+         SMALL_H8, EMPTY_AND_SHORT, SMALL_MID, SMALL_SIB, SMALL_MULTI]
 
 ALL = {s.name: s for s in HEADLINE + SMALL}
 
@@ -268,6 +276,12 @@ def make(spec: Spec, n_kv_chunk_pages: int = 1024, with_latent: bool = True) -> 
         T = B
         q_seq = np.arange(B, dtype=np.int32)
         q_pos = (lens - 1).astype(np.int32)  # -1 for an empty sequence
+    elif spec.mode == "multi":
+        m = spec.tokens_per_seq
+        assert m >= 1 and np.all(lens >= m), f"{spec.name}: every sequence needs {m} positions"
+        T = B * m
+        q_seq = np.repeat(np.arange(B, dtype=np.int32), m)
+        q_pos = (np.repeat(lens, m) - m + np.tile(np.arange(m), B)).astype(np.int32)
     else:
         assert B == 1 and spec.prefill_tokens <= int(lens[0])
         T = spec.prefill_tokens

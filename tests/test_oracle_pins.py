@@ -171,7 +171,7 @@ def test_mx_scores_group_by_group():
 # invariants: causality, counts, duplicates, page placement
 # ---------------------------------------------------------------------------------
 @pytest.mark.parametrize("spec", [W.SMALL_DECODE_BF16, W.SMALL_PREFILL, W.EMPTY_AND_SHORT,
-                                  W.SMALL_TIES])
+                                  W.SMALL_TIES, W.SMALL_MULTI])
 def test_selection_invariants(spec):
     wl = W.make(spec)
     toks = range(wl.n_tokens) if wl.n_tokens <= 64 else list(range(0, 40)) + list(range(wl.n_tokens - 24, wl.n_tokens))
@@ -233,6 +233,21 @@ def test_sfa_with_k_at_least_l_is_dense_causal_attention():
         idx, _, out = O.step(wl, tok)
         assert idx[:tok + 1].tolist() == list(range(tok + 1))
         assert np.allclose(out, ref[tok], rtol=0, atol=1e-12)
+
+
+def test_multi_token_draft_sees_its_own_prefix():
+    """Multi-token decode: the m query tokens of a sequence sit at its last m positions
+    and token j sees positions 0 .. L - m + j only; where that prefix is shorter than K
+    it selects all of it, so consecutive draft tokens select nested prefixes."""
+    wl = W.make(W.SMALL_MULTI)
+    m = W.SMALL_MULTI.tokens_per_seq
+    L0 = int(wl.seq_lens[0])
+    assert L0 <= W.SMALL_MULTI.topk
+    for j in range(m):
+        idx, _ = O.indexer_topk(wl, j)  # tokens 0 .. m - 1 belong to sequence 0
+        assert int(wl.q_pos[j]) == L0 - m + j
+        n = L0 - m + j + 1
+        assert np.array_equal(idx[:n], np.arange(n)) and np.all(idx[n:] == -1)
 
 
 def test_prefill_row0_attends_to_key0_only():
