@@ -49,7 +49,7 @@
 extern "C" {
 #endif
 
-#define DSA_ABI_VERSION 1
+#define DSA_ABI_VERSION 2
 
 /* A cudaStream_t, kept opaque so that this header needs no CUDA header. */
 typedef struct CUstream_st* dsa_stream_t;
@@ -237,6 +237,40 @@ dsa_status_t dsa_indexer_topk_noalloc(const dsa_indexer_args_t* args,
                                       const dsa_tokens_t* tokens,
                                       int32_t* out_idx, float* out_score,
                                       dsa_stream_t stream);
+
+/* ---- Index prolog without weights: dynamic MXFP8 quantisation ------------------- */
+/* MXFP8 with groups of 32 ("Day0 Inference Optimization on Ascend CANN", section 3,
+ * "Full Quantization of LI with MXFP8"; "Adapting and Optimizing Inference for a New
+ * Model Architecture on Ascend", section 4.2).  The pages leave the scale rule open; the
+ * library takes the OCP microscaling one: each group of 32 consecutive elements of a
+ * row shares the E8M0 scale 2^e with e = floor(log2(amax)) - 8 (amax: the group's
+ * largest magnitude), clamped to [-127, 127], and e = -127 for an all-zero group; each
+ * element is stored as the E4M3 value nearest x / 2^e, ties to even, saturating at
+ * +-448.  Inputs must be finite.  The result is the layout the indexer reads with
+ * DSA_SCALE_MX_E8M0_G32. */
+
+/* Quantises n_rows rows of dim bf16 values, device x [n_rows, dim] (16-byte aligned;
+ * dim a multiple of 32, at most 8192), into device codes e4m3 [n_rows, dim] (8-byte
+ * aligned) and device scales E8M0 [n_rows, dim / 32]: e.g. the indexer query viewed as
+ * [T * n_heads, dim].  n_rows == 0 enqueues nothing.  The caller owns every buffer. */
+dsa_status_t dsa_quantize_mxfp8(const void* x, int64_t n_rows, int32_t dim,
+                                void* codes, void* scales, dsa_stream_t stream);
+
+/* Appends new keys to the paged MXFP8 K-index cache: the bf16 key of every token i,
+ * device k_new [T, dim] (16-byte aligned), is quantised as above and written to the
+ * cache row of token i's position: page block_table[b * max_pages_per_seq + pos / 64],
+ * slot pos % 64, in cache_codes (device e4m3 [num_pages, 64, dim], 16-byte aligned) and
+ * cache_scales (device E8M0 [num_pages, 64, dim / 32]).  b = token_seq[i] (or i) and
+ * pos = token_pos[i], or seq_lens[b] - 1 when token_pos is NULL (the newest stored
+ * position).  dim: 64 or 128 (the indexer's).  A position outside the page table sets
+ * DSA_DEVERR_TOKEN, a page id outside [0, num_pages) DSA_DEVERR_PAGE_ID, in ws's error
+ * word; that token is skipped and the others are written.  ws: 256-byte aligned, at
+ * least 256 bytes (only the error word is used; it is not cleared by the call). */
+dsa_status_t dsa_index_cache_append_mxfp8(const void* k_new, int32_t dim,
+                                          const dsa_page_table_t* pages,
+                                          const dsa_tokens_t* tokens,
+                                          void* cache_codes, void* cache_scales,
+                                          void* ws, size_t ws_bytes, dsa_stream_t stream);
 
 /* ---- Errors and introspection --------------------------------------------------- */
 /* Copies the device error word out of ws (synchronises `stream`) into *err. */

@@ -82,6 +82,11 @@ def _load() -> C.CDLL:
     lib.dsa_fused_decode.argtypes = [P(IndexerArgs), P(IndexCache), P(SfaArgs), P(LatentCache),
                                      P(PageTable), P(Tokens), _vp, _vp, _vp, sz, _vp, P(Trace)]
     lib.dsa_fused_decode.restype = C.c_int
+    lib.dsa_quantize_mxfp8.argtypes = [_vp, C.c_int64, C.c_int32, _vp, _vp, _vp]
+    lib.dsa_quantize_mxfp8.restype = C.c_int
+    lib.dsa_index_cache_append_mxfp8.argtypes = [_vp, C.c_int32, P(PageTable), P(Tokens), _vp, _vp, _vp,
+                                                 C.c_size_t, _vp]
+    lib.dsa_index_cache_append_mxfp8.restype = C.c_int
     lib.dsa_read_device_error.argtypes = [_vp, P(C.c_uint32), _vp]
     lib.dsa_read_device_error.restype = C.c_int
     lib.dsa_clear_device_error.argtypes = [_vp, _vp]
@@ -112,7 +117,8 @@ def _check(status: int, where: str):
 
 from ._api import (  # noqa: E402  (needs `lib` above)
     DeviceInputs, Plan, indexer_topk, sparse_attn, fused_decode, read_device_error,
-    clear_device_error, workspace_size, alloc_workspace)
+    clear_device_error, workspace_size, alloc_workspace, quantize_mxfp8, index_cache_append_mxfp8)
 
 __all__ = ["lib", "DsaError", "DeviceInputs", "Plan", "indexer_topk", "sparse_attn", "fused_decode",
-           "read_device_error", "clear_device_error", "workspace_size", "alloc_workspace", "Trace"]
+           "read_device_error", "clear_device_error", "workspace_size", "alloc_workspace", "Trace",
+           "quantize_mxfp8", "index_cache_append_mxfp8"]

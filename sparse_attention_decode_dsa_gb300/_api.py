@@ -140,3 +140,40 @@ def read_device_error(ws: torch.Tensor, stream=None) -> int:
 
 def clear_device_error(ws: torch.Tensor, stream=None):
     _check(lib.dsa_clear_device_error(_ptr(ws), _stream_ptr(stream)), "dsa_clear_device_error")
+
+
+def quantize_mxfp8(x: torch.Tensor, codes: Optional[torch.Tensor] = None, scales: Optional[torch.Tensor] = None,
+                   stream=None):
+    """MXFP8 (groups of 32) of bf16 rows x [..., dim] -> (e4m3 codes uint8 [..., dim], E8M0
+    scales uint8 [..., dim / 32]), computed by the library's kernel."""
+    assert x.is_cuda and x.element_size() == 2 and x.is_contiguous()
+    dim = int(x.shape[-1])
+    rows = x.numel() // dim if dim else 0
+    if codes is None:
+        codes = torch.empty(x.shape, dtype=torch.uint8, device=x.device)
+    if scales is None:
+        scales = torch.empty(x.shape[:-1] + (dim // 32,), dtype=torch.uint8, device=x.device)
+    _check(lib.dsa_quantize_mxfp8(_ptr(x), rows, dim, _ptr(codes), _ptr(scales), _stream_ptr(stream)),
+           "dsa_quantize_mxfp8")
+    return codes, scales
+
+
+def index_cache_append_mxfp8(k_new: torch.Tensor, cache_codes: torch.Tensor, cache_scales: torch.Tensor,
+                             block_table: torch.Tensor, seq_lens: torch.Tensor, seq_lens_host: torch.Tensor,
+                             ws: torch.Tensor, token_seq: Optional[torch.Tensor] = None,
+                             token_pos: Optional[torch.Tensor] = None, token_seq_host: Optional[torch.Tensor] = None,
+                             token_pos_host: Optional[torch.Tensor] = None, stream=None):
+    """Quantises the new key of every token (bf16 k_new [T, dim]) and writes it to that
+    token's (page, slot) of the paged MXFP8 cache (codes [pages, 64, dim], scales
+    [pages, 64, dim / 32]).  Token i is batch row token_seq[i] (or i) at position
+    token_pos[i] (or seq_len - 1)."""
+    assert k_new.is_cuda and k_new.element_size() == 2 and k_new.is_contiguous()
+    B, maxp = block_table.shape
+    pages = PageTable(_ptr(block_table), _ptr(seq_lens), _i32_host_ptr(seq_lens_host), B, maxp, 64,
+                      int(cache_codes.shape[0]))
+    tokens = Tokens(int(k_new.shape[0]), _ptr(token_seq), _ptr(token_pos), _i32_host_ptr(token_seq_host),
+                    _i32_host_ptr(token_pos_host))
+    _check(lib.dsa_index_cache_append_mxfp8(_ptr(k_new), int(k_new.shape[-1]), C.byref(pages), C.byref(tokens),
+                                            _ptr(cache_codes), _ptr(cache_scales), _ptr(ws),
+                                            ws.numel() * ws.element_size(), _stream_ptr(stream)),
+           "dsa_index_cache_append_mxfp8")

@@ -469,6 +469,52 @@ dsa_status_t dsa_fused_decode(const dsa_indexer_args_t* iargs, const dsa_index_c
   return st;
 }
 
+dsa_status_t dsa_quantize_mxfp8(const void* x, int64_t n_rows, int32_t dim, void* codes, void* scales,
+                                dsa_stream_t stream) {
+  if (!x || !codes || !scales) return fail(DSA_ERR_INVALID_ARG, "x, codes and scales are required");
+  if (n_rows < 0 || n_rows > INT32_MAX) return fail(DSA_ERR_INVALID_ARG, "n_rows = %lld outside [0, 2^31)", (long long)n_rows);
+  if (dim < 32 || dim > 8192 || dim % 32)
+    return fail(DSA_ERR_INVALID_ARG, "dim = %d: a multiple of 32 in [32, 8192]", dim);
+  if (((uintptr_t)x) % 16 || ((uintptr_t)codes) % 8)
+    return fail(DSA_ERR_INVALID_ARG, "x must be 16-byte and codes 8-byte aligned");
+  Mxfp8Params p{};
+  p.x = (const uint16_t*)x;
+  p.n_rows = n_rows;
+  p.dim = dim;
+  p.codes = (uint8_t*)codes;
+  p.scales = (uint8_t*)scales;
+  p.append = false;
+  cudaError_t e = launch_mxfp8_quant(p, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "MXFP8 quantisation launch");
+  return DSA_OK;
+}
+
+dsa_status_t dsa_index_cache_append_mxfp8(const void* k_new, int32_t dim, const dsa_page_table_t* pages,
+                                          const dsa_tokens_t* tokens, void* cache_codes, void* cache_scales,
+                                          void* ws, size_t ws_bytes, dsa_stream_t stream) {
+  if (!k_new || !cache_codes || !cache_scales)
+    return fail(DSA_ERR_INVALID_ARG, "k_new, cache_codes and cache_scales are required");
+  if (dim != 64 && dim != 128) return fail(DSA_ERR_UNSUPPORTED, "dim must be 64 or 128 (got %d)", dim);
+  if (((uintptr_t)k_new) % 16 || ((uintptr_t)cache_codes) % 16)
+    return fail(DSA_ERR_INVALID_ARG, "k_new and cache_codes must be 16-byte aligned");
+  int32_t mv = 0;
+  dsa_status_t st = check_pages_tokens(pages, tokens, &mv);
+  if (st != DSA_OK) return st;
+  if ((st = check_ws(ws, ws_bytes, kAlign)) != DSA_OK) return st;
+  Mxfp8Params p{};
+  p.x = (const uint16_t*)k_new;
+  p.n_rows = tokens->n_tokens;
+  p.dim = dim;
+  p.codes = (uint8_t*)cache_codes;
+  p.scales = (uint8_t*)cache_scales;
+  p.append = true;
+  p.tv = token_view(pages, tokens, mv);
+  p.err = (uint32_t*)ws;
+  cudaError_t e = launch_mxfp8_quant(p, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "K-index append launch");
+  return DSA_OK;
+}
+
 dsa_status_t dsa_read_device_error(const void* ws, uint32_t* err, dsa_stream_t stream) {
   if (!ws || !err) return fail(DSA_ERR_INVALID_ARG, "ws and err are required");
   cudaError_t e = cudaMemcpyAsync(err, ws, sizeof(uint32_t), cudaMemcpyDeviceToHost, (cudaStream_t)stream);

@@ -149,4 +149,18 @@ cudaError_t launch_topk(const TopkParams& p, int32_t max_visible, cudaStream_t s
 cudaError_t launch_sfa_tc(const SfaParams& p, cudaStream_t s);
 cudaError_t launch_clear(void* p, size_t bytes, cudaStream_t s);  // bytes: multiple of 16
 
+// Index prolog: MXFP8 quantisation (groups of 32) of bf16 rows, written to row i of
+// codes / scales, or (append) to the cache row of token i's (page, slot).
+struct Mxfp8Params {
+  const uint16_t* x;   // [n_rows, dim] bf16, 16-byte aligned
+  int64_t n_rows;
+  int32_t dim;         // a multiple of 32
+  uint8_t* codes;      // [rows, dim] e4m3, 8-byte aligned
+  uint8_t* scales;     // [rows, dim / 32] E8M0
+  bool append;         // destination from (token_seq, token_pos) through the page table
+  TokenView tv;        // (append only)
+  uint32_t* err;       // (append only) device error word
+};
+cudaError_t launch_mxfp8_quant(const Mxfp8Params& p, cudaStream_t s);
+
 }  // namespace dsa

@@ -23,7 +23,7 @@ def test_exports_every_declared_symbol():
 
 
 def test_version_and_strings():
-    assert dsa.lib.dsa_abi_version() == 1
+    assert dsa.lib.dsa_abi_version() == 2
     assert dsa.lib.dsa_status_string(0) == b"DSA_OK"
     assert dsa.lib.dsa_status_string(3) == b"DSA_ERR_WORKSPACE"
 
@@ -90,6 +90,34 @@ def test_e4m3_needs_scales():
 def test_workspace_checks(ws, ws_bytes):
     pages, toks, cache, args, keep = _structs()
     assert _call_indexer(pages, toks, cache, args, ws=ws, ws_bytes=ws_bytes) == dsa.DSA_ERR_WORKSPACE
+
+
+@pytest.mark.parametrize("x, rows, dim, codes, status", [
+    (FAKE, 4, 48, FAKE, dsa.DSA_ERR_INVALID_ARG),       # dim not a multiple of 32
+    (FAKE, 4, 0, FAKE, dsa.DSA_ERR_INVALID_ARG),
+    (FAKE, -1, 128, FAKE, dsa.DSA_ERR_INVALID_ARG),
+    (0, 4, 128, FAKE, dsa.DSA_ERR_INVALID_ARG),          # missing input
+    (FAKE + 8, 4, 128, FAKE, dsa.DSA_ERR_INVALID_ARG),   # x not 16-byte aligned
+    (FAKE, 4, 128, FAKE + 4, dsa.DSA_ERR_INVALID_ARG),   # codes not 8-byte aligned
+    (FAKE, 0, 128, FAKE, dsa.DSA_OK),                     # nothing to do: nothing enqueued
+])
+def test_quantize_mxfp8_host_checks(x, rows, dim, codes, status):
+    st = dsa.lib.dsa_quantize_mxfp8(C.c_void_p(x) if x else None, rows, dim,
+                                    C.c_void_p(codes), C.c_void_p(FAKE), None)
+    assert st == status
+
+
+@pytest.mark.parametrize("dim, ws, ws_bytes, status", [
+    (96, FAKE, 256, dsa.DSA_ERR_UNSUPPORTED),
+    (128, 0, 256, dsa.DSA_ERR_WORKSPACE),
+    (128, FAKE, 100, dsa.DSA_ERR_WORKSPACE),
+])
+def test_index_cache_append_host_checks(dim, ws, ws_bytes, status):
+    pages, toks, cache, args, keep = _structs()
+    st = dsa.lib.dsa_index_cache_append_mxfp8(C.c_void_p(FAKE), dim, C.byref(pages), C.byref(toks),
+                                              C.c_void_p(FAKE), C.c_void_p(FAKE),
+                                              C.c_void_p(ws) if ws else None, ws_bytes, None)
+    assert st == status
 
 
 def test_sfa_rejects_bad_shapes():
