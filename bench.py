@@ -179,6 +179,67 @@ def _oracle_sample(wl, budget_s):
 
 
 # ---------------------------------------------------------------------------------------
+def run_prolog(args):
+    """The index prolog on its own: dsa_quantize_mxfp8 over the 8192-token prefill query
+    (8192 x 64 heads x 128 bf16, 134 MB: larger than L2) and dsa_index_cache_append_mxfp8
+    of one decode step's 32 new keys into a 16384-page MXFP8 cache.  Inputs resident in
+    HBM; CUDA events on the launch stream around K back-to-back launches."""
+    import torch
+    import sparse_attention_decode_dsa_gb300 as dsa
+    torch.manual_seed(0)
+    dev = torch.device("cuda", 0)
+    rows, dim = 8192 * 64, 128
+    x = (torch.randn(rows, dim, device=dev) * 4).to(torch.bfloat16)
+    codes = torch.empty(rows, dim, dtype=torch.uint8, device=dev)
+    scales = torch.empty(rows, dim // 32, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    for _ in range(max(3, args.warmup)):
+        dsa.quantize_mxfp8(x, codes, scales)
+    torch.cuda.synchronize()
+    b, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    b.record(stream)
+    for _ in range(args.steps):
+        dsa.quantize_mxfp8(x, codes, scales)
+    e.record(stream)
+    torch.cuda.synchronize()
+    q_us = b.elapsed_time(e) * 1e3 / args.steps
+    q_bytes = rows * dim * 2 + rows * dim + rows * dim // 32  # bf16 in, e4m3 + E8M0 out
+    # append: B = 32 sequences of 32768 positions over a 16384-page pool
+    B, L, pool = 32, 32768, 16384
+    maxp = L // 64
+    bt = torch.randperm(pool, device=dev).to(torch.int32).view(B, maxp)
+    lens_h = torch.full((B,), L, dtype=torch.int32)
+    lens = lens_h.to(dev)
+    cc = torch.zeros(pool, 64, dim, dtype=torch.uint8, device=dev)
+    cs = torch.zeros(pool, 64, dim // 32, dtype=torch.uint8, device=dev)
+    k_new = (torch.randn(B, dim, device=dev) * 4).to(torch.bfloat16)
+    ws = dsa.alloc_workspace(256)
+    for _ in range(max(3, args.warmup)):
+        dsa.index_cache_append_mxfp8(k_new, cc, cs, bt, lens, lens_h, ws)
+    torch.cuda.synchronize()
+    b.record(stream)
+    for _ in range(args.steps):
+        dsa.index_cache_append_mxfp8(k_new, cc, cs, bt, lens, lens_h, ws)
+    e.record(stream)
+    torch.cuda.synchronize()
+    a_us = b.elapsed_time(e) * 1e3 / args.steps
+    assert dsa.read_device_error(ws) == 0
+    peak, _, _, peak_src = _peaks()
+    achieved = q_bytes / (q_us * 1e-6) / 1e9
+    print(json.dumps({
+        "metric": "index prolog: MXFP8 quantisation GB/s (8192 x 64 x 128 bf16 rows)", "value": achieved,
+        "unit": "GB/s", "higher_is_better": True, "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "quantize_us": q_us, "append_32_keys_us": a_us, "dtype": "bf16 -> e4m3 + E8M0",
+        "roofline": {"kernel": "mxfp8_quant", "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "algorithmic_bytes": q_bytes,
+                     "peak_source": "measured (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured" else "fallback"},
+        "config": {"workload": "index_prolog", "rows": rows, "dim": dim, "group": 32,
+                   "append": {"batch": B, "context": L, "pool_pages": pool},
+                   "l2": "no flush: 134 MB in + 71 MB out per launch > L2"},
+        "data": "synthetic (torch.randn * 4, seeded)"}))
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -190,7 +251,11 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=0)
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--prolog", action="store_true",
+                    help="time the index prolog instead (MXFP8 quantisation, K-index append)")
     args = ap.parse_args()
+    if args.prolog:
+        return run_prolog(args)
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
