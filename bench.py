@@ -158,6 +158,22 @@ def _traffic(kernel, workload, units):
     return d["bytes_per_unit"] * units
 
 
+def max_over_ranks(ms, dist=None, device=None):
+    """The slowest rank's time in ms (all ranks get it); the local time without a group."""
+    if dist is None:
+        return float(ms)
+    import torch
+    t = torch.tensor([float(ms)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(world, units_per_rank, ms):
+    """Units all ranks processed (replicas: each rank the same count) per second, over
+    the slowest rank's time."""
+    return world * units_per_rank / (ms * 1e-3)
+
+
 def _cores():
     try:
         return len(os.sched_getaffinity(0))
@@ -341,11 +357,7 @@ def main():
     if dist:
         dist.barrier()
     clk = clocks.stop()
-    total_ms = t_begin.elapsed_time(t_end)
-    if dist:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(t_begin.elapsed_time(t_end), dist, dev)
     assert dsa.read_device_error(ws) == 0
 
     # traced pass (per-kernel durations)
@@ -392,7 +404,7 @@ def main():
                     else "fallback 1.7 PFLOP/s sustained"}
 
     ms_per_step = total_ms / args.steps
-    value = world * T * args.steps / (total_ms * 1e-3)
+    value = whole_job_rate(world, T * args.steps, total_ms)
 
     # ---- the same step replayed from a CUDA graph (host launch cost taken out) ----------
     graph = None
@@ -413,8 +425,8 @@ def main():
             g.replay()
         g_e.record()
         torch.cuda.synchronize()
-        g_ms = g_b.elapsed_time(g_e) / args.steps
-        graph = {"us_per_step": 1e3 * g_ms, "value": world * T / (g_ms * 1e-3), "unit": UNIT,
+        g_ms = g_b.elapsed_time(g_e) / args.steps  # this rank's (no collective inside the try)
+        graph = {"us_per_step": 1e3 * g_ms, "value": whole_job_rate(world, T, g_ms), "unit": UNIT,
                  "note": "one dsa_fused_decode captured once, replayed back to back"}
         assert dsa.read_device_error(ws) == 0
     except Exception as ex:  # report, do not fail the bench line
@@ -473,8 +485,8 @@ def main():
     stream.wait_stream(down_s)
     e_e.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = e_b.elapsed_time(e_e)
-    e2e_val = world * T * e2e_steps / (e2e_ms * 1e-3)
+    e2e_ms = max_over_ranks(e_b.elapsed_time(e_e), dist, dev)
+    e2e_val = whole_job_rate(world, T * e2e_steps, e2e_ms)
     assert dsa.read_device_error(ws) == 0
     assert torch.equal(sets[(e2e_steps - 1) % 2]["h_out"][0], out_idx.cpu()), "end-to-end indices differ"
 
