@@ -66,6 +66,8 @@ class Spec:
     seed: int = 0
     prefill_tokens: int = 0        # prefill: query tokens 0..T-1 of sequence 0
     tokens_per_seq: int = 1        # multi: query tokens at positions L_b - m .. L_b - 1
+    kv_format: str = "bf16"        # latent cache: "bf16", or "fp8_tile128" (latent dims e4m3
+                                   # with an f32 scale per 128-element tile, rope dims bf16)
     int_seed: Optional[int] = None  # seed for the integer / latent streams (defaults to seed)
     description: str = ""
 
@@ -155,6 +157,11 @@ SMALL_MULTI = Spec(
     description="multi-token decode: 4 query tokens per sequence at its last 4 positions "
                 "(a speculative draft), each seeing the prefix up to itself")
 
+# the attention kernels read a bf16 latent cache; this one exists for the oracle only
+SMALL_FP8_KV = replace(SMALL_DECODE_BF16, name="small_fp8_kv", kv_format="fp8_tile128", seed=7011,
+                       description="as small_decode_bf16 with an FP8 latent cache: e4m3 latent "
+                                   "dims with an f32 scale per 128-dim tile, bf16 rope dims")
+
 SMALL = [SMALL_DECODE_BF16, SMALL_DECODE_FP8, SMALL_DECODE_MX, SMALL_TIES, SMALL_PREFILL,
          SMALL_H8, EMPTY_AND_SHORT, SMALL_MID, SMALL_SIB, SMALL_MULTI]
 
@@ -212,9 +219,12 @@ class Workload:
     head_w: np.ndarray            # f32 [T, H_I]
     idx_k: np.ndarray             # u16 or u8 [num_pages, 64, d]
     idx_k_scale: Optional[np.ndarray]  # None | f32 [num_pages, 64] | u8 [num_pages, 64, d/32]
-    kv: np.ndarray                # u16 (bf16) [num_pages, 64, 576]
+    kv: np.ndarray                # u16 (bf16) [num_pages, 64, 576]; None for an FP8 cache
     sfa_q: np.ndarray             # u16 (bf16) [T, H, 576]
     extras: dict = field(default_factory=dict)
+    kv_codes: Optional[np.ndarray] = None  # FP8 cache: u8 (e4m3) [num_pages, 64, 512]
+    kv_scale: Optional[np.ndarray] = None  # FP8 cache: f32 [num_pages, 64, 4], one per 128 dims
+    kv_rope: Optional[np.ndarray] = None   # FP8 cache: u16 (bf16) [num_pages, 64, 64]
 
     @property
     def n_tokens(self) -> int:
@@ -354,6 +364,29 @@ def make(spec: Spec, n_kv_chunk_pages: int = 1024, with_latent: bool = True) -> 
         return Workload(spec=spec, seq_lens=lens, block_table=bt, num_pages=pool, q_seq=q_seq,
                         q_pos=q_pos, idx_q=idx_q, idx_q_scale=idx_q_scale, head_w=head_w,
                         idx_k=idx_k, idx_k_scale=idx_k_scale, kv=None, sfa_q=None)
+    sfa_q_bits = lambda: bf16_bits_from_f32(ri[_S_QS].standard_normal((T, H, KV_DIM), dtype=np.float32))
+    if spec.kv_format == "fp8_tile128":
+        # latent dims: integers in [-15, 15] as e4m3 (exact) times a power-of-two scale
+        # 2^u, u in [-4, -2], per 128-dim tile; rope dims N(0,1) -> bf16; dead slots NaN
+        g = ri[_S_KV]
+        codes = np.full((pool, PAGE_SIZE, V_DIM), E4M3_NAN, dtype=np.uint8)
+        scl = np.full((pool, PAGE_SIZE, V_DIM // 128), np.nan, dtype=np.float32)
+        rope = np.full((pool, PAGE_SIZE, KV_DIM - V_DIM), BF16_NAN, dtype=np.uint16)
+        enc = _int8_encoder("e4m3")
+        for p0 in range(0, used, n_kv_chunk_pages):
+            p1 = min(used, p0 + n_kv_chunk_pages)
+            n = p1 - p0
+            c = enc[g.integers(-15, 16, size=(n, PAGE_SIZE, V_DIM)).astype(np.int8).view(np.uint8)]
+            sc = np.ldexp(np.float32(1.0), g.integers(-4, -1, size=(n, PAGE_SIZE, V_DIM // 128))).astype(np.float32)
+            rp = bf16_bits_from_f32(g.standard_normal((n, PAGE_SIZE, KV_DIM - V_DIM), dtype=np.float32))
+            dead = ~live_logical[p0:p1]
+            c[dead], sc[dead], rp[dead] = E4M3_NAN, np.nan, BF16_NAN
+            codes[phys_pages[p0:p1]], scl[phys_pages[p0:p1]], rope[phys_pages[p0:p1]] = c, sc, rp
+        return Workload(spec=spec, seq_lens=lens, block_table=bt, num_pages=pool, q_seq=q_seq,
+                        q_pos=q_pos, idx_q=idx_q, idx_q_scale=idx_q_scale, head_w=head_w,
+                        idx_k=idx_k, idx_k_scale=idx_k_scale, kv=None, sfa_q=sfa_q_bits(),
+                        kv_codes=codes, kv_scale=scl, kv_rope=rope)
+    assert spec.kv_format == "bf16", spec.kv_format
     kv = np.empty((pool, PAGE_SIZE, KV_DIM), dtype=np.uint16)
     kv[...] = BF16_NAN
     g = ri[_S_KV]
@@ -362,7 +395,7 @@ def make(spec: Spec, n_kv_chunk_pages: int = 1024, with_latent: bool = True) -> 
         chunk = bf16_bits_from_f32(g.standard_normal((p1 - p0, PAGE_SIZE, KV_DIM), dtype=np.float32))
         chunk[~live_logical[p0:p1]] = BF16_NAN
         kv[phys_pages[p0:p1]] = chunk
-    sfa_q = bf16_bits_from_f32(ri[_S_QS].standard_normal((T, H, KV_DIM), dtype=np.float32))
+    sfa_q = sfa_q_bits()
 
     return Workload(spec=spec, seq_lens=lens, block_table=bt, num_pages=pool, q_seq=q_seq,
                     q_pos=q_pos, idx_q=idx_q, idx_q_scale=idx_q_scale, head_w=head_w,
@@ -394,6 +427,10 @@ def with_block_table(wl: Workload, new_bt_pages: np.ndarray, new_pool: int) -> W
     ks = None
     if wl.idx_k_scale is not None:
         ks = move(wl.idx_k_scale, np.nan if wl.idx_k_scale.dtype == np.float32 else E8M0_NAN)
+    fp8 = wl.kv_codes is not None
     return replace(wl, block_table=bt, num_pages=new_pool,
                    idx_k=move(wl.idx_k, BF16_NAN if isbf else E4M3_NAN), idx_k_scale=ks,
-                   kv=move(wl.kv, BF16_NAN))
+                   kv=None if fp8 else move(wl.kv, BF16_NAN),
+                   kv_codes=move(wl.kv_codes, E4M3_NAN) if fp8 else None,
+                   kv_scale=move(wl.kv_scale, np.nan) if fp8 else None,
+                   kv_rope=move(wl.kv_rope, BF16_NAN) if fp8 else None)

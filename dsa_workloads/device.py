@@ -19,6 +19,9 @@ def _dev(a, device, dtype=None):
 
 def to_device(wl, device="cuda", with_latent=True):
     from sparse_attention_decode_dsa_gb300 import DeviceInputs
+    if with_latent and wl.kv is None and wl.kv_codes is not None:
+        raise NotImplementedError("the attention kernels read a bf16 latent cache; "
+                                  "the FP8 latent layout exists in the oracle only")
     decode = wl.spec.mode == "decode"
     bf = torch.bfloat16
     kbits = torch.bfloat16 if wl.idx_k.dtype == np.uint16 else torch.uint8

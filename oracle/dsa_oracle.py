@@ -186,11 +186,32 @@ def sparse_attention(q: np.ndarray, rows: np.ndarray, scale: float, v_dim: int =
     return p @ rows[:, :v_dim]
 
 
+def decode_latent_fp8(codes: np.ndarray, scales: np.ndarray, rope_bits: np.ndarray) -> np.ndarray:
+    """FP8 latent rows -> float64 [..., 576]: each e4m3 latent element times the f32 scale
+    of its 128-element tile (element j uses scale j // 128), followed by the bf16 rope
+    dims.  FP8 quantisation of the SFA cache per token and head in tiles of 128 elements
+    ("Day0 Inference Optimization on Ascend CANN", section 3, "FP8 Block Quantization
+    for SFA KV Cache"; "Adapting and Optimizing Inference ...", section 4.3); the latent
+    row has no heads, and the pages do not say how the 64 rope dims are stored: bf16
+    here."""
+    lat = decode_e4m3(codes) * np.repeat(np.asarray(scales, dtype=np.float64), 128, axis=-1)
+    return np.concatenate([lat, decode_bf16(rope_bits)], axis=-1)
+
+
+def latent_rows(wl, b: int, positions: np.ndarray) -> np.ndarray:
+    """float64 latent rows [n, 576] of sequence b at the given positions (bf16 or FP8 cache)."""
+    bt = wl.block_table[b]
+    if wl.kv is not None:
+        return decode_bf16(logical_rows(wl.kv, bt, positions))
+    return decode_latent_fp8(logical_rows(wl.kv_codes, bt, positions), logical_rows(wl.kv_scale, bt, positions),
+                             logical_rows(wl.kv_rope, bt, positions))
+
+
 def sfa(wl, token: int, idx: np.ndarray) -> np.ndarray:
     """Sparse Flash Attention of one query token over its index list, [H, 512] float64."""
     b = int(wl.q_seq[token])
     sel = idx[idx >= 0]
-    rows = decode_bf16(logical_rows(wl.kv, wl.block_table[b], sel))
+    rows = latent_rows(wl, b, sel)
     return sparse_attention(decode_bf16(wl.sfa_q[token]), rows, wl.spec.softmax_scale)
 
 

@@ -15,7 +15,7 @@ from tests import test_oracle_pins as P
 _orig = {name: getattr(O, name) for name in
          ["index_scores", "topk_select", "sparse_attention", "visible_count",
           "dequant_index_keys", "dequant_index_query", "logical_rows", "decode_e4m3",
-          "decode_e8m0", "decode_bf16"]}
+          "decode_e8m0", "decode_bf16", "decode_latent_fp8"]}
 
 
 def _scores_no_weights(q, w, k, act="identity"):
@@ -100,6 +100,16 @@ def _e8m0_bias126(bits):
     return _orig["decode_e8m0"](bits) * 2.0
 
 
+def _latent_fp8_tile64(codes, scales, rope_bits):
+    sc = np.asarray(scales, dtype=np.float64)
+    lat = O.decode_e4m3(codes) * np.repeat(np.concatenate([sc, sc], axis=-1), 64, axis=-1)
+    return np.concatenate([lat, O.decode_bf16(rope_bits)], axis=-1)
+
+
+def _latent_fp8_no_scale(codes, scales, rope_bits):
+    return _orig["decode_latent_fp8"](codes, np.ones_like(scales), rope_bits)
+
+
 MUTANTS = {
     "scores: head weights dropped": ("index_scores", _scores_no_weights),
     "scores: head weights misaligned": ("index_scores", _scores_reversed_weights),
@@ -117,6 +127,8 @@ MUTANTS = {
     "paging: page table ignored": ("logical_rows", _logical_rows_unpaged),
     "e4m3: exponent bias 8": ("decode_e4m3", _e4m3_bias8),
     "e8m0: exponent bias 126": ("decode_e8m0", _e8m0_bias126),
+    "fp8 latent: tiles of 64 elements": ("decode_latent_fp8", _latent_fp8_tile64),
+    "fp8 latent: tile scale dropped": ("decode_latent_fp8", _latent_fp8_no_scale),
 }
 
 PINS = [
@@ -132,6 +144,7 @@ PINS = [
     lambda: P.test_paged_equals_contiguous(W.SMALL_H8),
     P.test_sfa_with_k_at_least_l_is_dense_causal_attention,
     P.test_prefill_row0_attends_to_key0_only,
+    P.test_fp8_latent_decode_closed_form,
 ]
 
 

@@ -186,7 +186,7 @@ def test_selection_invariants(spec):
         assert not np.isnan(sc[:sel.shape[0]]).any()     # never touched a NaN slot
 
 
-@pytest.mark.parametrize("spec", [W.SMALL_DECODE_MX, W.SMALL_PREFILL, W.SMALL_H8])
+@pytest.mark.parametrize("spec", [W.SMALL_DECODE_MX, W.SMALL_PREFILL, W.SMALL_H8, W.SMALL_FP8_KV])
 def test_paged_equals_contiguous(spec):
     wl = W.make(spec)
     npg = (wl.seq_lens + 63) // 64
@@ -383,3 +383,47 @@ def test_fp8_decode_shares_integers_with_bf16_decode():
     c = W.make(W.FP8_DECODE, with_latent=False)
     assert np.array_equal(O.decode_bf16(a.idx_q), O.decode_e4m3(c.idx_q))
     assert np.array_equal(O.decode_bf16(a.idx_k[:64]), O.decode_e4m3(c.idx_k[:64]))
+
+
+# ---------------------------------------------------------------------------------
+# FP8 latent cache (e4m3 latent dims, an f32 scale per 128-dim tile, bf16 rope dims)
+# ---------------------------------------------------------------------------------
+def test_fp8_latent_decode_closed_form():
+    """Element j of the latent uses the scale of tile j // 128; rope dims are bf16."""
+    codes = np.zeros((1, 512), dtype=np.uint8)
+    codes[0, [0, 127, 128, 255, 256, 511]] = [0x38, 0x40, 0x38, 0xB8, 0x30, 0x44]  # 1, 2, 1, -1, 0.5, 3
+    scales = np.array([[0.25, 0.125, 8.0, 4.0]], dtype=np.float32)
+    rope = np.zeros((1, 64), dtype=np.uint16)
+    rope[0, 0], rope[0, 63] = 0x3F80, 0xC000  # 1.0, -2.0
+    row = O.decode_latent_fp8(codes, scales, rope)[0]
+    assert row.shape == (576,)
+    assert row[0] == 0.25 and row[127] == 0.5 and row[128] == 0.125 and row[255] == -0.125
+    assert row[256] == 4.0 and row[511] == 12.0
+    assert row[512] == 1.0 and row[575] == -2.0
+    assert np.count_nonzero(row) == 8
+
+
+def test_fp8_latent_sfa_equals_bf16_sfa_of_the_same_values():
+    """The FP8 cache holds integers in [-15, 15] times powers of two, which bf16 also
+    holds exactly: written as a bf16 cache, every token's attention is the same."""
+    wl = W.make(W.SMALL_FP8_KV)
+    vals = O.decode_latent_fp8(wl.kv_codes, wl.kv_scale, wl.kv_rope)  # NaN in dead slots
+    bits = W.bf16_bits_from_f32(vals.astype(np.float32))
+    assert np.array_equal(O.decode_bf16(bits), vals, equal_nan=True)  # exact re-encoding
+    wl_bf = W.replace(wl, kv=bits, kv_codes=None, kv_scale=None, kv_rope=None)
+    for tok in range(wl.n_tokens):
+        idx, _ = O.indexer_topk(wl, tok)
+        assert np.array_equal(O.sfa(wl, tok, idx), O.sfa(wl_bf, tok, idx))
+
+
+def test_fp8_latent_workload_values():
+    """The generator's FP8 latent: finite integer e4m3 codes in [-15, 15] on live slots,
+    power-of-two tile scales in [2^-4, 2^-2], NaN on dead slots (a stray read shows)."""
+    wl = W.make(W.SMALL_FP8_KV)
+    live = ~np.isnan(wl.kv_scale[..., 0])
+    v = O.decode_e4m3(wl.kv_codes[live])
+    assert np.all(np.isfinite(v)) and np.all(v == np.round(v)) and np.abs(v).max() <= 15
+    sc = wl.kv_scale[live]
+    assert np.all(np.isin(sc, [2.0 ** -4, 2.0 ** -3, 2.0 ** -2]))
+    assert np.all(np.isnan(O.decode_e4m3(wl.kv_codes[~live])))
+
