@@ -63,6 +63,8 @@ def algorithmic(wl):
     k_row = s.idx_dim * k_elem + (4 if s.idx_scale == "per_token" else (s.idx_dim // 32 if s.idx_scale == "mx" else 0))
     if s.mode == "decode":
         key_tokens = int(vis.sum())            # every visible key row read once
+    elif s.mode == "multi":
+        key_tokens = int(wl.seq_lens.sum())    # each sequence's keys read once for all its draft tokens
     else:
         key_tokens = int(wl.seq_lens[0])       # the prefix is read once (shared by all rows)
     q_bytes = T * s.idx_heads * s.idx_dim * k_elem + T * s.idx_heads * 4

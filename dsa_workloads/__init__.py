@@ -111,6 +111,25 @@ RAGGED_MXFP8_DECODE = Spec(
 
 HEADLINE = [TINY_DECODE, BF16_DECODE, FP8_DECODE, CAUSAL_PREFILL, RAGGED_MXFP8_DECODE]
 
+# The causal prefill with a quantised indexer (both operators run quantised in prefill
+# as well as decode): the same integers, K-index and query in e4m3 with per-token f32
+# scales, or MXFP8 with the ragged decode's scale recipe
+CAUSAL_PREFILL_FP8 = replace(
+    CAUSAL_PREFILL, name="causal_prefill_fp8", idx_dtype="e4m3", idx_scale="per_token", seed=1006,
+    int_seed=1004,
+    description="as causal_prefill, indexer q and K-index e4m3 with per-token f32 power-of-two scales")
+CAUSAL_PREFILL_MX = replace(
+    CAUSAL_PREFILL, name="causal_prefill_mxfp8", idx_dtype="e4m3", idx_scale="mx", head_w_exps=(-3, 0),
+    seed=1007, int_seed=1004,
+    description="as causal_prefill, MXFP8 indexer (E8M0 per 32) with the ragged decode's scale recipe")
+# Multi-token decode at the BF16 decode's sizes: 4 draft tokens per sequence at its last
+# four positions (the rows of a sequence share one K-index stream)
+BF16_MULTI_DECODE = replace(
+    BF16_DECODE, name="bf16_multi_decode", mode="multi", tokens_per_seq=4, seed=1008, int_seed=1002,
+    description="as bf16_decode with 4 query tokens per sequence at its last 4 positions (128 tokens)")
+
+EXTRA = [CAUSAL_PREFILL_FP8, CAUSAL_PREFILL_MX, BF16_MULTI_DECODE]
+
 # ---------------------------------------------------------------------------------
 # Small parity cases: several tiles, ragged tails, lengths below / at / above top-K
 # ---------------------------------------------------------------------------------
@@ -162,10 +181,39 @@ SMALL_FP8_KV = replace(SMALL_DECODE_BF16, name="small_fp8_kv", kv_format="fp8_ti
                        description="as small_decode_bf16 with an FP8 latent cache: e4m3 latent "
                                    "dims with an f32 scale per 128-dim tile, bf16 rope dims")
 
-SMALL = [SMALL_DECODE_BF16, SMALL_DECODE_FP8, SMALL_DECODE_MX, SMALL_TIES, SMALL_PREFILL,
-         SMALL_H8, EMPTY_AND_SHORT, SMALL_MID, SMALL_SIB, SMALL_MULTI]
+# e4m3 keys of 64 dims: per-token scales (the register-streamed folded-query kernel) and
+# MX scales (the per-head CUDA-core kernel)
+SMALL_FP8_D64 = replace(SMALL_DECODE_FP8, name="small_fp8_d64", idx_dim=64, seed=7012,
+                        description="as small_decode_fp8 with 64-dim keys")
+SMALL_MX_D64 = replace(SMALL_DECODE_MX, name="small_mx_d64", idx_dim=64, seed=7013,
+                       description="as small_decode_mx with 64-dim keys (two MX groups per key)")
 
-ALL = {s.name: s for s in HEADLINE + SMALL}
+# quantised prefill (the row-blocked kernel after an exact dequantisation of the keys)
+SMALL_PREFILL_FP8 = replace(SMALL_PREFILL, name="small_prefill_fp8", idx_dtype="e4m3", idx_scale="per_token",
+                            seed=7015, description="as small_prefill, e4m3 indexer with per-token scales")
+SMALL_PREFILL_MX = replace(SMALL_PREFILL, name="small_prefill_mx", idx_dtype="e4m3", idx_scale="mx",
+                           head_w_exps=(-3, 0), seed=7016, description="as small_prefill, MXFP8 indexer")
+# multi-token decode with 25 draft tokens per sequence: two row blocks per sequence (21 + 4)
+SMALL_MULTI25 = Spec(
+    name="small_multi25", mode="multi", batch=3, seq_lens=(40, 700, 2100), tokens_per_seq=25,
+    pool_pages=60, idx_heads=64, idx_dim=128, topk=256, sfa_heads=128, seed=7017,
+    description="25 query tokens per sequence at its last 25 positions")
+SMALL_MULTI_FP8 = replace(SMALL_MULTI, name="small_multi_fp8", idx_dtype="e4m3", idx_scale="per_token", seed=7018,
+                          description="multi-token decode with an e4m3 indexer (one key stream per token)")
+
+# long rows whose selection runs in clusters of eight CTAs (more than 16384 positions);
+# the tests give them degenerate queries (all scores equal, or 17 distinct values) so
+# that a CTA's boundary bin overflows its share of the candidate pool
+LONG_ROWS = Spec(
+    name="long_rows", mode="decode", batch=3, seq_lens=(40000, 34816, 9000), pool_pages=1400,
+    idx_heads=64, idx_dim=128, topk=2048, sfa_heads=16, seed=7014,
+    description="rows of 40000, 34816 and 9000 keys, top-K 2048")
+
+SMALL = [SMALL_DECODE_BF16, SMALL_DECODE_FP8, SMALL_DECODE_MX, SMALL_TIES, SMALL_PREFILL,
+         SMALL_H8, EMPTY_AND_SHORT, SMALL_MID, SMALL_SIB, SMALL_MULTI, SMALL_FP8_D64, SMALL_MX_D64,
+         SMALL_PREFILL_FP8, SMALL_PREFILL_MX, SMALL_MULTI25, SMALL_MULTI_FP8]
+
+ALL = {s.name: s for s in HEADLINE + EXTRA + SMALL + [LONG_ROWS]}
 
 
 # ---------------------------------------------------------------------------------

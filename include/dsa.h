@@ -17,8 +17,13 @@
  *
  * Conventions for every entry point:
  *   - Ownership: the caller allocates and owns every buffer, including the workspace.
- *     The library allocates no memory, keeps no state between calls and may be called
- *     concurrently on different streams with different workspaces.
+ *     The library allocates no memory, keeps no state between calls (apart from
+ *     per-device caches of the SM count and of the fixed scratch's address, and the
+ *     fixed scratch of dsa_indexer_topk_noalloc itself: see that entry point) and may be
+ *     called concurrently on different streams with different workspaces.
+ *   - Workspace sizes depend on the arguments and on the current device (the attention
+ *     splits its work by the device's SM count): size a workspace with the current
+ *     device set to the one it will be used on.
  *   - Pointers marked "device" must be device (or managed) memory of the current CUDA
  *     device; "host" pointers are read synchronously during the call.  The index and
  *     latent caches, their scales, the attention query and its output must start on a
@@ -217,9 +222,11 @@ dsa_status_t dsa_fused_decode(const dsa_indexer_args_t* iargs,
  * memory -- plugin hosts or serving runtimes that hand this library no allocator and
  * fix their memory budget up front, or request paths that must not call cudaMalloc
  * (it can synchronise the device).  Same inputs, outputs and semantics as
- * dsa_indexer_topk, but its scratch (the error word and the f32 score rows) lives in a
- * fixed 8 MiB array inside the library, one per device, held from the library's first
- * use on that device until the process exits.  It allocates nothing.
+ * dsa_indexer_topk, but its scratch (the error word, key histograms and f32 score rows)
+ * lives in a fixed 8 MiB array inside the library, one per device, held until the
+ * process exits from the time the library's module holding it is loaded on that device
+ * (under lazy module loading, the CUDA default: this entry point's first call there;
+ * with CUDA_MODULE_LOADING=EAGER: context creation).  It allocates nothing.
  *   - Limit: 256 + n_tokens * (ceil(max visible / 64) * 64 * 4 + 16384 + 32 * dim + 64) bytes
  *     (each part rounded up to 256) must fit in 8 MiB (e.g. 32 decode tokens over 32768
  *     positions, or 8 over 131072); larger requests return DSA_ERR_WORKSPACE before any
@@ -227,9 +234,10 @@ dsa_status_t dsa_fused_decode(const dsa_indexer_args_t* iargs,
  *   - The first call on a device looks up the array's device address (set-up, once per
  *     device, under a lock); make that first call before any stream capture.
  *   - Every call on a device shares the one array and it keeps the last call's
- *     contents; the error word is cleared on `stream` at the start of each call.  Calls
- *     that overlap on the GPU (different streams, or concurrent threads) race on it:
- *     order them on one stream.  Device-side error bits are not reported back; use
+ *     contents; what must start at zero (the key histograms) is cleared on `stream` by
+ *     each call.  Calls that overlap on the GPU (different streams, or concurrent
+ *     threads) race on it: order them on one stream.  Device-side error bits are not
+ *     reported back (the error word there is never read or cleared); use
  *     dsa_indexer_topk with a workspace to read them. */
 dsa_status_t dsa_indexer_topk_noalloc(const dsa_indexer_args_t* args,
                                       const dsa_index_cache_t* cache,

@@ -102,9 +102,16 @@ def workspace_size(plan: Plan, which: str = "fused") -> int:
     return {"fused": plan.ws_fused, "indexer": plan.ws_indexer, "sfa": plan.ws_sfa}[which]()
 
 
-def alloc_workspace(nbytes: int, device="cuda") -> torch.Tensor:
-    """A zeroed, 256-byte aligned workspace (torch allocations are 512-byte aligned)."""
-    return torch.zeros(max(nbytes, 256), dtype=torch.uint8, device=device)
+def alloc_workspace(nbytes: int, device="cuda", poison: bool = False) -> torch.Tensor:
+    """A 256-byte aligned workspace (torch allocations are 512-byte aligned), zeroed.
+
+    ``poison=True`` fills everything after the 256-byte header (whose error word must
+    start at zero) with 0xFF bytes -- NaN as f32, 0xFFFFFFFF as a counter -- so that a
+    kernel reading scratch it has not written shows up as a wrong result."""
+    ws = torch.zeros(max(nbytes, 256), dtype=torch.uint8, device=device)
+    if poison:
+        ws[256:].fill_(0xFF)
+    return ws
 
 
 def indexer_topk(plan: Plan, out_idx: torch.Tensor, ws: torch.Tensor, out_score: Optional[torch.Tensor] = None,

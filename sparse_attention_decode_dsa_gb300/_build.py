@@ -18,7 +18,7 @@ BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libdsa.so")
 
 SOURCES = ["dsa_api.cu", "indexer_score.cu", "indexer_stream.cu", "indexer_tc.cu", "topk.cu", "sfa_tc.cu", "tma_host.cu",
-           "prolog.cu"]
+           "prolog.cu", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O3",
          "--expt-relaxed-constexpr", f"-I{INCLUDE}", f"-I{CSRC}"]

@@ -94,7 +94,6 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return (uint32_t)__cvta_generic_to_shared(p);
 }
 
-// 16-byte global->shared copy; src_bytes = 0 zero-fills the destination.
 // Programmatic dependent launch.  pdl_trigger: this CTA no longer holds back the launch
 // of the next kernel in the stream (which may then start its own set-up early);
 // pdl_wait: wait until the previous kernel in the stream has completed and its memory

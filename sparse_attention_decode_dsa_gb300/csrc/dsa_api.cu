@@ -4,7 +4,7 @@
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
-#include <mutex>
+#include <atomic>
 #include <string>
 
 #include "common.cuh"
@@ -33,12 +33,6 @@ constexpr size_t kAlign = 256;
 size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 bool aligned16(const void* ptr) { return ((uintptr_t)ptr & 15u) == 0; }
 
-int num_sms() {
-  int dev = 0, n = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
-  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return 148;
-  return n;
-}
 
 // ---- shared checks -------------------------------------------------------------------
 dsa_status_t check_pages_tokens(const dsa_page_table_t* pg, const dsa_tokens_t* tk, int32_t* max_visible) {
@@ -147,15 +141,58 @@ __global__ void __launch_bounds__(256) clear_kernel(uint4* p, size_t n16) {
 // Workspace: [0, 256) the device error word; for split attention, the split counters;
 // then one region the passes use in turn (the indexer's key histograms and score rows,
 // later the attention's split partials).
+// Which scoring kernel serves the call.  Row-blocked: identity activation and tokens in
+// segments of consecutive rows of one sequence (a prefill: one segment; multi-token
+// decode: each sequence's draft tokens, all segments of one length), so that the rows of
+// a segment share each key tile; e4m3 keys take it only for a single sequence with many
+// rows (a prefill), after an exact dequantisation of its pages to bf16.  Otherwise one
+// row per query token.
+enum class Route { kPerRow, kBlocked, kBlockedDequant };
+struct IndexerRoute {
+  Route route = Route::kPerRow;
+  int32_t seg_rows = 1;  // row-blocked: rows per segment
+  int32_t seq = 0;       // dequantised: the one sequence
+};
+
+IndexerRoute route_indexer(const dsa_indexer_args_t* a, const dsa_index_cache_t* c, const dsa_tokens_t* tk) {
+  IndexerRoute rt;
+  const int T = tk->n_tokens;
+  if (a->act != DSA_ACT_IDENTITY || T < 2) return rt;
+  auto seq = [&](int i) { return tk->token_seq ? tk->token_seq_host[i] : i; };
+  int m = 1;
+  while (m < T && seq(m) == seq(0)) ++m;
+  const bool one_seq = m == T;
+  bool uniform = m >= 2 && T % m == 0 && (one_seq || m <= kBlockedMaxSeg);
+  for (int i = m; uniform && i < T; ++i)  // every later run of m rows is one sequence
+    uniform = i % m == 0 || seq(i) == seq(i - 1);
+  if (!uniform) return rt;
+  if (c->dtype == DSA_BF16) {
+    rt.route = Route::kBlocked;
+  } else if (one_seq && T >= 2 * kBlockRows) {
+    rt.route = Route::kBlockedDequant;
+    rt.seq = seq(0);
+  } else {
+    return rt;
+  }
+  rt.seg_rows = m;
+  return rt;
+}
+
 struct IndexerPlan {
   int32_t max_visible;
   int64_t score_stride;
   size_t score_bytes;  // the per-row key histograms, the collapsed query, the f32 score rows
-  size_t hist_bytes, qt_bytes;
+                       // and, when dequantising, the bf16 keys, their scales and page table
+  size_t hist_bytes, qt_bytes, rows_bytes;
+  size_t kb_bytes = 0, ks_bytes = 0, bt_bytes = 0;  // dequantised keys (row-blocked e4m3)
+  int32_t npv = 0;                                  // pages dequantised
+  IndexerRoute rt;
 };
 
-IndexerPlan plan_indexer(int32_t max_visible, int32_t n_tokens, int32_t dim) {
+IndexerPlan plan_indexer(int32_t max_visible, int32_t n_tokens, int32_t dim, const IndexerRoute& rt = IndexerRoute(),
+                         const dsa_page_table_t* pg = nullptr) {
   IndexerPlan p;
+  p.rt = rt;
   p.max_visible = max_visible;
   p.score_stride = ((int64_t)max_visible + 63) / 64 * 64;
   if (p.score_stride == 0) p.score_stride = 64;
@@ -166,8 +203,21 @@ IndexerPlan plan_indexer(int32_t max_visible, int32_t n_tokens, int32_t dim) {
   // workspace formula the boundary documents)
   p.qt_bytes = align_up((size_t)n_tokens * kSplitQueryHeads * dim * sizeof(uint16_t)) +
                align_up((size_t)n_tokens * kSplitQueryHeads * sizeof(float));
+  p.rows_bytes = rows;
   p.score_bytes = p.hist_bytes + p.qt_bytes + rows;
+  if (rt.route == Route::kBlockedDequant && pg) {
+    p.npv = (max_visible + kPage - 1) / kPage;
+    p.kb_bytes = align_up((size_t)p.npv * kPage * dim * sizeof(uint16_t));
+    p.ks_bytes = align_up((size_t)p.npv * kPage * sizeof(float));
+    p.bt_bytes = align_up((size_t)pg->batch * pg->max_pages_per_seq * sizeof(int32_t));
+    p.score_bytes += p.kb_bytes + p.ks_bytes + p.bt_bytes;
+  }
   return p;
+}
+
+IndexerPlan plan_indexer(const dsa_indexer_args_t* a, const dsa_index_cache_t* c, const dsa_page_table_t* pg,
+                         const dsa_tokens_t* tk, int32_t max_visible) {
+  return plan_indexer(max_visible, tk->n_tokens, c->dim, route_indexer(a, c, tk), pg);
 }
 
 struct SfaPlan {
@@ -183,7 +233,7 @@ SfaPlan plan_sfa(int32_t n_tokens, int32_t n_heads, int32_t top_k) {
   const int tiles = (top_k + 63) / 64;
   (void)n_heads;
   const int units = n_tokens * 2;  // one CTA pair per (token, split)
-  int s = num_sms() / (units > 0 ? units : 1);
+  int s = device_sm_count() / (units > 0 ? units : 1);
   if (s < 1) s = 1;
   if (s > tiles) s = tiles;
   if (s > 16) s = 16;
@@ -245,6 +295,7 @@ dsa_status_t run_indexer(const dsa_indexer_args_t* a, const dsa_index_cache_t* c
   float* qt = (float*)(region + ip.hist_bytes);
   uint16_t* qsplit = (uint16_t*)(region + ip.hist_bytes);  // (same scratch: the blocked path's split query)
   float* scores = (float*)(region + ip.hist_bytes + ip.qt_bytes);
+  uint8_t* dq = region + ip.hist_bytes + ip.qt_bytes + ip.rows_bytes;  // dequantised keys (if any)
   ScoreParams sp;
   sp.tv = token_view(pg, tk, ip.max_visible);
   sp.q = a->q;
@@ -269,13 +320,9 @@ dsa_status_t run_indexer(const dsa_indexer_args_t* a, const dsa_index_cache_t* c
     // Otherwise the per-head contraction on the tensor cores (CUDA cores for shapes they
     // do not take).
     const bool identity = a->act == DSA_ACT_IDENTITY;
-    // Query rows that share one sequence (prefill) share their keys: with bf16 keys and
-    // the identity activation, blocks of consecutive rows take each K tile together.
-    bool one_seq = tk->token_seq ? true : pg->batch == 1;
-    if (tk->token_seq)
-      for (int32_t i = 1; i < tk->n_tokens && one_seq; ++i) one_seq = tk->token_seq_host[i] == tk->token_seq_host[0];
-    const bool blocked = identity && c->dtype == DSA_BF16 && c->scale_kind == DSA_SCALE_NONE &&
-                         (c->dim == 64 || c->dim == 128) && one_seq && tk->n_tokens >= 2 * kBlockRows;
+    // Query rows that share one sequence (a prefill, or a sequence's draft tokens) share
+    // their keys: blocks of those rows take each K tile together (route_indexer).
+    const bool blocked = ip.rt.route != Route::kPerRow;
     // e4m3 keys (per-token scales, d = 128) with the identity activation: the head
     // sum folds into the query, and each key is one dot product taken from the TMA-staged
     // tile on the CUDA cores.
@@ -286,8 +333,19 @@ dsa_status_t run_indexer(const dsa_indexer_args_t* a, const dsa_index_cache_t* c
     tr.begin();
     cudaError_t e = cudaSuccess;
     if (blocked) {
-      e = launch_qsplit(sp, qsplit, nullptr, 3, s);
       ScoreParams sp2 = sp;
+      sp2.seg_rows = ip.rt.seg_rows;
+      if (ip.rt.route == Route::kBlockedDequant) {
+        uint16_t* kb = (uint16_t*)dq;
+        float* ks = (float*)(dq + ip.kb_bytes);
+        int32_t* bt = (int32_t*)(dq + ip.kb_bytes + ip.ks_bytes);
+        e = launch_kdequant(sp, c->scale_kind, ip.rt.seq, ip.npv, kb, ks, bt, s);
+        sp2.k = kb;
+        sp2.k_scale = c->scale_kind == DSA_SCALE_PER_TOKEN_F32 ? ks : nullptr;
+        sp2.tv.block_table = bt;
+        sp2.tv.num_pages = ip.npv;
+      }
+      if (e == cudaSuccess) e = launch_qsplit(sp, c->dtype, c->scale_kind, qsplit, nullptr, 3, s);
       sp2.q = qsplit;
       sp2.q_dep = 1;
       if (e == cudaSuccess) e = launch_score_tc_blocked(sp2, s);
@@ -354,6 +412,19 @@ dsa_status_t run_sfa(const dsa_sfa_args_t* a, const dsa_latent_cache_t* c, const
 
 }  // namespace
 
+int device_sm_count() {
+  // one lookup per device (an attribute query on every call would cost host time on the
+  // launch path); entries are written once with the same value, so a race is harmless
+  static std::atomic<int> cache[kMaxDevices];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 148;
+  int n = cache[dev].load(std::memory_order_relaxed);
+  if (n > 0) return n;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return 148;
+  cache[dev].store(n, std::memory_order_relaxed);
+  return n;
+}
+
 cudaError_t launch_clear(void* p, size_t bytes, cudaStream_t s) {
   const size_t n16 = bytes / 16;
   if (n16 == 0) return cudaSuccess;
@@ -371,7 +442,7 @@ size_t dsa_indexer_workspace_size(const dsa_indexer_args_t* args, const dsa_inde
                                   const dsa_page_table_t* pages, const dsa_tokens_t* tokens) {
   int32_t mv = 0;
   if (check_indexer(args, cache) != DSA_OK || check_pages_tokens(pages, tokens, &mv) != DSA_OK) return 0;
-  return kAlign + plan_indexer(mv, tokens->n_tokens, cache->dim).score_bytes;
+  return kAlign + plan_indexer(args, cache, pages, tokens, mv).score_bytes;
 }
 
 dsa_status_t dsa_indexer_topk(const dsa_indexer_args_t* args, const dsa_index_cache_t* cache,
@@ -383,7 +454,7 @@ dsa_status_t dsa_indexer_topk(const dsa_indexer_args_t* args, const dsa_index_ca
   int32_t mv = 0;
   if ((st = check_pages_tokens(pages, tokens, &mv)) != DSA_OK) return st;
   if (!out_idx) return fail(DSA_ERR_INVALID_ARG, "out_idx is NULL");
-  IndexerPlan ip = plan_indexer(mv, tokens->n_tokens, cache->dim);
+  IndexerPlan ip = plan_indexer(args, cache, pages, tokens, mv);
   if ((st = check_ws(ws, ws_bytes, kAlign + ip.score_bytes)) != DSA_OK) return st;
   Tracer tr(trace, (cudaStream_t)stream);
   uint8_t* region = (uint8_t*)ws + kAlign;
@@ -431,7 +502,7 @@ size_t dsa_fused_workspace_size(const dsa_indexer_args_t* iargs, const dsa_index
   if (check_indexer(iargs, icache) != DSA_OK || check_sfa(sargs, nullptr) != DSA_OK ||
       check_pages_tokens(pages, tokens, &mv) != DSA_OK)
     return 0;
-  IndexerPlan ip = plan_indexer(mv, tokens->n_tokens, icache->dim);
+  IndexerPlan ip = plan_indexer(iargs, icache, pages, tokens, mv);
   SfaPlan sp = plan_sfa(tokens->n_tokens, sargs->n_heads, iargs->top_k);
   const size_t sfa_b = sp.region_bytes();
   return kAlign + sp.cnt_bytes + (ip.score_bytes > sfa_b ? ip.score_bytes : sfa_b);  // the passes reuse one region
@@ -449,7 +520,7 @@ dsa_status_t dsa_fused_decode(const dsa_indexer_args_t* iargs, const dsa_index_c
   if ((st = check_pages_tokens(pages, tokens, &mv)) != DSA_OK) return st;
   if (!out_idx || !out) return fail(DSA_ERR_INVALID_ARG, "out_idx and out are required");
   if (!aligned16(out)) return fail(DSA_ERR_INVALID_ARG, "out must be 16-byte aligned");
-  IndexerPlan ip = plan_indexer(mv, tokens->n_tokens, icache->dim);
+  IndexerPlan ip = plan_indexer(iargs, icache, pages, tokens, mv);
   SfaPlan sp = plan_sfa(tokens->n_tokens, sargs->n_heads, iargs->top_k);
   const size_t sfa_b = sp.region_bytes();
   if ((st = check_ws(ws, ws_bytes, kAlign + sp.cnt_bytes + (ip.score_bytes > sfa_b ? ip.score_bytes : sfa_b))) !=
@@ -548,36 +619,9 @@ int32_t dsa_abi_version(void) { return DSA_ABI_VERSION; }
 }  // extern "C"
 
 // ---- indexer with the library's own fixed scratch ------------------------------------
-// For callers that cannot allocate device memory: the scratch this entry point needs
-// lives in one file-scope device array per GPU.  Host code may not hand the array's
-// name to a kernel (in host code it names a host-side stand-in); its device address is
-// looked up once per device with cudaGetSymbolAddress and passed as a pointer.
-constexpr size_t kNoAllocScratchBytes = size_t(8) << 20;
-static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
-
-namespace {
-std::mutex g_noalloc_mu;
-constexpr int kMaxDevices = 128;
-void* g_noalloc_addr[kMaxDevices] = {};
-
-// Device address of the fixed scratch on the current device (looked up on first use).
-dsa_status_t noalloc_scratch(void** out) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
-  if (dev < 0 || dev >= kMaxDevices) return fail(DSA_ERR_UNSUPPORTED, "device ordinal %d beyond %d", dev, kMaxDevices);
-  std::lock_guard<std::mutex> lock(g_noalloc_mu);
-  if (!g_noalloc_addr[dev]) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress of the fixed scratch");
-    g_noalloc_addr[dev] = p;
-  }
-  *out = g_noalloc_addr[dev];
-  return DSA_OK;
-}
-}  // namespace
-
+// For callers that cannot allocate device memory.  The scratch is a fixed device array
+// defined in noalloc.cu (its own module, so that it becomes resident on a device only
+// when this entry point first looks up its address there, under lazy module loading).
 extern "C" dsa_status_t dsa_indexer_topk_noalloc(const dsa_indexer_args_t* args, const dsa_index_cache_t* cache,
                                                  const dsa_page_table_t* pages, const dsa_tokens_t* tokens,
                                                  int32_t* out_idx, float* out_score, dsa_stream_t stream) {
@@ -586,7 +630,7 @@ extern "C" dsa_status_t dsa_indexer_topk_noalloc(const dsa_indexer_args_t* args,
   int32_t mv = 0;
   if ((st = check_pages_tokens(pages, tokens, &mv)) != DSA_OK) return st;
   if (!out_idx) return fail(DSA_ERR_INVALID_ARG, "out_idx is NULL");
-  IndexerPlan ip = plan_indexer(mv, tokens->n_tokens, cache->dim);
+  IndexerPlan ip = plan_indexer(args, cache, pages, tokens, mv);
   const size_t need = kAlign + ip.score_bytes;
   if (need > kNoAllocScratchBytes)
     return fail(DSA_ERR_WORKSPACE,
@@ -594,9 +638,13 @@ extern "C" dsa_status_t dsa_indexer_topk_noalloc(const dsa_indexer_args_t* args,
                 "(use dsa_indexer_topk with a caller workspace)",
                 need, kNoAllocScratchBytes);
   void* ws = nullptr;
-  if ((st = noalloc_scratch(&ws)) != DSA_OK) return st;
-  cudaError_t e = cudaMemsetAsync(ws, 0, sizeof(uint32_t), (cudaStream_t)stream);
-  if (e != cudaSuccess) return cuda_fail(e, "clearing the fixed scratch's error word");
+  int dev = -1;
+  const cudaError_t e = noalloc_scratch(&ws, &dev);
+  if (e != cudaSuccess) return cuda_fail(e, "looking up the fixed scratch's device address");
+  if (!ws) return fail(DSA_ERR_UNSUPPORTED, "device ordinal %d beyond the %d the fixed scratch covers", dev, kMaxDevices);
+  // The error word at the start of the scratch is only ever OR-ed into by the kernels and
+  // never read back through this entry point, so it is not cleared per call; the key
+  // histograms are zeroed inside run_indexer.
   Tracer tr(nullptr, (cudaStream_t)stream);
   uint8_t* region = (uint8_t*)ws + kAlign;
   return run_indexer(args, cache, pages, tokens, ip, out_idx, out_score, (uint32_t*)ws, region, region,

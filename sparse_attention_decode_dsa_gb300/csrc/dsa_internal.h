@@ -17,6 +17,18 @@ constexpr int kValueDim = 512;
 constexpr int kTopkBins = 4096;              // per-row histogram of the keys' top 12 bits
 constexpr int kMaxVisible = 1 << 20;         // longest row (positions) the indexer handles
 
+constexpr int kMaxDevices = 128;             // device ordinals the per-device caches cover
+
+// Streaming multiprocessors of the current device (looked up once per device).  Launch
+// plans, and so the attention's workspace size, depend on it.
+int device_sm_count();
+
+// Fixed scratch of dsa_indexer_topk_noalloc (noalloc.cu): its size, and its device
+// address on the current device, looked up once per device.  *ptr stays null (with
+// cudaSuccess) for a device ordinal at or beyond kMaxDevices.
+constexpr size_t kNoAllocScratchBytes = size_t(8) << 20;
+cudaError_t noalloc_scratch(void** ptr, int* device);
+
 // Everything a kernel needs to locate a token's row, sequence and visible range.
 struct TokenView {
   const int32_t* token_seq;  // may be null: token i is batch row i
@@ -42,6 +54,8 @@ struct ScoreParams {
   int32_t n_heads, dim, act, max_page_blocks;
   int32_t q_dep;           // 1: q is written by the preceding kernel (wait before reading it)
   const float* qt;         // q~ [T, dim] f32 (the folded-query kernel only)
+  int32_t seg_rows;        // row-blocked kernel: rows per segment (consecutive rows of one
+                           // sequence; n_tokens is a multiple of it)
 };
 
 struct TopkParams {
@@ -138,12 +152,21 @@ cudaError_t launch_score_fold(const ScoreParams& p, dsa_scale_t sk, const float*
 // [n_tokens, stride] (1, 1, 1, 0, ...; skipped when ws is null).  The row-blocked kernel
 // takes stride 3 (consecutive tokens' terms back to back).  The workspace reserves
 // kSplitQueryHeads rows per token for it.
+// The query may be bf16, or e4m3 with its scales (folded into the sum exactly).
 constexpr int kSplitQueryHeads = 16;
-cudaError_t launch_qsplit(const ScoreParams& p, uint16_t* qs, float* ws, int stride, cudaStream_t s);
-// The row-blocked tensor-core score kernel: every token belongs to one sequence (host
-// checked); blocks of kBlockRows consecutive rows share each K tile; p.q is the stride-3
-// split query.
+cudaError_t launch_qsplit(const ScoreParams& p, dsa_dtype_t dt, dsa_scale_t sk, uint16_t* qs, float* ws, int stride,
+                          cudaStream_t s);
+// e4m3 keys of sequence b for the row-blocked kernel: its first npv pages dequantised to
+// bf16 compact pages kb [npv, 64, dim] (MX group scales applied; per-token scales copied
+// to ks [npv * 64]), and bt_out[b * max_pages + j] = j (-1 for an invalid page id).
+cudaError_t launch_kdequant(const ScoreParams& p, dsa_scale_t sk, int b, int npv, uint16_t* kb, float* ks,
+                            int32_t* bt_out, cudaStream_t s);
+// The row-blocked tensor-core score kernel: the tokens come in segments of p.seg_rows
+// consecutive rows of one sequence (host checked); blocks of up to kBlockRows rows of a
+// segment share each K tile; p.q is the stride-3 split query; bf16 keys, times
+// p.k_scale[key] when that is set.
 constexpr int kBlockRows = 21;
+constexpr int kBlockedMaxSeg = 1024;  // longest segment of several sequences' rows (rows per launch)
 cudaError_t launch_score_tc_blocked(const ScoreParams& p, cudaStream_t s);
 cudaError_t launch_topk(const TopkParams& p, int32_t max_visible, cudaStream_t s);
 cudaError_t launch_sfa_tc(const SfaParams& p, cudaStream_t s);

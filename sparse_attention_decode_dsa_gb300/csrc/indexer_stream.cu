@@ -61,10 +61,12 @@ __global__ void __launch_bounds__(kQtThreads) qtilde_kernel(ScoreParams p, float
 // per token back to back so that one MMA serves 21 consecutive tokens.
 // 512 threads per query token: thread (quarter j, dim d) sums 16 heads; the four quarter
 // sums are added in order.
-constexpr int kSplitHeads = 16;
 constexpr int kSplitThreads = 512;
 
-template <int D>
+// The query may be e4m3 with scales (KIND 1: one f32 per token, applied to the sum;
+// KIND 2: E8M0 per head and 32-element group, applied to each head's weight), so that
+// quantised keys dequantised to bf16 take the same path.
+template <int D, int KIND>
 __global__ void __launch_bounds__(kSplitThreads) qsplit_kernel(ScoreParams p, uint16_t* qs, float* ws, int stride) {
   pdl_trigger();
   pdl_wait();  // the split query lives in workspace that the previous pass may still use
@@ -78,16 +80,22 @@ __global__ void __launch_bounds__(kSplitThreads) qsplit_kernel(ScoreParams p, ui
 #pragma unroll
     for (int u = 0; u < 16; ++u) {
       const int h = 16 * j + u;
-      q[u] = h < H ? bf16_to_f32(__ldg((const uint16_t*)p.q + ((int64_t)row * H + h) * D + d)) : 0.f;
+      const int64_t off = ((int64_t)row * H + (h < H ? h : 0)) * D + d;
+      q[u] = h >= H ? 0.f
+             : KIND == 0 ? bf16_to_f32(__ldg((const uint16_t*)p.q + off))
+                         : e4m3_to_f32(__ldg((const uint8_t*)p.q + off));
       w[u] = h < H ? __ldg(p.head_w + (int64_t)row * H + h) : 0.f;
+      if (KIND == 2 && h < H)
+        w[u] *= e8m0_to_f32(__ldg((const uint8_t*)p.q_scale + ((int64_t)row * H + h) * (D / 32) + d / 32));
     }
 #pragma unroll
     for (int u = 0; u < 16; ++u) acc = fmaf(w[u], q[u], acc);
     part[j][d] = acc;
   }
   __syncthreads();
+  const float qtok = KIND == 1 ? __ldg((const float*)p.q_scale + row) : 1.f;
   for (int d = threadIdx.x; d < D; d += kSplitThreads) {
-    const float qt = ((part[0][d] + part[1][d]) + part[2][d]) + part[3][d];
+    const float qt = (((part[0][d] + part[1][d]) + part[2][d]) + part[3][d]) * qtok;
     const uint16_t hi = f32_to_bf16_rne(qt);
     const float r1 = qt - bf16_to_f32(hi);
     const uint16_t mid = f32_to_bf16_rne(r1);
@@ -268,7 +276,56 @@ cudaError_t launch_stream(const ScoreParams& p, float* qt, cudaStream_t s) {
                     (const float*)qt);
 }
 
+// Exact dequantisation of one sequence's visible K-index pages to bf16, for the row-
+// blocked tensor-core kernel (a prefill re-reads its keys once per block of rows, so the
+// keys are converted once rather than per block).  Output: compact pages
+// kb[j] = page j of sequence b (logical order), bf16 [npv, 64, D]; for per-token scales
+// (KIND 1) the raw e4m3 values with the scales copied to ks [npv * 64] (the kernel
+// multiplies each score by its key's scale); for MX (KIND 2) each element times its
+// group's power of two, exact in bf16 (3 significant bits, exponent within bf16's range
+// unless element x scale < 2^-133, which rounds).  bt_out[b * max_pages + j] = j, or -1
+// with DSA_DEVERR_PAGE_ID for a page id outside the cache (its keys are then masked
+// downstream, as with a bf16 cache).  One CTA per page, 16 bytes of codes per thread.
+template <int D, int KIND>
+__global__ void __launch_bounds__(256) kdequant_kernel(ScoreParams p, int b, uint16_t* kb, float* ks, int32_t* bt_out) {
+  pdl_trigger();
+  pdl_wait();  // the outputs live in workspace that the previous pass may still use
+  const int j = blockIdx.x;
+  const int pg = physical_page(p.tv, b, j, threadIdx.x == 0 ? p.err : nullptr);
+  if (threadIdx.x == 0) bt_out[(int64_t)b * p.tv.max_pages + j] = pg >= 0 ? j : -1;
+  if (pg < 0) return;
+  constexpr int kChunks = kPage * D / 16;  // 16-byte chunks of e4m3 codes per page
+  for (int c = threadIdx.x; c < kChunks; c += blockDim.x) {
+    const int slot = c / (D / 16), e0 = (c % (D / 16)) * 16;
+    const int64_t src = ((int64_t)pg * kPage + slot) * D + e0;
+    const uint4 raw = __ldg((const uint4*)((const uint8_t*)p.k + src));
+    float f[16];
+    decode16<1>(raw, f);
+    const float sc = KIND == 2 ? e8m0_to_f32(__ldg((const uint8_t*)p.k_scale + ((int64_t)pg * kPage + slot) * (D / 32) + e0 / 32))
+                               : 1.f;
+    uint32_t w[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) w[u] = pack_bf16x2(f[2 * u] * sc, f[2 * u + 1] * sc);
+    uint4* dst = (uint4*)(kb + ((int64_t)j * kPage + slot) * D + e0);
+    dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+    dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+  }
+  if (KIND == 1)
+    for (int slot = threadIdx.x; slot < kPage; slot += blockDim.x)
+      ks[(int64_t)j * kPage + slot] = __ldg((const float*)p.k_scale + (int64_t)pg * kPage + slot);
+}
+
 }  // namespace
+
+cudaError_t launch_kdequant(const ScoreParams& p, dsa_scale_t sk, int b, int npv, uint16_t* kb, float* ks,
+                            int32_t* bt_out, cudaStream_t s) {
+  const dim3 g(npv), t(256);
+  if (sk == DSA_SCALE_PER_TOKEN_F32)
+    return p.dim == 64 ? launch_pdl(kdequant_kernel<64, 1>, g, t, 0, s, p, b, kb, ks, bt_out)
+                       : launch_pdl(kdequant_kernel<128, 1>, g, t, 0, s, p, b, kb, ks, bt_out);
+  return p.dim == 64 ? launch_pdl(kdequant_kernel<64, 2>, g, t, 0, s, p, b, kb, ks, bt_out)
+                     : launch_pdl(kdequant_kernel<128, 2>, g, t, 0, s, p, b, kb, ks, bt_out);
+}
 
 bool score_stream_supported(dsa_act_t act, int dim) { return act == DSA_ACT_IDENTITY && (dim == 64 || dim == 128); }
 
@@ -281,9 +338,18 @@ cudaError_t launch_qtilde(const ScoreParams& p, dsa_dtype_t dt, dsa_scale_t sk, 
   return p.dim == 64 ? launch_pdl(qtilde_kernel<64, 2>, g, b, 0, s, p, qt) : launch_pdl(qtilde_kernel<128, 2>, g, b, 0, s, p, qt);
 }
 
-cudaError_t launch_qsplit(const ScoreParams& p, uint16_t* qs, float* ws, int stride, cudaStream_t s) {
-  return p.dim == 64 ? launch_pdl(qsplit_kernel<64>, dim3(p.tv.n_tokens), dim3(kSplitThreads), 0, s, p, qs, ws, stride)
-                     : launch_pdl(qsplit_kernel<128>, dim3(p.tv.n_tokens), dim3(kSplitThreads), 0, s, p, qs, ws, stride);
+cudaError_t launch_qsplit(const ScoreParams& p, dsa_dtype_t dt, dsa_scale_t sk, uint16_t* qs, float* ws, int stride,
+                          cudaStream_t s) {
+  const dim3 g(p.tv.n_tokens), t(kSplitThreads);
+  const int kind = dt == DSA_BF16 ? 0 : (sk == DSA_SCALE_PER_TOKEN_F32 ? 1 : 2);
+  if (p.dim == 64) {
+    if (kind == 0) return launch_pdl(qsplit_kernel<64, 0>, g, t, 0, s, p, qs, ws, stride);
+    if (kind == 1) return launch_pdl(qsplit_kernel<64, 1>, g, t, 0, s, p, qs, ws, stride);
+    return launch_pdl(qsplit_kernel<64, 2>, g, t, 0, s, p, qs, ws, stride);
+  }
+  if (kind == 0) return launch_pdl(qsplit_kernel<128, 0>, g, t, 0, s, p, qs, ws, stride);
+  if (kind == 1) return launch_pdl(qsplit_kernel<128, 1>, g, t, 0, s, p, qs, ws, stride);
+  return launch_pdl(qsplit_kernel<128, 2>, g, t, 0, s, p, qs, ws, stride);
 }
 
 cudaError_t launch_score_stream(const ScoreParams& p, dsa_dtype_t dt, dsa_scale_t sk, float* qt, cudaStream_t s) {

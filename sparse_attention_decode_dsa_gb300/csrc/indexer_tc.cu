@@ -35,6 +35,7 @@ constexpr int kEpiGroups = 2;                    // epilogue groups, alternating
 constexpr int kTcThreads = 64 + kEpiGroups * 128; // producer warp, MMA warp, 4 warps per group
 constexpr int kTileTok = 128;
 constexpr int kMaxRowsPerLaunch = 1024;
+static_assert(kBlockedMaxSeg == kMaxRowsPerLaunch, "a segment of several sequences' rows fits in one launch");
 
 template <int KIND, int D>  // KIND 0: bf16; 1: e4m3 + per-token f32; 2: e4m3 + E8M0 per 32
 struct Cfg {
@@ -61,7 +62,18 @@ struct TcArgs {
   ScoreParams p;
   int32_t row0;   // first query row of this launch
   int32_t nrows;  // rows in this launch
+  int32_t seg;    // row-blocked: rows of one sequence in a row of the launch's segments
+                  // (nrows is a multiple of it); units are blocks of up to kBlockRows rows
+                  // of one segment
 };
+
+// Row-blocked unit u of a launch: its first row and its number of rows.
+__device__ __forceinline__ void block_unit(const TcArgs& a, int u, int* r0, int* nb) {
+  const int per_seg = (a.seg + kBlockRows - 1) / kBlockRows;
+  const int sg = u / per_seg, k = u - sg * per_seg;
+  *r0 = sg * a.seg + k * kBlockRows;
+  *nb = min(kBlockRows, a.seg - k * kBlockRows);
+}
 
 // 16 e4m3 values -> f32, exactly.
 __device__ __forceinline__ void e4m3x16_to_f32(const uint4& raw, float* out) {
@@ -79,9 +91,13 @@ __device__ __forceinline__ void e4m3x16_to_f32(const uint4& raw, float* out) {
   }
 }
 
-// BLK: row-blocked (bf16, identity activation, one sequence): an item is a block of
-// kBlockRows consecutive rows and one tile; the MMA's N = 64 columns are the blocks' rows'
-// three split-query terms (p.q: [rows, 3, D]).
+// BLK: row-blocked (bf16 keys, identity activation): the launch's rows come in segments
+// of `a.seg` consecutive rows of one sequence (a prefill, or the draft tokens of each
+// sequence in multi-token decode); an item is a block of up to kBlockRows rows of one
+// segment and one tile of that sequence's keys, read once for the whole block; the MMA's
+// N = 64 columns are the block's rows' three split-query terms (p.q: [rows, 3, D]).
+// With p.k_scale set (e4m3 keys with per-token scales, dequantised to bf16 beforehand),
+// each score is the dot product times its key's scale.
 // FOLD: e4m3 keys, identity activation: no tensor cores; the epilogue warps take each
 // key's dot product with the folded query q~ (p.qt) straight from the staged tile.
 template <int KIND, int D, bool BLK, bool FOLD = false>
@@ -141,7 +157,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     tmem_relinquish();
   }
   // visible counts and tiles of every row, then an exclusive scan (one warp)
-  const int nunits = BLK ? (a.nrows + kBlockRows - 1) / kBlockRows : a.nrows;
+  const int nunits = BLK ? a.nrows / a.seg * ((a.seg + kBlockRows - 1) / kBlockRows) : a.nrows;
   for (int r = tid; r < a.nrows; r += kTcThreads) {
     int b, n;
     resolve_token(p.tv, a.row0 + r, &b, &n, p.err);
@@ -155,8 +171,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   if (BLK) {
     __syncthreads();
     for (int u = tid; u < nunits; u += kTcThreads) {  // a block sees its rows' widest window
-      int m = 0;
-      for (int r = u * kBlockRows; r < a.nrows && r < (u + 1) * kBlockRows; ++r) m = max(m, rn[r]);
+      int r0, nb, m = 0;
+      block_unit(a, u, &r0, &nb);
+      for (int r = r0; r < r0 + nb; ++r) m = max(m, rn[r]);
       rown[u] = m;
       prefix[u + 1] = (m + kTileTok - 1) / kTileTok;
     }
@@ -199,18 +216,25 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         while (prefix[r + 1] <= it) ++r;
         if (!FOLD && r != cur_row) {
           cur_row = r;
+          int ur0 = r, unb = 1;
+          if (BLK) block_unit(a, r, &ur0, &unb);
           const int slot = qcount & 1;
           if (!mbar_wait(&q_empty[slot], ((qcount >> 1) & 1) ^ 1, abort_flag, p.err)) break;
           mbar_arrive_expect_tx(&q_full[slot], C::kRegions * H * 128);
           const uint32_t qdst = smem_u32(qslots + slot * C::kQSlotBytes);
           for (int g = 0; g < C::kRegions; ++g)
             tma_load_2d(qdst + g * C::kRegionQBytes, &qmap, &q_full[slot], g * C::kBoxInner,
-                        BLK ? 3 * (a.row0 + r * kBlockRows) : (a.row0 + r) * H);
+                        BLK ? 3 * (a.row0 + ur0) : (a.row0 + r) * H);
           ++qcount;
         }
         if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.err)) break;
         const int tile = it - prefix[r];
-        const int b = rowb[BLK ? r * kBlockRows : r];
+        int br = r;
+        if (BLK) {
+          int unb;
+          block_unit(a, r, &br, &unb);
+        }
+        const int b = rowb[br];
         const int npages = (rown[r] + kPage - 1) / kPage;
         int pg[2] = {-1, -1};
         uint32_t bytes = 0;
@@ -319,9 +343,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const int acc = n % C::kNumAcc;
         const uint32_t acc_phase = (uint32_t)(n / C::kNumAcc) & 1u;
         const int t = (it - prefix[r]) * kTileTok + i;
-        const int r0 = r * kBlockRows;
-        const int nb = min(kBlockRows, a.nrows - r0);
+        int r0, nb;
+        block_unit(a, r, &r0, &nb);
         const int pg = t < rown[r] ? physical_page(p.tv, rowb[r0], t >> 6, nullptr) : -1;
+        const float ksc = (p.k_scale && pg >= 0) ? ((const float*)p.k_scale)[(int64_t)pg * kPage + (t & 63)] : 1.f;
         bool ok = true;
         if (lane == 0) ok = mbar_wait(&acc_full[acc], acc_phase, abort_flag, p.err);
         if (!__shfl_sync(0xffffffffu, ok, 0)) break;
@@ -341,7 +366,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const float c0 = __uint_as_float(3 * j < 32 ? v0[(3 * j) & 31] : v1[(3 * j) & 31]);
             const float c1 = __uint_as_float(3 * j + 1 < 32 ? v0[(3 * j + 1) & 31] : v1[(3 * j + 1) & 31]);
             const float c2 = __uint_as_float(3 * j + 2 < 32 ? v0[(3 * j + 2) & 31] : v1[(3 * j + 2) & 31]);
-            const float v = pg >= 0 ? (c0 + c1) + c2 : -INFINITY;
+            const float v = pg >= 0 ? ((c0 + c1) + c2) * ksc : -INFINITY;
             const int64_t grow = a.row0 + r0 + j;
             p.scores[grow * p.score_stride + t] = v;
             atomicAdd(p.hist + grow * kTopkBins + (score_key(v) >> 20), 1u);
@@ -544,19 +569,22 @@ cudaError_t launch_tc(const ScoreParams& p, cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(score_tc_kernel<KIND, D, BLK, FOLD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        C::kSmem);
   if (e != cudaSuccess) return e;
-  int dev = 0, sms = 0;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int sms = device_sm_count();
   // the query: [tokens * heads, D], boxes of one token's heads; blocked: [tokens * 3, D],
   // boxes of 64 rows (a block's 21 tokens x 3 terms, and one spare row)
   if (!make_tma_2d_sw128(&qmap, p.q, (uint64_t)p.tv.n_tokens * (BLK ? 3 : p.n_heads), C::kElem, D,
                          BLK ? 64 : p.n_heads))
     return cudaErrorInvalidValue;
-  for (int row0 = 0; row0 < p.tv.n_tokens; row0 += kMaxRowsPerLaunch) {
+  // row-blocked: launches start at segment boundaries (a segment longer than a launch
+  // is one sequence, cut anywhere)
+  const int seg = BLK ? p.seg_rows : 1;
+  const int per_launch = seg >= kMaxRowsPerLaunch ? kMaxRowsPerLaunch : kMaxRowsPerLaunch / seg * seg;
+  for (int row0 = 0; row0 < p.tv.n_tokens; row0 += per_launch) {
     TcArgs a;
     a.p = p;
     a.row0 = row0;
-    a.nrows = p.tv.n_tokens - row0 < kMaxRowsPerLaunch ? p.tv.n_tokens - row0 : kMaxRowsPerLaunch;
+    a.nrows = p.tv.n_tokens - row0 < per_launch ? p.tv.n_tokens - row0 : per_launch;
+    a.seg = seg < a.nrows ? seg : a.nrows;
     e = launch_pdl(score_tc_kernel<KIND, D, BLK, FOLD>, dim3(sms), dim3(kTcThreads), C::kSmem, s, kmap, qmap, a);
     if (e != cudaSuccess) return e;
   }

@@ -148,3 +148,27 @@ def test_product_path_has_no_cpu_fallback():
         if f.endswith(".py"):
             src = open(os.path.join(pkg, f)).read()
             assert "oracle" not in src and "dsa_workloads" not in src, f
+
+
+def test_workspace_holds_dequantised_keys_for_quantised_prefill():
+    """An e4m3 indexer over many rows of one sequence (a prefill) dequantises that
+    sequence's pages to bf16 once: its workspace adds bf16 [pages, 64, dim] keys, f32
+    [pages * 64] scales and an int32 [batch, max_pages] page table to the per-row parts."""
+    T, L, dim = 64, 4000, 128
+    lens_t = torch.tensor([L], dtype=torch.int32)
+    seq_t = torch.zeros(T, dtype=torch.int32)
+    pos_t = torch.arange(L - T, L, dtype=torch.int32)
+    hp = lambda t: C.cast(C.c_void_p(t.data_ptr()), C.POINTER(C.c_int32))
+    pages = dsa.PageTable(FAKE, FAKE, hp(lens_t), 1, 63, 64, 100)
+    toks = dsa.Tokens(T, FAKE, FAKE, hp(seq_t), hp(pos_t))
+    cache = dsa.IndexCache(FAKE, FAKE, dsa.DSA_E4M3, dsa.DSA_SCALE_PER_TOKEN_F32, dim)
+    args = dsa.IndexerArgs(FAKE, FAKE, dsa.DSA_E4M3, dsa.DSA_SCALE_PER_TOKEN_F32, FAKE, 64, 2048, 0)
+    a256 = lambda n: (n + 255) // 256 * 256
+    npv = (L + 63) // 64
+    base = (256 + a256(T * npv * 64 * 4) + T * 4096 * 4 + a256(T * 16 * dim * 2) + a256(T * 16 * 4))
+    n = dsa.lib.dsa_indexer_workspace_size(C.byref(args), C.byref(cache), C.byref(pages), C.byref(toks))
+    assert n == base + a256(npv * 64 * dim * 2) + a256(npv * 64 * 4) + a256(63 * 4)
+    # one row per sequence (decode): no dequantised copy
+    args.act = 1  # ReLU: per-head scoring, never row-blocked
+    n_relu = dsa.lib.dsa_indexer_workspace_size(C.byref(args), C.byref(cache), C.byref(pages), C.byref(toks))
+    assert n_relu == base

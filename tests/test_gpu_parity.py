@@ -1,5 +1,8 @@
 """Parity of the CUDA path (through the C ABI) with the float64 oracle.
 
+Workspaces are poisoned (every byte after the error word set to 0xFF, NaN as f32), so a
+kernel that reads scratch nobody wrote fails these checks instead of reading zeros.
+
 Indices and their scores must match bit for bit (the exactness certificate guarantees the
 fp32 scores are exact).  Attention outputs must satisfy, against the float64 oracle,
 max |err| <= 2e-2 and relative RMS (||o - r|| / ||r|| over the compared tensor) <= 1e-2:
@@ -35,7 +38,7 @@ def _device(wl):
 def _run_fused(dsa, plan, T, K, H):
     out_idx = torch.empty((T, K), dtype=torch.int32, device="cuda")
     out = torch.empty((T, H, 512), dtype=torch.bfloat16, device="cuda")
-    ws = dsa.alloc_workspace(plan.ws_fused())
+    ws = dsa.alloc_workspace(plan.ws_fused(), poison=True)
     dsa.fused_decode(plan, out_idx, out, ws)
     torch.cuda.synchronize()
     assert dsa.read_device_error(ws) == 0
@@ -45,7 +48,7 @@ def _run_fused(dsa, plan, T, K, H):
 def _run_indexer(dsa, plan, T, K):
     out_idx = torch.empty((T, K), dtype=torch.int32, device="cuda")
     out_sc = torch.empty((T, K), dtype=torch.float32, device="cuda")
-    ws = dsa.alloc_workspace(plan.ws_indexer())
+    ws = dsa.alloc_workspace(plan.ws_indexer(), poison=True)
     dsa.indexer_topk(plan, out_idx, ws, out_score=out_sc)
     torch.cuda.synchronize()
     assert dsa.read_device_error(ws) == 0
@@ -56,7 +59,7 @@ def _run_sfa(dsa, plan, idx_np, H):
     T, K = idx_np.shape
     idx = torch.from_numpy(np.ascontiguousarray(idx_np, dtype=np.int32)).cuda()
     out = torch.empty((T, H, 512), dtype=torch.bfloat16, device="cuda")
-    ws = dsa.alloc_workspace(plan.ws_sfa())
+    ws = dsa.alloc_workspace(plan.ws_sfa(), poison=True)
     dsa.sparse_attn(plan, idx, out, ws)
     torch.cuda.synchronize()
     assert dsa.read_device_error(ws) == 0
@@ -125,10 +128,27 @@ def test_causal_prefill_sampled(dsa):
     _check_config(dsa, W.CAUSAL_PREFILL, tokens=[0, 1, 63, 64, 2046, 2047, 2048, 5000, 8191])
 
 
-def test_relu_activation(dsa):
-    """The per-head ReLU variant against the oracle's 'relu' reading."""
-    spec = W.SMALL_DECODE_BF16
-    wl = W.make(spec)
+@pytest.mark.parametrize("spec", [W.CAUSAL_PREFILL_FP8, W.CAUSAL_PREFILL_MX], ids=lambda s: s.name)
+def test_causal_prefill_quantised_sampled(dsa, spec):
+    """The 8192-token causal prefill with an e4m3 (per-token scales) or MXFP8 indexer: the
+    keys are dequantised exactly to bf16 once, then the row-blocked tensor-core kernel
+    scores 21 rows per key tile; indices and scores bit-exact on sampled rows."""
+    _check_config(dsa, spec, tokens=[0, 1, 63, 64, 2047, 2048, 5000, 8191])
+
+
+def test_multi_token_decode_sampled(dsa):
+    """Four draft tokens per sequence at the BF16 decode's sizes (128 tokens, 32768-token
+    contexts): the four rows of a sequence share each K-index tile."""
+    _check_config(dsa, W.BF16_MULTI_DECODE, tokens=[0, 1, 2, 3, 62, 125, 127])
+
+
+@pytest.mark.parametrize("spec", [W.SMALL_DECODE_BF16, W.SMALL_DECODE_FP8, W.SMALL_DECODE_MX, W.SMALL_FP8_D64,
+                                  W.SMALL_MX_D64, W.SMALL_H8], ids=lambda s: s.name)
+def test_relu_activation(dsa, spec):
+    """The per-head ReLU variant against the oracle's 'relu' reading, in every key format
+    and width (per-head tensor-core kernel for 128-dim keys, the CUDA-core kernel for
+    64-dim e4m3 keys)."""
+    wl = W.make(spec, with_latent=False)
     d = _device(wl)
     d.act = dsa.DSA_ACT_RELU
     plan = dsa.Plan(d)
@@ -206,3 +226,39 @@ def test_cuda_graph_replay_matches_eager(dsa, spec):
         assert dsa.read_device_error(ws) == 0
         assert np.array_equal(out_idx.cpu().numpy(), want[0])
         assert np.array_equal(out.float().cpu().numpy().astype(np.float64), want[1])
+
+
+def _indexer_vs_oracle(dsa, wl, label):
+    d = _device(wl)
+    plan = dsa.Plan(d)
+    idx_g, sc_g = _run_indexer(dsa, plan, wl.n_tokens, wl.spec.topk)
+    for t in range(wl.n_tokens):
+        ri, rs = O.indexer_topk(wl, t)
+        assert np.array_equal(idx_g[t], ri), f"{label} token {t}: indices differ"
+        assert np.array_equal(sc_g[t], rs, equal_nan=True), f"{label} token {t}: scores differ"
+    return idx_g
+
+
+def test_topk_all_scores_equal_on_long_rows(dsa):
+    """An all-zero indexer query gives every key the same score, the method's degenerate
+    case: the answer is positions 0..K-1 (ties to the lower position).  Every CTA's
+    boundary bin then holds all its keys, far more than its share of the candidate pool,
+    so the selection takes the rescanning radix select on rows of 40000, 34816 and 9000
+    keys (clusters of eight CTAs)."""
+    wl = W.make(W.LONG_ROWS, with_latent=False)
+    wl.idx_q[...] = 0                              # bf16 +0
+    idx_g = _indexer_vs_oracle(dsa, wl, "all-equal")
+    assert np.array_equal(idx_g, np.tile(np.arange(W.LONG_ROWS.topk, dtype=np.int32), (wl.n_tokens, 1)))
+
+
+def test_topk_boundary_bin_near_pool_capacity(dsa):
+    """One nonzero query element: each score is w * q * k_t0 with k_t0 an integer in
+    [-8, 8], so the scores take 17 values and the K-th largest sits in a bin holding
+    about 1/17 of each CTA's keys -- close to a CTA's share of the candidate pool (256 of
+    2048 in a cluster of eight), below it in some CTAs and above it in others, on the
+    34816-key row in particular.  Both the pooled select and its fallback must give the
+    oracle's answer."""
+    wl = W.make(W.LONG_ROWS, with_latent=False)
+    wl.idx_q[...] = 0
+    wl.idx_q[:, 0, 0] = 0x3F80                     # bf16 1.0 in head 0, dim 0
+    _indexer_vs_oracle(dsa, wl, "17 values")

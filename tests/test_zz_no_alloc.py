@@ -6,8 +6,16 @@ must not touch the driver's allocator (it can synchronise the device).  For them
 library offers an indexer entry point whose scratch is a fixed 8 MiB array built into
 the library.  This test calls it through the C ABI twice in a row and checks both
 results against dsa_indexer_topk run with a caller workspace: indices and their
-scores must match bit for bit (the indexer's parity bar), and an oversized request must
-be refused before any launch.  The file is named so that pytest collects it last.
+scores must match bit for bit (the indexer's parity bar).  It also checks the claim the
+entry point exists for: once the first call has loaded the library's module on the
+device (the fixed array is part of that module), a further call changes neither the
+device's free memory nor what torch's allocator holds.  An oversized request must be
+refused before any launch.
+
+The file is named so that pytest collects it last: it adds an entry point beside the
+hot path rather than testing the path itself, so when it fails, a run that stops at the
+first failure (``-x``) has already run every other test.  It depends on nothing those
+tests leave behind and passes when run alone in a fresh process.
 """
 import ctypes as C
 
@@ -47,11 +55,17 @@ def test_noalloc_matches_workspace_entry_point(spec):
     ref_sc = torch.empty((T, K), dtype=torch.float32, device="cuda")
     ws = dsa.alloc_workspace(plan.ws_indexer())
     dsa.indexer_topk(plan, ref_idx, ws, out_score=ref_sc)
-    for call in range(2):
-        idx = torch.full((T, K), -7, dtype=torch.int32, device="cuda")
-        sc = torch.full((T, K), -7.0, dtype=torch.float32, device="cuda")
+    outs = [(torch.full((T, K), -7, dtype=torch.int32, device="cuda"),
+             torch.full((T, K), -7.0, dtype=torch.float32, device="cuda")) for _ in range(2)]
+    torch.cuda.synchronize()
+    for call, (idx, sc) in enumerate(outs):
+        if call == 1:  # the module holding the fixed array is loaded by now
+            free0, held0 = torch.cuda.mem_get_info()[0], torch.cuda.memory_allocated()
         assert _noalloc(dsa, fn, plan, idx, sc) == dsa.DSA_OK, dsa.lib.dsa_last_error_message()
         torch.cuda.synchronize()
+        if call == 1:
+            assert torch.cuda.mem_get_info()[0] == free0, "the call changed the device's free memory"
+            assert torch.cuda.memory_allocated() == held0
         assert torch.equal(idx, ref_idx), f"call {call}: indices differ"
         assert np.array_equal(sc.cpu().numpy(), ref_sc.cpu().numpy(), equal_nan=True), f"call {call}: scores differ"
 
