@@ -76,11 +76,24 @@ def algorithmic(wl):
     idx_bytes = T * s.topk * 4
     score_flops = 2.0 * s.idx_heads * s.idx_dim * float(vis.sum())
     gather_rows = int(sel.sum())
-    sfa_bytes = gather_rows * 1152 + T * s.sfa_heads * 576 * 2 + T * s.sfa_heads * 512 * 2 + idx_bytes
+    kv_row = 1152 if s.kv_format == "bf16" else 512 + 4 * 4 + 64 * 2   # FP8: codes, 4 tile scales, bf16 rope
+    sfa_bytes = gather_rows * kv_row + T * s.sfa_heads * 576 * 2 + T * s.sfa_heads * 512 * 2 + idx_bytes
     sfa_flops = 2.0 * s.sfa_heads * (576 + 512) * float(sel.sum())
     meta = wl.block_table.nbytes + wl.seq_lens.nbytes
+    # The row-blocked scorer (a prefill; a sequence's draft tokens) folds the head sum into
+    # the query: per block of up to 21 rows and 128-key tile it runs one M = 128, N = 64
+    # (21 rows x 3 split terms), K = d MMA.  Its executed tensor work, not the per-head
+    # definition's, is what its tensor fraction is measured on.
+    blk_flops = 0.0
+    if s.mode in ("prefill", "multi") and s.idx_heads and T >= 2:
+        seg = T if s.mode == "prefill" else s.tokens_per_seq
+        for s0 in range(0, T, seg):
+            for r0 in range(s0, s0 + seg, 21):
+                mv = int(vis[r0:min(r0 + 21, s0 + seg)].max(initial=0))
+                blk_flops += 2.0 * 128 * 64 * s.idx_dim * ((mv + 127) // 128)
     return {
-        "indexer_score": {"bytes": key_tokens * k_row + q_bytes + meta, "flops": score_flops},
+        "indexer_score": {"bytes": key_tokens * k_row + q_bytes + meta, "flops": score_flops,
+                          "executed_flops": blk_flops},
         "indexer_topk": {"bytes": idx_bytes, "flops": 0.0},
         "sfa": {"bytes": sfa_bytes, "flops": sfa_flops},
         "hist_clear": {"bytes": T * 4096 * 4, "flops": 0.0},
@@ -289,6 +302,10 @@ def main():
               "top_k": spec.topk, "index_heads": spec.idx_heads, "index_dim": spec.idx_dim,
               "index_dtype": spec.idx_dtype + ("" if spec.idx_scale == "none" else "+" + spec.idx_scale),
               "sfa_heads": spec.sfa_heads, "kv_dim": 576, "page_size": 64, "seed": spec.seed}
+    if spec.kv_format != "bf16":
+        config["kv_format"] = spec.kv_format
+    if spec.mode == "multi":
+        config["tokens_per_seq"] = spec.tokens_per_seq
 
     if args.impl == "reference":
         return run_reference(args, spec, config, world, rank)
@@ -316,7 +333,8 @@ def main():
     work = algorithmic(wl)
     l2_bytes = torch.cuda.get_device_properties(dev).L2_cache_size
     input_bytes = sum(int(t.numel() * t.element_size()) for t in
-                      [d.idx_k, d.kv, d.idx_q, d.sfa_q, d.head_w, d.block_table] if t is not None)
+                      [d.idx_k, d.kv, d.kv_codes, d.kv_scale, d.kv_rope, d.idx_q, d.sfa_q, d.head_w, d.block_table]
+                      if t is not None)
 
     def step(trace=None):
         dsa.fused_decode(plan, out_idx, out, ws, stream=stream, trace=trace)
@@ -404,6 +422,24 @@ def main():
                     "frac": ach / bf16_tf_sust, "traffic": traffic, "algorithmic_flops": dom_work["flops"],
                     "peak_source": f"{peak_src} (MEASURED_PEAKS.json bf16_tflops_sustained)" if peak_src == "measured"
                     else "fallback 1.7 PFLOP/s sustained"}
+
+    # every kernel against its own bound: HBM bytes for all; tensor flops for the attention
+    # and the row-blocked scorer
+    kroof = {}
+    for k, st in kstats.items():
+        wk = work.get(k)
+        if not wk or st["avg_us"] <= 0:
+            continue
+        a_s = st["avg_us"] * 1e-6
+        r = {"algorithmic_bytes": wk["bytes"], "achieved_gbs": wk["bytes"] / a_s / 1e9,
+             "frac_hbm": wk["bytes"] / a_s / 1e9 / hbm_gbs}
+        fl = wk.get("executed_flops") or (wk["flops"] if k == "sfa" else 0.0)
+        if fl:
+            r["tensor_tflops"] = fl / a_s / 1e12
+            r["frac_tensor"] = fl / a_s / 1e12 / bf16_tf
+            if k == "indexer_score":
+                r["flops_note"] = "executed by the row-blocked (head-folded) scorer, not the per-head definition's"
+        kroof[k] = r
 
     ms_per_step = total_ms / args.steps
     value = whole_job_rate(world, T * args.steps, total_ms)
@@ -510,6 +546,7 @@ def main():
                        "parallelism": "replicas" if world > 1 else "single GPU"},
             "roofline": roofline,
             "kernels": kstats,
+            "kernel_rooflines": kroof,
             "kernel_timing": "per-launch CUDA events on the launch stream, in a traced pass of the same "
                              f"{args.steps} steps right after the timed region (events between launches "
                              "serialise them; that pass took " + f"{1e3 * traced_ms / args.steps:.1f} us/step)",

@@ -128,7 +128,13 @@ BF16_MULTI_DECODE = replace(
     BF16_DECODE, name="bf16_multi_decode", mode="multi", tokens_per_seq=4, seed=1008, int_seed=1002,
     description="as bf16_decode with 4 query tokens per sequence at its last 4 positions (128 tokens)")
 
-EXTRA = [CAUSAL_PREFILL_FP8, CAUSAL_PREFILL_MX, BF16_MULTI_DECODE]
+# The BF16 decode with an FP8 latent cache (e4m3 latent dims, an f32 scale per 128-dim
+# tile, bf16 rope dims): the attention gathers 656 instead of 1152 bytes per row
+FP8KV_DECODE = replace(
+    BF16_DECODE, name="bf16_decode_fp8kv", kv_format="fp8_tile128", seed=1009, int_seed=1002,
+    description="as bf16_decode with an FP8 latent cache (tiles of 128, f32 scales, bf16 rope)")
+
+EXTRA = [CAUSAL_PREFILL_FP8, CAUSAL_PREFILL_MX, BF16_MULTI_DECODE, FP8KV_DECODE]
 
 # ---------------------------------------------------------------------------------
 # Small parity cases: several tiles, ragged tails, lengths below / at / above top-K
@@ -176,7 +182,7 @@ SMALL_MULTI = Spec(
     description="multi-token decode: 4 query tokens per sequence at its last 4 positions "
                 "(a speculative draft), each seeing the prefix up to itself")
 
-# the attention kernels read a bf16 latent cache; this one exists for the oracle only
+# FP8 latent cache (the attention dequantises gathered rows in shared memory)
 SMALL_FP8_KV = replace(SMALL_DECODE_BF16, name="small_fp8_kv", kv_format="fp8_tile128", seed=7011,
                        description="as small_decode_bf16 with an FP8 latent cache: e4m3 latent "
                                    "dims with an f32 scale per 128-dim tile, bf16 rope dims")
@@ -211,7 +217,7 @@ LONG_ROWS = Spec(
 
 SMALL = [SMALL_DECODE_BF16, SMALL_DECODE_FP8, SMALL_DECODE_MX, SMALL_TIES, SMALL_PREFILL,
          SMALL_H8, EMPTY_AND_SHORT, SMALL_MID, SMALL_SIB, SMALL_MULTI, SMALL_FP8_D64, SMALL_MX_D64,
-         SMALL_PREFILL_FP8, SMALL_PREFILL_MX, SMALL_MULTI25, SMALL_MULTI_FP8]
+         SMALL_PREFILL_FP8, SMALL_PREFILL_MX, SMALL_MULTI25, SMALL_MULTI_FP8, SMALL_FP8_KV]
 
 ALL = {s.name: s for s in HEADLINE + EXTRA + SMALL + [LONG_ROWS]}
 

@@ -19,10 +19,8 @@ def _dev(a, device, dtype=None):
 
 def to_device(wl, device="cuda", with_latent=True):
     from sparse_attention_decode_dsa_gb300 import DeviceInputs
-    if with_latent and wl.kv is None and wl.kv_codes is not None:
-        raise NotImplementedError("the attention kernels read a bf16 latent cache; "
-                                  "the FP8 latent layout exists in the oracle only")
     decode = wl.spec.mode == "decode"
+    fp8kv = with_latent and wl.kv_codes is not None
     bf = torch.bfloat16
     kbits = torch.bfloat16 if wl.idx_k.dtype == np.uint16 else torch.uint8
     qs = wl.idx_q_scale
@@ -41,6 +39,9 @@ def to_device(wl, device="cuda", with_latent=True):
         idx_q_scale=_dev(qs, device),
         idx_k_scale=_dev(ks, device),
         kv=_dev(wl.kv.view(np.int16), device, bf) if (with_latent and wl.kv is not None) else None,
+        kv_codes=_dev(wl.kv_codes, device) if fp8kv else None,
+        kv_scale=_dev(wl.kv_scale, device) if fp8kv else None,
+        kv_rope=_dev(wl.kv_rope.view(np.int16), device, bf) if fp8kv else None,
         sfa_q=_dev(wl.sfa_q.view(np.int16), device, bf) if (with_latent and wl.sfa_q is not None) else None,
         softmax_scale=float(wl.spec.softmax_scale),
         token_seq=None if decode else _dev(wl.q_seq, device),

@@ -54,7 +54,7 @@
 extern "C" {
 #endif
 
-#define DSA_ABI_VERSION 2
+#define DSA_ABI_VERSION 3
 
 /* A cudaStream_t, kept opaque so that this header needs no CUDA header. */
 typedef struct CUstream_st* dsa_stream_t;
@@ -134,11 +134,22 @@ typedef struct {
   dsa_act_t act;
 } dsa_indexer_args_t;
 
-/* MLA latent cache: row = [latent (v_dim) | rope (dim - v_dim)], bf16. */
+/* MLA latent cache: row = [latent (v_dim) | rope (dim - v_dim)].
+ * bf16 (dtype DSA_BF16): data = bf16 [num_pages, 64, dim]; scale and rope NULL.
+ * FP8 (dtype DSA_E4M3): the latent dims quantised per token in tiles of 128 ("Day0
+ * Inference Optimization on Ascend CANN", section 3, "FP8 Block Quantization for SFA KV
+ * Cache": tile 128, half the bytes read): data = e4m3 codes [num_pages, 64, v_dim],
+ * scale = f32 [num_pages, 64, v_dim / 128] (latent element j of a row is
+ * code * scale[j / 128]), rope = the rope dims in bf16 [num_pages, 64, dim - v_dim]
+ * (the pages leave their storage open).  ABI version 3 added dtype, scale and rope;
+ * zero them for a bf16 cache. */
 typedef struct {
-  const void* data;        /* device [num_pages, 64, dim] bf16                        */
+  const void* data;        /* device, see above                                       */
   int32_t dim;             /* 576                                                      */
   int32_t v_dim;           /* 512: the value is the leading v_dim entries of the row  */
+  dsa_dtype_t dtype;       /* DSA_BF16 or DSA_E4M3                                    */
+  const void* scale;       /* device f32 [num_pages, 64, v_dim / 128] (FP8), or NULL  */
+  const void* rope;        /* device bf16 [num_pages, 64, dim - v_dim] (FP8), or NULL */
 } dsa_latent_cache_t;
 
 /* Sparse-attention query side. */
@@ -279,6 +290,38 @@ dsa_status_t dsa_index_cache_append_mxfp8(const void* k_new, int32_t dim,
                                           const dsa_tokens_t* tokens,
                                           void* cache_codes, void* cache_scales,
                                           void* ws, size_t ws_bytes, dsa_stream_t stream);
+
+/* ---- Cache append: the new token's rows written into the paged caches ------------ */
+/* A decode step stores each new token's K-index row and latent row before the indexer
+ * and the attention read them (both operators read the paged caches directly: "Day0
+ * Inference Optimization on Ascend CANN", section 2).  Token i's rows go to page
+ * block_table[b * max_pages_per_seq + pos / 64], slot pos % 64, with b = token_seq[i] (or
+ * i) and pos = token_pos[i] (or seq_lens[b] - 1: the newest stored position).  A position
+ * outside the page table sets DSA_DEVERR_TOKEN, a page id outside [0, num_pages)
+ * DSA_DEVERR_PAGE_ID, in ws's error word; that token is skipped and the others are
+ * written.  ws: 256-byte aligned, at least 256 bytes (only the error word is used; it
+ * is not cleared by the call).  The cache structs' buffers are written, not only read.
+ *
+ * FP8 formats use absmax block quantisation (the pages leave the rule open): a block's
+ * f32 scale is amax / 448 (amax: its largest magnitude; 448: the largest E4M3 value),
+ * computed as an IEEE binary32 division, or 1 for an all-zero block; each element is
+ * stored as the E4M3 value nearest to the binary32 quotient x / scale, ties to even,
+ * saturating at +-448.  Inputs must be finite. */
+
+/* K-index rows: device k_new bf16 [T, cache->dim] (16-byte aligned) into `cache`: bf16
+ * (copied), e4m3 with DSA_SCALE_PER_TOKEN_F32 (one block per row: codes to data, the
+ * scale to scale[page, slot]) or e4m3 with DSA_SCALE_MX_E8M0_G32 (as
+ * dsa_index_cache_append_mxfp8). */
+dsa_status_t dsa_index_cache_append(const void* k_new, const dsa_index_cache_t* cache,
+                                    const dsa_page_table_t* pages, const dsa_tokens_t* tokens,
+                                    void* ws, size_t ws_bytes, dsa_stream_t stream);
+
+/* Latent rows: device rows_new bf16 [T, cache->dim] (16-byte aligned) into `cache`: bf16
+ * (copied) or FP8 (each 128-dim latent tile a block: codes to data, scales to scale; the
+ * rope dims copied to rope). */
+dsa_status_t dsa_latent_cache_append(const void* rows_new, const dsa_latent_cache_t* cache,
+                                     const dsa_page_table_t* pages, const dsa_tokens_t* tokens,
+                                     void* ws, size_t ws_bytes, dsa_stream_t stream);
 
 /* ---- Errors and introspection --------------------------------------------------- */
 /* Copies the device error word out of ws (synchronises `stream`) into *err. */

@@ -48,7 +48,8 @@ class IndexerArgs(C.Structure):
 
 
 class LatentCache(C.Structure):
-    _fields_ = [("data", _vp), ("dim", C.c_int32), ("v_dim", C.c_int32)]
+    _fields_ = [("data", _vp), ("dim", C.c_int32), ("v_dim", C.c_int32), ("dtype", C.c_int),
+                ("scale", _vp), ("rope", _vp)]
 
 
 class SfaArgs(C.Structure):
@@ -87,6 +88,10 @@ def _load() -> C.CDLL:
     lib.dsa_index_cache_append_mxfp8.argtypes = [_vp, C.c_int32, P(PageTable), P(Tokens), _vp, _vp, _vp,
                                                  C.c_size_t, _vp]
     lib.dsa_index_cache_append_mxfp8.restype = C.c_int
+    lib.dsa_index_cache_append.argtypes = [_vp, P(IndexCache), P(PageTable), P(Tokens), _vp, C.c_size_t, _vp]
+    lib.dsa_index_cache_append.restype = C.c_int
+    lib.dsa_latent_cache_append.argtypes = [_vp, P(LatentCache), P(PageTable), P(Tokens), _vp, C.c_size_t, _vp]
+    lib.dsa_latent_cache_append.restype = C.c_int
     lib.dsa_read_device_error.argtypes = [_vp, P(C.c_uint32), _vp]
     lib.dsa_read_device_error.restype = C.c_int
     lib.dsa_clear_device_error.argtypes = [_vp, _vp]
@@ -117,8 +122,9 @@ def _check(status: int, where: str):
 
 from ._api import (  # noqa: E402  (needs `lib` above)
     DeviceInputs, Plan, indexer_topk, sparse_attn, fused_decode, read_device_error,
-    clear_device_error, workspace_size, alloc_workspace, quantize_mxfp8, index_cache_append_mxfp8)
+    clear_device_error, workspace_size, alloc_workspace, quantize_mxfp8, index_cache_append_mxfp8,
+    index_cache_append, latent_cache_append)
 
 __all__ = ["lib", "DsaError", "DeviceInputs", "Plan", "indexer_topk", "sparse_attn", "fused_decode",
            "read_device_error", "clear_device_error", "workspace_size", "alloc_workspace", "Trace",
-           "quantize_mxfp8", "index_cache_append_mxfp8"]
+           "quantize_mxfp8", "index_cache_append_mxfp8", "index_cache_append", "latent_cache_append"]

@@ -48,6 +48,9 @@ class DeviceInputs:
     idx_q_scale: Optional[torch.Tensor] = None
     idx_k_scale: Optional[torch.Tensor] = None
     kv: Optional[torch.Tensor] = None    # bf16 [num_pages, 64, 576]
+    kv_codes: Optional[torch.Tensor] = None  # FP8 latent cache: e4m3 codes [num_pages, 64, 512]
+    kv_scale: Optional[torch.Tensor] = None  #   f32 [num_pages, 64, 4], one per 128-dim tile
+    kv_rope: Optional[torch.Tensor] = None   #   bf16 [num_pages, 64, 64]
     sfa_q: Optional[torch.Tensor] = None  # bf16 [T, H, 576]
     softmax_scale: float = 576 ** -0.5
     token_seq: Optional[torch.Tensor] = None
@@ -81,7 +84,10 @@ class Plan:
         self.icache = IndexCache(_ptr(d.idx_k), _ptr(d.idx_k_scale), dt, sk, int(d.idx_k.shape[-1]))
         self.iargs = IndexerArgs(_ptr(d.idx_q), _ptr(d.idx_q_scale), dt, sk, _ptr(d.head_w),
                                  int(d.idx_q.shape[1]), int(d.top_k), int(d.act))
-        self.lcache = LatentCache(_ptr(d.kv), 576, 512) if d.kv is not None else None
+        if d.kv_codes is not None:
+            self.lcache = LatentCache(_ptr(d.kv_codes), 576, 512, DSA_E4M3, _ptr(d.kv_scale), _ptr(d.kv_rope))
+        else:
+            self.lcache = LatentCache(_ptr(d.kv), 576, 512, DSA_BF16, None, None) if d.kv is not None else None
         self.sargs = (SfaArgs(_ptr(d.sfa_q), int(d.sfa_q.shape[1]), float(d.softmax_scale))
                       if d.sfa_q is not None else None)
 
@@ -184,3 +190,49 @@ def index_cache_append_mxfp8(k_new: torch.Tensor, cache_codes: torch.Tensor, cac
                                             _ptr(cache_codes), _ptr(cache_scales), _ptr(ws),
                                             ws.numel() * ws.element_size(), _stream_ptr(stream)),
            "dsa_index_cache_append_mxfp8")
+
+
+def _pages_tokens(block_table, seq_lens, seq_lens_host, num_pages, n_tokens, token_seq, token_pos, token_seq_host,
+                  token_pos_host):
+    B, maxp = block_table.shape
+    pages = PageTable(_ptr(block_table), _ptr(seq_lens), _i32_host_ptr(seq_lens_host), B, maxp, 64, int(num_pages))
+    tokens = Tokens(int(n_tokens), _ptr(token_seq), _ptr(token_pos), _i32_host_ptr(token_seq_host),
+                    _i32_host_ptr(token_pos_host))
+    return pages, tokens
+
+
+def index_cache_append(k_new: torch.Tensor, cache: torch.Tensor, cache_scale: Optional[torch.Tensor],
+                       block_table: torch.Tensor, seq_lens: torch.Tensor, seq_lens_host: torch.Tensor,
+                       ws: torch.Tensor, token_seq=None, token_pos=None, token_seq_host=None, token_pos_host=None,
+                       stream=None):
+    """Writes the new key of every token (bf16 k_new [T, dim]) to its (page, slot) of the
+    paged K-index cache: bf16 cache [pages, 64, dim] (copied), or e4m3 (uint8) with
+    per-token f32 scales [pages, 64] or MX E8M0 scales [pages, 64, dim / 32]."""
+    assert k_new.is_cuda and k_new.element_size() == 2 and k_new.is_contiguous()
+    if cache.element_size() == 2:
+        dt, sk = DSA_BF16, DSA_SCALE_NONE
+    else:
+        dt = DSA_E4M3
+        sk = DSA_SCALE_PER_TOKEN_F32 if cache_scale.dtype == torch.float32 else DSA_SCALE_MX_E8M0_G32
+    icache = IndexCache(_ptr(cache), _ptr(cache_scale), dt, sk, int(cache.shape[-1]))
+    pages, tokens = _pages_tokens(block_table, seq_lens, seq_lens_host, cache.shape[0], k_new.shape[0], token_seq,
+                                  token_pos, token_seq_host, token_pos_host)
+    _check(lib.dsa_index_cache_append(_ptr(k_new), C.byref(icache), C.byref(pages), C.byref(tokens), _ptr(ws),
+                                      ws.numel() * ws.element_size(), _stream_ptr(stream)), "dsa_index_cache_append")
+
+
+def latent_cache_append(rows_new: torch.Tensor, cache: torch.Tensor, block_table: torch.Tensor,
+                        seq_lens: torch.Tensor, seq_lens_host: torch.Tensor, ws: torch.Tensor,
+                        cache_scale: Optional[torch.Tensor] = None, cache_rope: Optional[torch.Tensor] = None,
+                        token_seq=None, token_pos=None, token_seq_host=None, token_pos_host=None, stream=None):
+    """Writes the new latent row of every token (bf16 rows_new [T, 576]) to its (page,
+    slot) of the paged latent cache: bf16 cache [pages, 64, 576] (copied), or FP8 (codes
+    uint8 [pages, 64, 512], f32 scales [pages, 64, 4] per 128-dim tile, bf16 rope
+    [pages, 64, 64])."""
+    assert rows_new.is_cuda and rows_new.element_size() == 2 and rows_new.is_contiguous()
+    fp8 = cache.element_size() == 1
+    lcache = LatentCache(_ptr(cache), 576, 512, DSA_E4M3 if fp8 else DSA_BF16, _ptr(cache_scale), _ptr(cache_rope))
+    pages, tokens = _pages_tokens(block_table, seq_lens, seq_lens_host, cache.shape[0], rows_new.shape[0], token_seq,
+                                  token_pos, token_seq_host, token_pos_host)
+    _check(lib.dsa_latent_cache_append(_ptr(rows_new), C.byref(lcache), C.byref(pages), C.byref(tokens), _ptr(ws),
+                                       ws.numel() * ws.element_size(), _stream_ptr(stream)), "dsa_latent_cache_append")

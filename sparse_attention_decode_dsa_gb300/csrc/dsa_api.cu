@@ -122,6 +122,13 @@ dsa_status_t check_sfa(const dsa_sfa_args_t* a, const dsa_latent_cache_t* c) {
     if (!aligned16(c->data)) return fail(DSA_ERR_INVALID_ARG, "latent cache data must be 16-byte aligned");
     if (c->dim != kLatentDim || c->v_dim != kValueDim)
       return fail(DSA_ERR_UNSUPPORTED, "latent rows must be 576 wide with a 512-wide value (got %d/%d)", c->dim, c->v_dim);
+    if (c->dtype == DSA_E4M3) {
+      if (!c->scale || !c->rope) return fail(DSA_ERR_INVALID_ARG, "an FP8 latent cache needs scale and rope");
+      if (!aligned16(c->scale) || !aligned16(c->rope))
+        return fail(DSA_ERR_INVALID_ARG, "latent scales and rope must be 16-byte aligned");
+    } else if (c->dtype != DSA_BF16) {
+      return fail(DSA_ERR_INVALID_ARG, "unknown latent dtype");
+    }
   }
   return DSA_OK;
 }
@@ -385,7 +392,11 @@ dsa_status_t run_sfa(const dsa_sfa_args_t* a, const dsa_latent_cache_t* c, const
   SfaParams p;
   p.tv = token_view(pg, tk, max_visible);
   p.q = (const uint16_t*)a->q;
-  p.kv = (const uint16_t*)c->data;
+  const bool fp8 = c->dtype == DSA_E4M3;
+  p.kv = fp8 ? nullptr : (const uint16_t*)c->data;
+  p.kv_codes = fp8 ? (const uint8_t*)c->data : nullptr;
+  p.kv_scale = fp8 ? (const float*)c->scale : nullptr;
+  p.kv_rope = fp8 ? (const uint16_t*)c->rope : nullptr;
   p.idx = idx;
   p.out = (uint16_t*)out;
   const bool global_merge = sp_.n_splits > 1 && !sp_.sib_merge;
@@ -583,6 +594,66 @@ dsa_status_t dsa_index_cache_append_mxfp8(const void* k_new, int32_t dim, const 
   p.err = (uint32_t*)ws;
   cudaError_t e = launch_mxfp8_quant(p, (cudaStream_t)stream);
   if (e != cudaSuccess) return cuda_fail(e, "K-index append launch");
+  return DSA_OK;
+}
+
+dsa_status_t dsa_index_cache_append(const void* k_new, const dsa_index_cache_t* cache, const dsa_page_table_t* pages,
+                                    const dsa_tokens_t* tokens, void* ws, size_t ws_bytes, dsa_stream_t stream) {
+  if (!cache) return fail(DSA_ERR_INVALID_ARG, "cache is NULL");
+  if (cache->dtype == DSA_E4M3 && cache->scale_kind == DSA_SCALE_MX_E8M0_G32)
+    return dsa_index_cache_append_mxfp8(k_new, cache->dim, pages, tokens, const_cast<void*>(cache->data),
+                                        const_cast<void*>(cache->scale), ws, ws_bytes, stream);
+  if (!k_new || !cache->data) return fail(DSA_ERR_INVALID_ARG, "k_new and cache data are required");
+  if (cache->dim != 64 && cache->dim != 128) return fail(DSA_ERR_UNSUPPORTED, "dim must be 64 or 128 (got %d)", cache->dim);
+  const bool fp8 = cache->dtype == DSA_E4M3;
+  if (fp8 ? (cache->scale_kind != DSA_SCALE_PER_TOKEN_F32 || !cache->scale)
+          : (cache->dtype != DSA_BF16 || cache->scale_kind != DSA_SCALE_NONE))
+    return fail(DSA_ERR_UNSUPPORTED, "index cache format: bf16, or e4m3 with per-token f32 or MX scales");
+  if (!aligned16(k_new) || !aligned16(cache->data) || (cache->scale && !aligned16(cache->scale)))
+    return fail(DSA_ERR_INVALID_ARG, "k_new and the cache buffers must be 16-byte aligned");
+  int32_t mv = 0;
+  dsa_status_t st = check_pages_tokens(pages, tokens, &mv);
+  if (st != DSA_OK) return st;
+  if ((st = check_ws(ws, ws_bytes, kAlign)) != DSA_OK) return st;
+  IndexAppendParams p{};
+  p.x = (const uint16_t*)k_new;
+  p.n_rows = tokens->n_tokens;
+  p.data = const_cast<void*>(cache->data);
+  p.scales = (float*)const_cast<void*>(cache->scale);
+  p.tv = token_view(pages, tokens, mv);
+  p.err = (uint32_t*)ws;
+  cudaError_t e = launch_index_append(p, cache->dim, fp8, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "K-index append launch");
+  return DSA_OK;
+}
+
+dsa_status_t dsa_latent_cache_append(const void* rows_new, const dsa_latent_cache_t* cache,
+                                     const dsa_page_table_t* pages, const dsa_tokens_t* tokens, void* ws,
+                                     size_t ws_bytes, dsa_stream_t stream) {
+  if (!rows_new || !cache || !cache->data) return fail(DSA_ERR_INVALID_ARG, "rows_new and cache data are required");
+  if (cache->dim != kLatentDim || cache->v_dim != kValueDim)
+    return fail(DSA_ERR_UNSUPPORTED, "latent rows must be 576 wide with a 512-wide value (got %d/%d)", cache->dim,
+                cache->v_dim);
+  const bool fp8 = cache->dtype == DSA_E4M3;
+  if (!fp8 && cache->dtype != DSA_BF16) return fail(DSA_ERR_INVALID_ARG, "unknown latent dtype");
+  if (fp8 && (!cache->scale || !cache->rope)) return fail(DSA_ERR_INVALID_ARG, "an FP8 latent cache needs scale and rope");
+  if (!aligned16(rows_new) || !aligned16(cache->data) || (fp8 && (!aligned16(cache->scale) || !aligned16(cache->rope))))
+    return fail(DSA_ERR_INVALID_ARG, "rows_new and the cache buffers must be 16-byte aligned");
+  int32_t mv = 0;
+  dsa_status_t st = check_pages_tokens(pages, tokens, &mv);
+  if (st != DSA_OK) return st;
+  if ((st = check_ws(ws, ws_bytes, kAlign)) != DSA_OK) return st;
+  LatentAppendParams p{};
+  p.x = (const uint16_t*)rows_new;
+  p.n_rows = tokens->n_tokens;
+  p.data = fp8 ? nullptr : (uint16_t*)const_cast<void*>(cache->data);
+  p.codes = fp8 ? (uint8_t*)const_cast<void*>(cache->data) : nullptr;
+  p.scales = fp8 ? (float*)const_cast<void*>(cache->scale) : nullptr;
+  p.rope = fp8 ? (uint16_t*)const_cast<void*>(cache->rope) : nullptr;
+  p.tv = token_view(pages, tokens, mv);
+  p.err = (uint32_t*)ws;
+  cudaError_t e = launch_latent_append(p, fp8, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "latent append launch");
   return DSA_OK;
 }
 

@@ -72,7 +72,10 @@ struct TopkParams {
 struct SfaParams {
   TokenView tv;
   const uint16_t* q;       // bf16 [T, H, 576]
-  const uint16_t* kv;      // bf16 [num_pages, 64, 576]
+  const uint16_t* kv;      // bf16 [num_pages, 64, 576] (bf16 cache)
+  const uint8_t* kv_codes; // FP8 cache: e4m3 [num_pages, 64, 512]; null for a bf16 cache
+  const float* kv_scale;   //   f32 [num_pages, 64, 4]: one scale per 128-dim tile
+  const uint16_t* kv_rope; //   bf16 [num_pages, 64, 64]
   const int32_t* idx;      // [T, K]
   uint16_t* out;           // bf16 [T, H, 512]
   float* part_o;           // [T, S, 2 halves, 256 dims, H]: each split's O / l (null when S == 1)
@@ -185,5 +188,32 @@ struct Mxfp8Params {
   uint32_t* err;       // (append only) device error word
 };
 cudaError_t launch_mxfp8_quant(const Mxfp8Params& p, cudaStream_t s);
+
+// Append of each new token's latent row ([T, 576] bf16) to its (page, slot) of the
+// latent cache: bf16 rows (data), or FP8 (codes [.., 512] e4m3, scales [.., 4] f32 per
+// 128-dim tile, rope [.., 64] bf16).
+struct LatentAppendParams {
+  const uint16_t* x;   // [n_rows, 576] bf16, 16-byte aligned
+  int64_t n_rows;
+  uint16_t* data;      // bf16 cache
+  uint8_t* codes;      // FP8 cache
+  float* scales;
+  uint16_t* rope;
+  TokenView tv;
+  uint32_t* err;
+};
+cudaError_t launch_latent_append(const LatentAppendParams& p, bool fp8, cudaStream_t s);
+
+// Append of each new token's key ([T, dim] bf16) to a bf16 K-index cache or an e4m3 one
+// with one f32 scale per token.
+struct IndexAppendParams {
+  const uint16_t* x;   // [n_rows, dim] bf16
+  int64_t n_rows;
+  void* data;          // [pages, 64, dim] bf16 or e4m3
+  float* scales;       // [pages, 64] (e4m3)
+  TokenView tv;
+  uint32_t* err;
+};
+cudaError_t launch_index_append(const IndexAppendParams& p, int dim, bool fp8, cudaStream_t s);
 
 }  // namespace dsa

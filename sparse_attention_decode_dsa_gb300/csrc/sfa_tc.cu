@@ -74,6 +74,13 @@ constexpr int kQropeBytes = 128 * 64;             // Q rope (own 32 dims) [128 r
 constexpr int kMaxXBytes = 2 * 2 * 128 * 4;       // finisher pairs' row maxima [tile parity][half][row]
 constexpr int kSmem = 1024 + kStages * kStageBytes + kQropeBytes + 3 * kXchBytes + kMaxXBytes + kMaxSplitLen * 4 + 512;
 static_assert(kSmem <= 232448, "shared memory budget");
+// FP8 latent cache: per tile and group of 4 slots, two 128-byte pieces of e4m3 codes
+// (this CTA's 256 latent dims) and the 64-byte rope piece; plus one 16-byte copy of each
+// row's four tile scales into a per-stage scale area [64 rows][4] f32.
+constexpr int kGathersFp8 = (kTok / 4) * 3;
+constexpr int kScaleArea = kTok * 16;
+constexpr int kSmemFp8 = kSmem + kStages * kScaleArea;
+static_assert(kSmemFp8 <= 232448, "shared memory budget (FP8 latent)");
 // Split merge: 64-column chunks of other splits' partials stream through the (then idle)
 // stage buffers, four at a time.
 constexpr int kMergeCols = 64;
@@ -86,8 +93,36 @@ constexpr uint32_t kMergeThreads = 5 * 32;                 // gather warp 0 + th
 constexpr uint32_t kSibBytes = 128 * 256 + 128 * 8;  // 128 rows x 128 fp16 columns, then (m, l) per row
 static_assert(2 * kSibBytes <= kStages * kStageBytes, "sibling merge buffers fit in the stage buffers");
 
+// 16 e4m3 codes times `sc` -> 16 bf16 (round to nearest even), as 8 packed pairs.
+__device__ __forceinline__ void e4m3x16_scaled_to_bf16(const uint4& raw, float sc, uint32_t (&out)[8]) {
+  const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+  const uint64_t sc2 = f2_pack(sc, sc);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w[i] & 0xFFFFu), __NV_E4M3);
+    const __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w[i] >> 16), __NV_E4M3);
+    float a0, a1, b0, b1;
+    f16x2_to_f32(*(const uint32_t*)&lo, a0, a1);
+    f16x2_to_f32(*(const uint32_t*)&hi, b0, b1);
+    f2_unpack(f2_mul(f2_pack(a0, a1), sc2), a0, a1);
+    f2_unpack(f2_mul(f2_pack(b0, b1), sc2), b0, b1);
+    out[2 * i] = cvt_bf16x2(a0, a1);
+    out[2 * i + 1] = cvt_bf16x2(b0, b1);
+  }
+}
+
 // Launched in clusters of two CTAs (the pair), or four (two splits x the pair) when the
 // two splits of a token merge inside the cluster.
+// FP8: the latent cache holds e4m3 codes with an f32 scale per 128-dim tile and bf16
+// rope dims.  The codes of this CTA's 256 latent dims land (TMA gather4, 128-byte
+// swizzled rows) in latent regions 2 and 3 of the stage, the row scales in the stage's
+// scale area and the rope dims in the rope region as for a bf16 cache; then the gather
+// warps turn each row into bf16 (code x scale, rounded to nearest even: exact when the
+// scale is a power of two) in latent regions 0-3, the layout the MMAs read.  Each row's
+// four 64-dim output pieces are written by four lanes of one warp after all four have
+// read their codes (the codes of row r sit in row r of regions 2-3, which pieces 2-3 of
+// row r overwrite), and kv_conv[stage] tells the MMA issuer that the tile is ready.
+template <bool FP8>
 __global__ void __launch_bounds__(kThreads, 1)
     sfa_tc_kernel(const __grid_constant__ CUtensorMap kvmap, const __grid_constant__ CUtensorMap ropemap,
                   const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap qropemap, SfaParams p) {
@@ -124,10 +159,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* m_full = m_ready + 1; // sibling merge: the sibling's columns arrived
   uint64_t* mfull = m_full + 1;   // [4]: split merge, a chunk of another split's partial landed
   uint64_t* mempty = mfull + 4;  // [4]: the merging warps (8-11) are done with that chunk buffer
-  uint32_t* tmem_base_s = (uint32_t*)(mempty + 4);
+  uint64_t* kv_conv = mempty + 4;  // [kStages] (FP8): the tile's rows are bf16 in the stage
+  uint32_t* tmem_base_s = (uint32_t*)(kv_conv + kStages);
   volatile int* abort_flag = (volatile int*)(tmem_base_s + 1);
   volatile int* last_s = (volatile int*)(abort_flag + 1);  // this CTA merges the splits
   int* last_valid_s = (int*)(last_s + 1);                   // last slot holding a selected row
+  float* scale_area = (float*)(bars + 64);                   // (FP8) [kStages][64 rows][4] f32
 
   int b, n_vis;
   resolve_token(p.tv, tok, &b, &n_vis, nullptr);
@@ -160,6 +197,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&mfull[i], 1);
       mbar_init(&mempty[i], 4);
     }
+    for (int i = 0; i < kStages; ++i) mbar_init(&kv_conv[i], kGatherWarps);
     *abort_flag = 0;
     *last_valid_s = -1;
     // the peer's partial logits of tiles 0 and 1 may arrive as soon as the cluster syncs
@@ -280,8 +318,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // latent dims (128-byte swizzled rows) and the 64-byte piece q = 4 of its rope dims
     // (64-byte swizzled rows), each one gather4 of four rows.  Gather i = 5g + q of a
     // tile is issued by lane i / 3 of warp i % 3.  Empty slots fetch a selected row;
-    // their logits are masked.
-    {
+    // their logits are masked.  (FP8: pieces q = 0, 1 of codes and q = 2 of rope per
+    // group, i = 3g + q, and each of the 64 rows' scales by one 16-byte copy; each warp
+    // converts tile n - 1 after issuing tile n, and the last tile after the loop.)
+    if constexpr (!FP8) {
       const int i = lane * kGatherWarps + warp;
       const bool mine = i < kGathers;
       const int g = i / 5, q = i - 5 * (i / 5);
@@ -306,6 +346,81 @@ __global__ void __launch_bounds__(kThreads, 1)
                       v.x >= 0 ? v.x : fill, v.y >= 0 ? v.y : fill, v.z >= 0 ? v.z : fill, v.w >= 0 ? v.w : fill);
         }
       }
+    } else {
+      const int i = lane * kGatherWarps + warp;
+      const bool gat = i < kGathersFp8;
+      const int g = i / 3, q = i - 3 * (i / 3);
+      const int x = q < 2 ? 256 * (int)c + 128 * q : 32 * (int)c;
+      const uint32_t doff = q < 2 ? (2 + q) * kRegion + g * 512 : 4 * kRegion + g * 256;
+      const CUtensorMap* map = q < 2 ? &kvmap : &ropemap;
+      // scale copies: lanes past the gathers take rows j and j + 48 (when below 64)
+      const int j0 = i - kGathersFp8;
+      const int nsc = gat ? 0 : (j0 + 48 < kTok ? 2 : 1);
+      const uint32_t my_bytes = __reduce_add_sync(0xffffffffu, gat ? (q < 2 ? 512u : 256u) : 16u * nsc);
+      bool good = true;
+      // converts tile m: rows [8 pp, 8 pp + 8) of the passes pp = warp, warp + 3, ...;
+      // lane = 4 * (row within the pass) + output piece
+      auto convert = [&](int m) {
+        const int stage = m % kStages;
+        bool ok = true;
+        if (lane == 0) ok = mbar_wait(&kv_full[stage], (m / kStages) & 1, abort_flag, p.err);
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        __syncwarp();
+        if (ok) {
+          uint8_t* st = stages + stage * kStageBytes;
+          const float* sca = scale_area + stage * (kTok * 4);
+          const int qo = lane & 3, piece = qo >> 1, half = qo & 1;
+          for (int pp = warp; pp < kTok / 8; pp += kGatherWarps) {
+            const int r = 8 * pp + (lane >> 2);
+            const uint32_t sw = (uint32_t)(r & 7);
+            const uint8_t* raw = st + (2 + piece) * kRegion + r * 128;
+            uint4 in[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) in[u] = *(const uint4*)(raw + ((((uint32_t)(4 * half + u)) ^ sw) << 4));
+            const float sc = sca[r * 4 + 2 * (int)c + piece];
+            __syncwarp();  // every lane has read its codes before any piece of its row is overwritten
+            uint8_t* out = st + qo * kRegion + r * 128;
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              uint32_t o[8];
+              e4m3x16_scaled_to_bf16(in[u], sc, o);
+              *(uint4*)(out + ((((uint32_t)(2 * u)) ^ sw) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+              *(uint4*)(out + ((((uint32_t)(2 * u + 1)) ^ sw) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
+            }
+            __syncwarp();
+          }
+          fence_proxy_async_smem();  // the MMAs read the rows (async proxy)
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&kv_conv[stage]);  // (also on failure: the issuer quits on the abort flag)
+        return ok;
+      };
+      for (int n = 0; n < n_tiles_run && good; ++n) {
+        const int stage = n % kStages;
+        if (lane == 0) {
+          if (n == 2) good = mbar_wait(q_ready, 0, abort_flag, p.err);
+          if (good) good = mbar_wait(&kv_empty[stage], ((n / kStages) & 1) ^ 1, abort_flag, p.err);
+          if (good) mbar_arrive_expect_tx(&kv_full[stage], my_bytes);
+        }
+        good = __shfl_sync(0xffffffffu, good, 0);  // warp-uniform from here on
+        if (!good) break;
+        __syncwarp();
+        uint8_t* st = stages + stage * kStageBytes;
+        if (gat) {
+          const int4 v = *(const int4*)(rowid + n * kTok + 4 * g);
+          tma_gather4(smem_u32(st) + doff, map, &kv_full[stage], x, v.x >= 0 ? v.x : fill, v.y >= 0 ? v.y : fill,
+                      v.z >= 0 ? v.z : fill, v.w >= 0 ? v.w : fill);
+        } else {
+          for (int k = 0; k < nsc; ++k) {
+            const int r = j0 + 48 * k;
+            const int rid = rowid[n * kTok + r];
+            bulk_load(smem_u32(scale_area + stage * (kTok * 4) + r * 4), p.kv_scale + (int64_t)(rid >= 0 ? rid : fill) * 4,
+                      16, &kv_full[stage]);
+          }
+        }
+        if (n > 0) good = convert(n - 1);
+      }
+      if (good && n_tiles_run > 0) convert(n_tiles_run - 1);
     }
     if (p.n_splits > 1 && !p.sib_merge && warp == 0) {
       // ---- split merge, producer: the other splits' partials, chunk by chunk -----------
@@ -363,7 +478,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int t = next_qk, stage = t % kStages, b = t & 1;
           bool ready = false;
           if (lane == 0)
-            ready = mbar_test(smem_u32(&kv_full[stage]), (t / kStages) & 1) &&
+            ready = mbar_test(smem_u32(FP8 ? &kv_conv[stage] : &kv_full[stage]), (t / kStages) & 1) &&
                     (t < 2 || mbar_test(smem_u32(&s_free[b]), ((t - 2) >> 1) & 1));
           if (__shfl_sync(0xffffffffu, ready, 0)) {
             tc_fence_after();
@@ -883,21 +998,29 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 cudaError_t launch_sfa_tc(const SfaParams& p, cudaStream_t s) {
   // the latent cache as [pages * 64 rows, 576]: one-row boxes of 64 elements (latent
-  // pieces, 128-byte swizzle) and of 32 elements (rope pieces, 64-byte swizzle)
+  // pieces, 128-byte swizzle) and of 32 elements (rope pieces, 64-byte swizzle); FP8:
+  // codes as [pages * 64, 512] with one-row boxes of 128 bytes, rope as [pages * 64, 64]
   CUtensorMap kvmap, ropemap;
   // Q as [tokens * heads, 576]: boxes of one token's heads, 64 elements (latent, 128-byte
   // swizzle) and 32 elements (rope, 64-byte swizzle) wide
   CUtensorMap qmap, qropemap;
-  if (!make_tma_2d_sw128(&kvmap, p.kv, (uint64_t)p.tv.num_pages * kPage, 2, kLatentDim, 1, false) ||
-      !make_tma_2d_sw64_rows(&ropemap, p.kv, (uint64_t)p.tv.num_pages * kPage, 2, kLatentDim) ||
+  const uint64_t rows = (uint64_t)p.tv.num_pages * kPage;
+  const bool fp8 = p.kv_codes != nullptr;
+  const bool kv_ok = fp8 ? make_tma_2d_sw128(&kvmap, p.kv_codes, rows, 1, kValueDim, 1, false) &&
+                               make_tma_2d_sw64_rows(&ropemap, p.kv_rope, rows, 2, kLatentDim - kValueDim)
+                         : make_tma_2d_sw128(&kvmap, p.kv, rows, 2, kLatentDim, 1, false) &&
+                               make_tma_2d_sw64_rows(&ropemap, p.kv, rows, 2, kLatentDim);
+  if (!kv_ok ||
       !make_tma_2d_sw128(&qmap, p.q, (uint64_t)p.tv.n_tokens * p.n_heads, 2, kLatentDim, p.n_heads, false) ||
       !make_tma_2d_sw64_rows(&qropemap, p.q, (uint64_t)p.tv.n_tokens * p.n_heads, 2, kLatentDim, p.n_heads))
     return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(sfa_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+  auto kernel = fp8 ? sfa_tc_kernel<true> : sfa_tc_kernel<false>;
+  const int smem = fp8 ? kSmemFp8 : kSmem;
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   dim3 grid(2 * p.n_splits, p.tv.n_tokens);
-  return launch_pdl_cluster(sfa_tc_kernel, grid, dim3(kThreads), kSmem, s, p.sib_merge ? 4u : 2u, kvmap, ropemap,
-                            qmap, qropemap, p);
+  return launch_pdl_cluster(kernel, grid, dim3(kThreads), smem, s, p.sib_merge ? 4u : 2u, kvmap, ropemap, qmap,
+                            qropemap, p);
 }
 
 }  // namespace dsa

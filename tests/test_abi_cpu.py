@@ -23,7 +23,7 @@ def test_exports_every_declared_symbol():
 
 
 def test_version_and_strings():
-    assert dsa.lib.dsa_abi_version() == 2
+    assert dsa.lib.dsa_abi_version() == 3
     assert dsa.lib.dsa_status_string(0) == b"DSA_OK"
     assert dsa.lib.dsa_status_string(3) == b"DSA_ERR_WORKSPACE"
 

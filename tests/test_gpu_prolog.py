@@ -124,3 +124,101 @@ def test_appended_cache_feeds_the_indexer_layout(dsa):
     assert normal.mean() > 0.5
     assert np.all(rel[normal] <= 2.0 ** -4)
     assert np.all(np.abs(back[y > 448]) == 448 * np.ldexp(1.0, scales.cpu().numpy().astype(np.int64) - 127).repeat(32, axis=1)[y > 448])
+
+
+# ---------------------------------------------------------------------------------
+# appends of new rows to bf16 / FP8 K-index caches and latent caches
+# ---------------------------------------------------------------------------------
+def _paged_layout(rng, pages=24):
+    B, maxp = 5, 6
+    lens = np.array([1, 64, 65, 300, 384], dtype=np.int32)
+    bt = np.full((B, maxp), -1, dtype=np.int32)
+    perm = rng.permutation(pages).astype(np.int32)
+    off = 0
+    for b in range(B):
+        npg = (lens[b] + 63) // 64
+        bt[b, :npg] = perm[off:off + npg]
+        off += npg
+    # a multi-token append with explicit positions, one on an unmapped page (skipped)
+    seq2 = np.array([3, 3, 3, 4, 0], dtype=np.int32)
+    pos2 = np.array([200, 201, 299, 383, 70], dtype=np.int32)
+    return pages, B, lens, bt, seq2, pos2
+
+
+def _run_two_appends(dsa, fn, k1, k2, bt, lens, seq2, pos2):
+    """fn(x, bt, lens, lens_host, ws, **tokens): a decode append (each sequence's newest
+    position) then the explicit multi-token one; returns the two error words."""
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    bt_d, lens_d, lens_h = dev(bt), dev(lens), torch.from_numpy(lens.copy())
+    ws = dsa.alloc_workspace(256)
+    fn(dev(k1.view(np.int16)), bt_d, lens_d, lens_h, ws)
+    e1 = dsa.read_device_error(ws)
+    dsa.clear_device_error(ws)
+    fn(dev(k2.view(np.int16)), bt_d, lens_d, lens_h, ws, token_seq=dev(seq2), token_pos=dev(pos2),
+       token_seq_host=torch.from_numpy(seq2.copy()), token_pos_host=torch.from_numpy(pos2.copy()))
+    return e1, dsa.read_device_error(ws)
+
+
+@pytest.mark.parametrize("fmt", ["bf16", "fp8"])
+@pytest.mark.parametrize("dim", [64, 128])
+def test_index_cache_append_formats_match_oracle(dsa, fmt, dim):
+    """bf16 rows copied; e4m3 rows with one f32 scale per token (absmax / 448) bit for bit
+    (codes and scale bits), including zero rows, signed zeros, subnormals and huge values."""
+    from oracle import fp8_quant as F
+    rng = np.random.default_rng(41 + dim)
+    pages, B, lens, bt, seq2, pos2 = _paged_layout(rng)
+    k1 = _rows(rng, 6, dim)[1:].copy()
+    k2 = _rows(rng, 6, dim)[::-1][:5].copy()
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    if fmt == "bf16":
+        cache0 = [rng.integers(0, 2 ** 16, (pages, 64, dim)).astype(np.uint16)]
+        d_c = dev(cache0[0].view(np.int16))
+        d_s = None
+        rows = lambda k: [k]
+    else:
+        cache0 = [rng.integers(0, 256, (pages, 64, dim)).astype(np.uint8),
+                  rng.standard_normal((pages, 64)).astype(np.float32)]
+        d_c, d_s = dev(cache0[0]), dev(cache0[1])
+        rows = lambda k: list(F.quantize_index_rows(k))
+    fn = lambda x, bt_d, lens_d, lens_h, ws, **kw: dsa.index_cache_append(x, d_c, d_s, bt_d, lens_d, lens_h, ws, **kw)
+    e1, e2 = _run_two_appends(dsa, fn, k1, k2, bt, lens, seq2, pos2)
+    assert e1 == 0 and e2 == dsa.DSA_DEVERR_PAGE_ID
+    want, bad = F.append(cache0, bt, np.arange(B), lens - 1, rows(k1))
+    assert bad == []
+    want, bad = F.append(want, bt, seq2, pos2, rows(k2))
+    assert bad == [4]
+    got = [d_c.cpu().numpy()] + ([d_s.cpu().numpy()] if d_s is not None else [])
+    for g, w in zip(got, want):
+        assert np.array_equal(g.view(np.uint8), np.ascontiguousarray(w).view(np.uint8))
+
+
+@pytest.mark.parametrize("fmt", ["bf16", "fp8"])
+def test_latent_cache_append_matches_oracle(dsa, fmt):
+    """bf16 latent rows copied; FP8 rows: each 128-dim latent tile quantised (absmax / 448)
+    to e4m3 codes and an f32 scale, the 64 rope dims copied, all bit for bit."""
+    from oracle import fp8_quant as F
+    rng = np.random.default_rng(53)
+    pages, B, lens, bt, seq2, pos2 = _paged_layout(rng)
+    k1 = _rows(rng, 6, 576)[1:].copy()
+    k2 = _rows(rng, 6, 576)[::-1][:5].copy()
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    if fmt == "bf16":
+        cache0 = [rng.integers(0, 2 ** 16, (pages, 64, 576)).astype(np.uint16)]
+        dc = [dev(cache0[0].view(np.int16))]
+        fn = lambda x, bt_d, lens_d, lens_h, ws, **kw: dsa.latent_cache_append(x, dc[0], bt_d, lens_d, lens_h, ws, **kw)
+        rows = lambda k: [k]
+    else:
+        cache0 = [rng.integers(0, 256, (pages, 64, 512)).astype(np.uint8),
+                  rng.standard_normal((pages, 64, 4)).astype(np.float32),
+                  rng.integers(0, 2 ** 16, (pages, 64, 64)).astype(np.uint16)]
+        dc = [dev(cache0[0]), dev(cache0[1]), dev(cache0[2].view(np.int16))]
+        fn = lambda x, bt_d, lens_d, lens_h, ws, **kw: dsa.latent_cache_append(
+            x, dc[0], bt_d, lens_d, lens_h, ws, cache_scale=dc[1], cache_rope=dc[2], **kw)
+        rows = lambda k: list(F.quantize_latent_rows(k))
+    e1, e2 = _run_two_appends(dsa, fn, k1, k2, bt, lens, seq2, pos2)
+    assert e1 == 0 and e2 == dsa.DSA_DEVERR_PAGE_ID
+    want, bad = F.append(cache0, bt, np.arange(B), lens - 1, rows(k1))
+    want, bad = F.append(want, bt, seq2, pos2, rows(k2))
+    assert bad == [4]
+    for g, w in zip(dc, want):
+        assert np.array_equal(g.cpu().numpy().view(np.uint8), np.ascontiguousarray(w).view(np.uint8))
