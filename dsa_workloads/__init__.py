@@ -207,6 +207,13 @@ SMALL_MULTI25 = Spec(
 SMALL_MULTI_FP8 = replace(SMALL_MULTI, name="small_multi_fp8", idx_dtype="e4m3", idx_scale="per_token", seed=7018,
                           description="multi-token decode with an e4m3 indexer (one key stream per token)")
 
+# five attention heads (not a multiple of four) and eight splits per token: the split
+# combine over a padded head stride
+SMALL_H5 = Spec(
+    name="small_h5", mode="decode", batch=3, seq_lens=(300, 777, 2100), pool_pages=60,
+    idx_heads=4, idx_dim=64, head_w_exps=(-3, 0), topk=512, sfa_heads=5, seed=7019,
+    description="5 SFA heads, 512 selected rows per token in eight splits")
+
 # long rows whose selection runs in clusters of eight CTAs (more than 16384 positions);
 # the tests give them degenerate queries (all scores equal, or 17 distinct values) so
 # that a CTA's boundary bin overflows its share of the candidate pool
@@ -217,7 +224,7 @@ LONG_ROWS = Spec(
 
 SMALL = [SMALL_DECODE_BF16, SMALL_DECODE_FP8, SMALL_DECODE_MX, SMALL_TIES, SMALL_PREFILL,
          SMALL_H8, EMPTY_AND_SHORT, SMALL_MID, SMALL_SIB, SMALL_MULTI, SMALL_FP8_D64, SMALL_MX_D64,
-         SMALL_PREFILL_FP8, SMALL_PREFILL_MX, SMALL_MULTI25, SMALL_MULTI_FP8, SMALL_FP8_KV]
+         SMALL_PREFILL_FP8, SMALL_PREFILL_MX, SMALL_MULTI25, SMALL_MULTI_FP8, SMALL_FP8_KV, SMALL_H5]
 
 ALL = {s.name: s for s in HEADLINE + EXTRA + SMALL + [LONG_ROWS]}
 

@@ -145,9 +145,8 @@ __global__ void __launch_bounds__(256) clear_kernel(uint4* p, size_t n16) {
 }
 
 // ---- workspace plans ------------------------------------------------------------------
-// Workspace: [0, 256) the device error word; for split attention, the split counters;
-// then one region the passes use in turn (the indexer's key histograms and score rows,
-// later the attention's split partials).
+// Workspace: [0, 256) the device error word; then one region the passes use in turn (the
+// indexer's key histograms and score rows, later the attention's split partials).
 // Which scoring kernel serves the call.  Row-blocked: identity activation and tokens in
 // segments of consecutive rows of one sequence (a prefill: one segment; multi-token
 // decode: each sequence's draft tokens, all segments of one length), so that the rows of
@@ -230,15 +229,13 @@ IndexerPlan plan_indexer(const dsa_indexer_args_t* a, const dsa_index_cache_t* c
 struct SfaPlan {
   int32_t n_splits, split_len;
   bool sib_merge;                      // two splits merged inside their cluster
-  size_t cnt_bytes;                    // split counters, right after the error word
-  size_t part_o_bytes, part_lse_bytes;  // in the shared region
+  size_t part_o_bytes, part_lse_bytes;  // in the shared region (more than two splits)
   size_t region_bytes() const { return part_o_bytes + part_lse_bytes; }
 };
 
 SfaPlan plan_sfa(int32_t n_tokens, int32_t n_heads, int32_t top_k) {
   SfaPlan p;
   const int tiles = (top_k + 63) / 64;
-  (void)n_heads;
   const int units = n_tokens * 2;  // one CTA pair per (token, split)
   int s = device_sm_count() / (units > 0 ? units : 1);
   if (s < 1) s = 1;
@@ -249,11 +246,11 @@ SfaPlan plan_sfa(int32_t n_tokens, int32_t n_heads, int32_t top_k) {
   p.n_splits = (tiles * 64 + p.split_len - 1) / p.split_len;  // drop empty splits
   p.sib_merge = p.n_splits == 2;
   if (p.n_splits > 1 && !p.sib_merge) {
-    p.cnt_bytes = align_up((size_t)n_tokens * 2 * sizeof(uint32_t));
-    p.part_o_bytes = align_up((size_t)n_tokens * p.n_splits * n_heads * kValueDim * sizeof(float));
-    p.part_lse_bytes = align_up((size_t)n_tokens * p.n_splits * 2 * n_heads * sizeof(float));
+    const size_t hp = (size_t)(n_heads + 3) / 4 * 4;  // head stride rounded up for 16-byte loads
+    p.part_o_bytes = align_up((size_t)n_tokens * p.n_splits * hp * kValueDim * sizeof(float));
+    p.part_lse_bytes = align_up((size_t)n_tokens * p.n_splits * 2 * hp * sizeof(float));
   } else {
-    p.cnt_bytes = p.part_o_bytes = p.part_lse_bytes = 0;
+    p.part_o_bytes = p.part_lse_bytes = 0;
   }
   return p;
 }
@@ -383,12 +380,10 @@ dsa_status_t run_indexer(const dsa_indexer_args_t* a, const dsa_index_cache_t* c
   return DSA_OK;
 }
 
-// `cnt`: the split counters (zero on entry when `cnt_zeroed`, else cleared here);
 // `region`: the pass region for the split partials.
 dsa_status_t run_sfa(const dsa_sfa_args_t* a, const dsa_latent_cache_t* c, const dsa_page_table_t* pg,
                      const dsa_tokens_t* tk, int32_t max_visible, const int32_t* idx, int32_t top_k, void* out,
-                     uint32_t* err, uint32_t* cnt, bool cnt_zeroed, uint8_t* region, const SfaPlan& sp_,
-                     cudaStream_t s, Tracer& tr) {
+                     uint32_t* err, uint8_t* region, const SfaPlan& sp_, cudaStream_t s, Tracer& tr) {
   SfaParams p;
   p.tv = token_view(pg, tk, max_visible);
   p.q = (const uint16_t*)a->q;
@@ -402,7 +397,6 @@ dsa_status_t run_sfa(const dsa_sfa_args_t* a, const dsa_latent_cache_t* c, const
   const bool global_merge = sp_.n_splits > 1 && !sp_.sib_merge;
   p.part_o = global_merge ? (float*)region : nullptr;
   p.part_lse = global_merge ? (float*)(region + sp_.part_o_bytes) : nullptr;
-  p.merge_cnt = global_merge ? cnt : nullptr;
   p.sib_merge = sp_.sib_merge ? 1 : 0;
   p.err = err;
   p.n_heads = a->n_heads;
@@ -410,14 +404,16 @@ dsa_status_t run_sfa(const dsa_sfa_args_t* a, const dsa_latent_cache_t* c, const
   p.n_splits = sp_.n_splits;
   p.split_len = sp_.split_len;
   p.scale_log2 = a->softmax_scale * 1.4426950408889634f;
-  if (global_merge && !cnt_zeroed) {
-    cudaError_t me = launch_clear(cnt, sp_.cnt_bytes, s);
-    if (me != cudaSuccess) return cuda_fail(me, "clearing the split counters");
-  }
   tr.begin();
   cudaError_t e = launch_sfa_tc(p, s);
   tr.end("sfa");
   if (e != cudaSuccess) return cuda_fail(e, "sparse attention launch");
+  if (global_merge) {
+    tr.begin();
+    e = launch_sfa_combine(p, s);
+    tr.end("sfa_combine");
+    if (e != cudaSuccess) return cuda_fail(e, "split combine launch");
+  }
   return DSA_OK;
 }
 
@@ -481,7 +477,7 @@ size_t dsa_sparse_attn_workspace_size(const dsa_sfa_args_t* args, const dsa_page
   if (check_sfa(args, nullptr) != DSA_OK || check_pages_tokens(pages, tokens, &mv) != DSA_OK) return 0;
   if (top_k < 1 || top_k > kMaxTopK) return 0;
   SfaPlan sp = plan_sfa(tokens->n_tokens, args->n_heads, top_k);
-  return kAlign + sp.cnt_bytes + sp.region_bytes();
+  return kAlign + sp.region_bytes();
 }
 
 dsa_status_t dsa_sparse_attn(const dsa_sfa_args_t* args, const dsa_latent_cache_t* cache,
@@ -497,11 +493,11 @@ dsa_status_t dsa_sparse_attn(const dsa_sfa_args_t* args, const dsa_latent_cache_
   if (!aligned16(out)) return fail(DSA_ERR_INVALID_ARG, "out must be 16-byte aligned");
   if (top_k < 1 || top_k > kMaxTopK) return fail(DSA_ERR_UNSUPPORTED, "top_k must be in [1, %d]", kMaxTopK);
   SfaPlan sp = plan_sfa(tokens->n_tokens, args->n_heads, top_k);
-  if ((st = check_ws(ws, ws_bytes, kAlign + sp.cnt_bytes + sp.region_bytes())) != DSA_OK) return st;
+  if ((st = check_ws(ws, ws_bytes, kAlign + sp.region_bytes())) != DSA_OK) return st;
   Tracer tr(trace, (cudaStream_t)stream);
   uint8_t* w8 = (uint8_t*)ws;
-  st = run_sfa(args, cache, pages, tokens, mv, idx, top_k, out, (uint32_t*)ws, (uint32_t*)(w8 + kAlign), false,
-               w8 + kAlign + sp.cnt_bytes, sp, (cudaStream_t)stream, tr);
+  st = run_sfa(args, cache, pages, tokens, mv, idx, top_k, out, (uint32_t*)ws, w8 + kAlign, sp, (cudaStream_t)stream,
+               tr);
   if (st == DSA_OK && tr.status != cudaSuccess) return cuda_fail(tr.status, "recording a trace event");
   return st;
 }
@@ -516,7 +512,7 @@ size_t dsa_fused_workspace_size(const dsa_indexer_args_t* iargs, const dsa_index
   IndexerPlan ip = plan_indexer(iargs, icache, pages, tokens, mv);
   SfaPlan sp = plan_sfa(tokens->n_tokens, sargs->n_heads, iargs->top_k);
   const size_t sfa_b = sp.region_bytes();
-  return kAlign + sp.cnt_bytes + (ip.score_bytes > sfa_b ? ip.score_bytes : sfa_b);  // the passes reuse one region
+  return kAlign + (ip.score_bytes > sfa_b ? ip.score_bytes : sfa_b);  // the passes reuse one region
 }
 
 dsa_status_t dsa_fused_decode(const dsa_indexer_args_t* iargs, const dsa_index_cache_t* icache,
@@ -534,18 +530,17 @@ dsa_status_t dsa_fused_decode(const dsa_indexer_args_t* iargs, const dsa_index_c
   IndexerPlan ip = plan_indexer(iargs, icache, pages, tokens, mv);
   SfaPlan sp = plan_sfa(tokens->n_tokens, sargs->n_heads, iargs->top_k);
   const size_t sfa_b = sp.region_bytes();
-  if ((st = check_ws(ws, ws_bytes, kAlign + sp.cnt_bytes + (ip.score_bytes > sfa_b ? ip.score_bytes : sfa_b))) !=
+  if ((st = check_ws(ws, ws_bytes, kAlign + (ip.score_bytes > sfa_b ? ip.score_bytes : sfa_b))) !=
       DSA_OK)
     return st;
   Tracer tr(trace, (cudaStream_t)stream);
   uint8_t* w8 = (uint8_t*)ws;
-  uint32_t* cnt = (uint32_t*)(w8 + kAlign);
-  uint8_t* region = w8 + kAlign + sp.cnt_bytes;
-  // one clear covers the split counters and the histograms that follow them
-  if ((st = run_indexer(iargs, icache, pages, tokens, ip, out_idx, nullptr, (uint32_t*)ws, region, cnt,
-                        sp.cnt_bytes + ip.hist_bytes, (cudaStream_t)stream, tr)) != DSA_OK)
+  uint8_t* region = w8 + kAlign;
+  // the indexer's clear zeroes the key histograms at the start of the region
+  if ((st = run_indexer(iargs, icache, pages, tokens, ip, out_idx, nullptr, (uint32_t*)ws, region, region,
+                        ip.hist_bytes, (cudaStream_t)stream, tr)) != DSA_OK)
     return st;
-  st = run_sfa(sargs, lcache, pages, tokens, mv, out_idx, iargs->top_k, out, (uint32_t*)ws, cnt, true, region, sp,
+  st = run_sfa(sargs, lcache, pages, tokens, mv, out_idx, iargs->top_k, out, (uint32_t*)ws, region, sp,
                (cudaStream_t)stream, tr);
   if (st == DSA_OK && tr.status != cudaSuccess) return cuda_fail(tr.status, "recording a trace event");
   return st;

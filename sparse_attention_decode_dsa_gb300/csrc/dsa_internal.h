@@ -78,9 +78,9 @@ struct SfaParams {
   const uint16_t* kv_rope; //   bf16 [num_pages, 64, 64]
   const int32_t* idx;      // [T, K]
   uint16_t* out;           // bf16 [T, H, 512]
-  float* part_o;           // [T, S, 2 halves, 256 dims, H]: each split's O / l (null when S == 1)
-  float* part_lse;         // [T, S, 2 halves, H]: each split's log2-sum-exp of its logits
-  uint32_t* merge_cnt;     // [T, 2 halves]: splits done so far; zero before the launch, left zero
+  float* part_o;           // [T, S, 2 halves, 256 dims, HP]: each split's O / l (more than two
+                           // splits); HP = H rounded up to a multiple of 4
+  float* part_lse;         // [T, S, 2 halves, HP]: each split's log2-sum-exp of its logits
   uint32_t* err;
   int32_t n_heads, top_k, n_splits, split_len;
   int32_t sib_merge;       // two splits, merged inside a cluster of four (no partials in memory)
@@ -173,6 +173,8 @@ constexpr int kBlockedMaxSeg = 1024;  // longest segment of several sequences' r
 cudaError_t launch_score_tc_blocked(const ScoreParams& p, cudaStream_t s);
 cudaError_t launch_topk(const TopkParams& p, int32_t max_visible, cudaStream_t s);
 cudaError_t launch_sfa_tc(const SfaParams& p, cudaStream_t s);
+// More than two splits: the merge of the attention kernel's partials into p.out.
+cudaError_t launch_sfa_combine(const SfaParams& p, cudaStream_t s);
 cudaError_t launch_clear(void* p, size_t bytes, cudaStream_t s);  // bytes: multiple of 16
 
 // Index prolog: MXFP8 quantisation (groups of 32) of bf16 rows, written to row i of

@@ -58,7 +58,9 @@ constexpr int kSendWarp0 = kMmaWarp + 1;          // warps 4-7 load and send the
 constexpr int kFinWarp0 = kSendWarp0 + 4;         // warps 8-11 finish key columns 0-31 of each tile and run
                                                   // the epilogue
 constexpr int kFinWarpB0 = kFinWarp0 + 4;         // warps 12-15 finish key columns 32-63
-constexpr int kThreads = (kFinWarpB0 + 4) * 32;
+constexpr int kExtraWarp0 = kFinWarpB0 + 4;       // warps 16-19: gather too (bf16 cache) or convert
+                                                  // the gathered FP8 rows (FP8 cache)
+constexpr int kThreads = (kExtraWarp0 + 4) * 32;
 constexpr int kTok = 64;                         // selected positions per tile
 constexpr int kStages = 4;
 constexpr int kRegion = kTok * 128;              // 64 rows x 128 B
@@ -76,38 +78,45 @@ constexpr int kSmem = 1024 + kStages * kStageBytes + kQropeBytes + 3 * kXchBytes
 static_assert(kSmem <= 232448, "shared memory budget");
 // FP8 latent cache: per tile and group of 4 slots, two 128-byte pieces of e4m3 codes
 // (this CTA's 256 latent dims) and the 64-byte rope piece; plus one 16-byte copy of each
-// row's four tile scales into a per-stage scale area [64 rows][4] f32.
+// row's four tile scales into a per-stage scale area [64 rows][4] f32, on the load/store
+// path (cp.async), beside the 48 gathers of a tile; the 48 copying lanes arrive on
+// kv_full as their copies land.
 constexpr int kGathersFp8 = (kTok / 4) * 3;
+constexpr int kScaleLanes = kGatherWarps * 32 - kGathersFp8;  // lanes of warps 0-2 past the gathers
+constexpr int kConvWarps = 4;                                 // warps 16-19
 constexpr int kScaleArea = kTok * 16;
 constexpr int kSmemFp8 = kSmem + kStages * kScaleArea;
 static_assert(kSmemFp8 <= 232448, "shared memory budget (FP8 latent)");
-// Split merge: 64-column chunks of other splits' partials stream through the (then idle)
-// stage buffers, four at a time.
-constexpr int kMergeCols = 64;
-constexpr int kMergeBuf = kMergeCols * kMaxSfaHeads * 4;  // 32 KB
-static_assert(4 * kMergeBuf <= kStages * kStageBytes, "merge ring fits in the stage buffers");
-static_assert(16 * kMaxSfaHeads * 4 <= 2 * kXchBytes, "split weights fit in the exchange buffers");
-constexpr uint32_t kMergeThreads = 5 * 32;                 // gather warp 0 + the four finishing warps
+static_assert(kScaleLanes == 48 && kTok - kScaleLanes <= kScaleLanes, "scale rows j and j + 48 cover the tile");
 // Sibling merge (two splits in one cluster): outbox and inbox of 128 rows x 128 f32
 // columns plus 128 (m, l) pairs each, in the stage buffers.
 constexpr uint32_t kSibBytes = 128 * 256 + 128 * 8;  // 128 rows x 128 fp16 columns, then (m, l) per row
 static_assert(2 * kSibBytes <= kStages * kStageBytes, "sibling merge buffers fit in the stage buffers");
 
-// 16 e4m3 codes times `sc` -> 16 bf16 (round to nearest even), as 8 packed pairs.
-__device__ __forceinline__ void e4m3x16_scaled_to_bf16(const uint4& raw, float sc, uint32_t (&out)[8]) {
+// Packed bf16 product (round to nearest even; subnormal inputs and results kept).
+__device__ __forceinline__ uint32_t mul_bf16x2(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("mul.rn.bf16x2 %0, %1, %2;\n" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+
+// 16 e4m3 codes times a scale -> 16 bf16, as 8 packed pairs, without the conversion pipe
+// (which the softmax warps keep busy): each code's bits s.eeee.mmm are spread into a
+// bf16 field as s.0000eeee.mmm0000, which encodes exactly code * 2^-120 (e = 0, the
+// E4M3 subnormals, becoming bf16 subnormals), then two packed products: by 2^60 (exact)
+// and by sc60 = bf16(scale * 2^60), one rounding.  (The scale enters rounded to bf16:
+// exact for power-of-two scales, else within 2^-9 relative of the f32 scale.)
+__device__ __forceinline__ void e4m3x16_scaled_to_bf16(const uint4& raw, uint32_t sc60, uint32_t (&out)[8]) {
   const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
-  const uint64_t sc2 = f2_pack(sc, sc);
+  constexpr uint32_t kTwo60 = 0x5D805D80u;  // bf16 pair (2^60, 2^60)
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    const __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w[i] & 0xFFFFu), __NV_E4M3);
-    const __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w[i] >> 16), __NV_E4M3);
-    float a0, a1, b0, b1;
-    f16x2_to_f32(*(const uint32_t*)&lo, a0, a1);
-    f16x2_to_f32(*(const uint32_t*)&hi, b0, b1);
-    f2_unpack(f2_mul(f2_pack(a0, a1), sc2), a0, a1);
-    f2_unpack(f2_mul(f2_pack(b0, b1), sc2), b0, b1);
-    out[2 * i] = cvt_bf16x2(a0, a1);
-    out[2 * i + 1] = cvt_bf16x2(b0, b1);
+#pragma unroll
+    for (int hf = 0; hf < 2; ++hf) {
+      const uint32_t t = __byte_perm(w[i], 0u, hf ? 0x4342u : 0x4140u);  // bytes 2hf, 2hf+1 in 16-bit lanes
+      const uint32_t f = ((t << 4) & 0x07F007F0u) | ((t << 8) & 0x80008000u);
+      out[2 * i + hf] = mul_bf16x2(mul_bf16x2(f, kTwo60), sc60);
+    }
   }
 }
 
@@ -157,13 +166,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* q_tma = drain + 1;    // Q (own dims) landed in shared memory
   uint64_t* m_ready = q_tma + 1;  // sibling merge: the sibling's inbox is free
   uint64_t* m_full = m_ready + 1; // sibling merge: the sibling's columns arrived
-  uint64_t* mfull = m_full + 1;   // [4]: split merge, a chunk of another split's partial landed
-  uint64_t* mempty = mfull + 4;  // [4]: the merging warps (8-11) are done with that chunk buffer
-  uint64_t* kv_conv = mempty + 4;  // [kStages] (FP8): the tile's rows are bf16 in the stage
+  uint64_t* kv_conv = m_full + 1;  // [kStages] (FP8): the tile's rows are bf16 in the stage
   uint32_t* tmem_base_s = (uint32_t*)(kv_conv + kStages);
   volatile int* abort_flag = (volatile int*)(tmem_base_s + 1);
-  volatile int* last_s = (volatile int*)(abort_flag + 1);  // this CTA merges the splits
-  int* last_valid_s = (int*)(last_s + 1);                   // last slot holding a selected row
+  int* last_valid_s = (int*)(abort_flag + 1);                // last slot holding a selected row
   float* scale_area = (float*)(bars + 64);                   // (FP8) [kStages][64 rows][4] f32
 
   int b, n_vis;
@@ -175,7 +181,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(&kv_full[s], kGatherWarps);
+      mbar_init(&kv_full[s], FP8 ? kGatherWarps + kScaleLanes : kGatherWarps + 4);
       mbar_init(&kv_empty[s], 1);
     }
     mbar_init(q_ready, 4);
@@ -193,11 +199,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(q_tma, 1);
     mbar_init(m_ready, 1);
     mbar_init(m_full, 1);
-    for (int i = 0; i < 4; ++i) {
-      mbar_init(&mfull[i], 1);
-      mbar_init(&mempty[i], 4);
-    }
-    for (int i = 0; i < kStages; ++i) mbar_init(&kv_conv[i], kGatherWarps);
+    for (int i = 0; i < kStages; ++i) mbar_init(&kv_conv[i], kConvWarps);
     *abort_flag = 0;
     *last_valid_s = -1;
     // the peer's partial logits of tiles 0 and 1 may arrive as soon as the cluster syncs
@@ -312,17 +314,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int n_tiles_run = last_valid >= 0 ? last_valid / kTok + 1 : 0;
   cluster_wait();  // both CTAs' barriers exist before any remote traffic
 
-  if (warp < kGatherWarps) {
+  if (warp < kGatherWarps || warp >= kExtraWarp0) {
     // ============================ gather (TMA) =========================================
     // Per tile and per group g of 4 slots: four 128-byte pieces q = 0..3 of this CTA's
     // latent dims (128-byte swizzled rows) and the 64-byte piece q = 4 of its rope dims
     // (64-byte swizzled rows), each one gather4 of four rows.  Gather i = 5g + q of a
-    // tile is issued by lane i / 3 of warp i % 3.  Empty slots fetch a selected row;
-    // their logits are masked.  (FP8: pieces q = 0, 1 of codes and q = 2 of rope per
-    // group, i = 3g + q, and each of the 64 rows' scales by one 16-byte copy; each warp
-    // converts tile n - 1 after issuing tile n, and the last tile after the loop.)
+    // tile is issued by lane i / 7 of gather warp i % 7 (warps 0-2, then 16-19).  Empty slots fetch a selected row;
+    // their logits are masked; warps 16-19 take gathers too (7 warps: issuing a gather
+    // costs its warp ~50 ns, so the issue is spread).  (FP8: pieces q = 0, 1 of codes and
+    // q = 2 of rope per group, i = 3g + q, by warps 0-2, whose remaining lanes copy the
+    // rows' scales; warps 16-19 convert each tile once it has landed.)
     if constexpr (!FP8) {
-      const int i = lane * kGatherWarps + warp;
+      const int gw = warp < kGatherWarps ? warp : kGatherWarps + (warp - kExtraWarp0);  // 7 gather warps
+      const int i = lane * (kGatherWarps + 4) + gw;
       const bool mine = i < kGathers;
       const int g = i / 5, q = i - 5 * (i / 5);
       const int x = q < 4 ? 256 * (int)c + 64 * q : 512 + 32 * (int)c;
@@ -346,110 +350,92 @@ __global__ void __launch_bounds__(kThreads, 1)
                       v.x >= 0 ? v.x : fill, v.y >= 0 ? v.y : fill, v.z >= 0 ? v.z : fill, v.w >= 0 ? v.w : fill);
         }
       }
-    } else {
+    } else if (warp < kGatherWarps) {
+      // FP8, issuers (warps 0-2, blocking waits): lane l of warp w takes item i = 3 l + w:
+      // gather i (i < 48: pieces q = i % 3 of group i / 3), else the scale copies of rows
+      // j = i - 48 and j + 48 (below 64)
       const int i = lane * kGatherWarps + warp;
       const bool gat = i < kGathersFp8;
       const int g = i / 3, q = i - 3 * (i / 3);
       const int x = q < 2 ? 256 * (int)c + 128 * q : 32 * (int)c;
       const uint32_t doff = q < 2 ? (2 + q) * kRegion + g * 512 : 4 * kRegion + g * 256;
       const CUtensorMap* map = q < 2 ? &kvmap : &ropemap;
-      // scale copies: lanes past the gathers take rows j and j + 48 (when below 64)
       const int j0 = i - kGathersFp8;
-      const int nsc = gat ? 0 : (j0 + 48 < kTok ? 2 : 1);
-      const uint32_t my_bytes = __reduce_add_sync(0xffffffffu, gat ? (q < 2 ? 512u : 256u) : 16u * nsc);
-      bool good = true;
-      // converts tile m: rows [8 pp, 8 pp + 8) of the passes pp = warp, warp + 3, ...;
-      // lane = 4 * (row within the pass) + output piece
-      auto convert = [&](int m) {
-        const int stage = m % kStages;
-        bool ok = true;
-        if (lane == 0) ok = mbar_wait(&kv_full[stage], (m / kStages) & 1, abort_flag, p.err);
-        ok = __shfl_sync(0xffffffffu, ok, 0);
-        __syncwarp();
-        if (ok) {
-          uint8_t* st = stages + stage * kStageBytes;
-          const float* sca = scale_area + stage * (kTok * 4);
-          const int qo = lane & 3, piece = qo >> 1, half = qo & 1;
-          for (int pp = warp; pp < kTok / 8; pp += kGatherWarps) {
-            const int r = 8 * pp + (lane >> 2);
-            const uint32_t sw = (uint32_t)(r & 7);
-            const uint8_t* raw = st + (2 + piece) * kRegion + r * 128;
-            uint4 in[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) in[u] = *(const uint4*)(raw + ((((uint32_t)(4 * half + u)) ^ sw) << 4));
-            const float sc = sca[r * 4 + 2 * (int)c + piece];
-            __syncwarp();  // every lane has read its codes before any piece of its row is overwritten
-            uint8_t* out = st + qo * kRegion + r * 128;
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              uint32_t o[8];
-              e4m3x16_scaled_to_bf16(in[u], sc, o);
-              *(uint4*)(out + ((((uint32_t)(2 * u)) ^ sw) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
-              *(uint4*)(out + ((((uint32_t)(2 * u + 1)) ^ sw) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
-            }
-            __syncwarp();
-          }
-          fence_proxy_async_smem();  // the MMAs read the rows (async proxy)
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&kv_conv[stage]);  // (also on failure: the issuer quits on the abort flag)
-        return ok;
-      };
-      for (int n = 0; n < n_tiles_run && good; ++n) {
+      const uint32_t my_bytes = __reduce_add_sync(0xffffffffu, gat ? (q < 2 ? 512u : 256u) : 0u);
+      uint32_t armed = 0, armed_parity = 0;  // stages with copies issued, and their phase parity
+      for (int n = 0; n < n_tiles_run; ++n) {
         const int stage = n % kStages;
+        bool good = true;
         if (lane == 0) {
+          // stage buffers 2-3 hold Q until the sending warps have moved it to tensor memory
           if (n == 2) good = mbar_wait(q_ready, 0, abort_flag, p.err);
           if (good) good = mbar_wait(&kv_empty[stage], ((n / kStages) & 1) ^ 1, abort_flag, p.err);
           if (good) mbar_arrive_expect_tx(&kv_full[stage], my_bytes);
         }
-        good = __shfl_sync(0xffffffffu, good, 0);  // warp-uniform from here on
-        if (!good) break;
+        if (!__shfl_sync(0xffffffffu, good, 0)) break;
         __syncwarp();
-        uint8_t* st = stages + stage * kStageBytes;
+        armed |= 1u << stage;
+        armed_parity = (armed_parity & ~(1u << stage)) | ((uint32_t)((n / kStages) & 1) << stage);
         if (gat) {
           const int4 v = *(const int4*)(rowid + n * kTok + 4 * g);
-          tma_gather4(smem_u32(st) + doff, map, &kv_full[stage], x, v.x >= 0 ? v.x : fill, v.y >= 0 ? v.y : fill,
-                      v.z >= 0 ? v.z : fill, v.w >= 0 ? v.w : fill);
+          tma_gather4(smem_u32(stages + stage * kStageBytes) + doff, map, &kv_full[stage], x, v.x >= 0 ? v.x : fill,
+                      v.y >= 0 ? v.y : fill, v.z >= 0 ? v.z : fill, v.w >= 0 ? v.w : fill);
         } else {
-          for (int k = 0; k < nsc; ++k) {
-            const int r = j0 + 48 * k;
+          for (int r = j0; r < kTok; r += kScaleLanes) {
             const int rid = rowid[n * kTok + r];
-            bulk_load(smem_u32(scale_area + stage * (kTok * 4) + r * 4), p.kv_scale + (int64_t)(rid >= 0 ? rid : fill) * 4,
-                      16, &kv_full[stage]);
+            cp_async16(smem_u32(scale_area + stage * (kTok * 4) + r * 4),
+                       p.kv_scale + (int64_t)(rid >= 0 ? rid : fill) * 4);
           }
+          cp_async_arrive_noinc(&kv_full[stage]);
         }
-        if (n > 0) good = convert(n - 1);
       }
-      if (good && n_tiles_run > 0) convert(n_tiles_run - 1);
-    }
-    if (p.n_splits > 1 && !p.sib_merge && warp == 0) {
-      // ---- split merge, producer: the other splits' partials, chunk by chunk -----------
-      __syncwarp();
-      named_bar_sync(1, kMergeThreads);  // partials published
-      named_bar_sync(1, kMergeThreads);  // the counter says whether this CTA merges
-      if (*last_s && lane == 0) {
-        fence_proxy_async_global();
-        const int S = p.n_splits;
-        const int64_t base = (int64_t)tok * S * 2 + c;
-        const uint32_t bytes = kMergeCols * H * 4;
-        int q = 0;
-        bool good = true;
-        for (int k = 0; good && k < 256 / kMergeCols; ++k)
-          for (int s2 = 0; good && s2 < S; ++s2) {
-            if (s2 == split) continue;
-            const int bi = q & 3;
-            if (q >= 4 && !(good = mbar_wait(&mempty[bi], ((q >> 2) - 1) & 1, abort_flag, p.err))) break;
-            mbar_arrive_expect_tx(&mfull[bi], bytes);
-            bulk_load(smem_u32(stages) + bi * kMergeBuf, p.part_o + ((base + 2 * s2) * 256 + kMergeCols * k) * H,
-                      bytes, &mfull[bi]);
-            ++q;
-          }
-        // nothing may still be landing in shared memory when the CTA exits
-        for (int i = q > 4 ? q - 4 : 0; i < q; ++i) {
+      // nothing may still be landing in shared memory once the CTA moves on (on the normal
+      // path these phases completed long ago)
+      if (lane == 0) {
+        for (int st = 0; st < kStages; ++st) {
+          if (!(armed >> st & 1)) continue;
           const long long t0 = clock64();
-          while (!mbar_try_wait(smem_u32(&mfull[i & 3]), (i >> 2) & 1) && clock64() - t0 < kWaitLimitCycles) {
+          while (!mbar_try_wait(smem_u32(&kv_full[st]), (armed_parity >> st) & 1) && clock64() - t0 < kWaitLimitCycles) {
           }
         }
+      }
+      __syncwarp();
+    } else {
+      // FP8, converters (warps 16-19, blocking waits): tile m once its rows have landed,
+      // rows [8 pp, 8 pp + 8) of the passes pp = warp - 16, warp - 12; lane = 4 * (row
+      // within the pass) + output piece
+      const int qo = lane & 3, piece = qo >> 1, half = qo & 1;
+      for (int m = 0; m < n_tiles_run; ++m) {
+        const int stage = m % kStages;
+        bool ok = true;
+        if (lane == 0) ok = mbar_wait(&kv_full[stage], (m / kStages) & 1, abort_flag, p.err);
+        if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+        __syncwarp();
+        uint8_t* st = stages + stage * kStageBytes;
+        const float* sca = scale_area + stage * (kTok * 4);
+        for (int pp = warp - kExtraWarp0; pp < kTok / 8; pp += kConvWarps) {
+          const int r = 8 * pp + (lane >> 2);
+          const uint32_t sw = (uint32_t)(r & 7);
+          const uint8_t* raw = st + (2 + piece) * kRegion + r * 128;
+          uint4 in[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) in[u] = *(const uint4*)(raw + ((((uint32_t)(4 * half + u)) ^ sw) << 4));
+          const float sc60 = sca[r * 4 + 2 * (int)c + piece] * 0x1p60f;  // exact: a power-of-two factor
+          const uint32_t sc2 = pack_bf16x2(sc60, sc60);
+          __syncwarp();  // every lane has read its codes before any piece of its row is overwritten
+          uint8_t* out = st + qo * kRegion + r * 128;
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            uint32_t o[8];
+            e4m3x16_scaled_to_bf16(in[u], sc2, o);
+            *(uint4*)(out + ((((uint32_t)(2 * u)) ^ sw) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+            *(uint4*)(out + ((((uint32_t)(2 * u + 1)) ^ sw) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
+          }
+          __syncwarp();
+        }
+        fence_proxy_async_smem();  // the MMAs read the rows (async proxy)
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&kv_conv[stage]);
       }
     }
   } else if (warp == kMmaWarp) {
@@ -875,11 +861,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     } else {
-      // Publish this split's part of the CTA's value half: O / l (column-major, so the
-      // stores and the merge's loads are coalesced across heads) and log2-sum-exp.
+      // More than two splits: publish this split's part of the CTA's value half, O / l
+      // (column-major, so the stores and the combine's loads are coalesced across heads)
+      // and its log2-sum-exp.
       const int64_t half_id = ((int64_t)tok * p.n_splits + split) * 2 + c;
       if (ok) {
-        float* po = p.part_o + half_id * 256 * H;
+        const int HP = (H + 3) & ~3;  // head stride of the partials (16-byte rows for the combine)
+        float* po = p.part_o + half_id * 256 * HP;
 #pragma unroll 1
         for (int ch = 0; ch < 8; ++ch) {
           uint32_t v[32];
@@ -892,93 +880,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           if (!live) continue;
 #pragma unroll
-          for (int j = 0; j < 32; ++j) po[(32 * ch + j) * H + h] = __uint_as_float(v[j]) * inv;
+          for (int j = 0; j < 32; ++j) po[(32 * ch + j) * HP + h] = __uint_as_float(v[j]) * inv;
         }
-        if (live) p.part_lse[half_id * H + h] = l > 0.f ? m_ref + __log2f(l) : -INFINITY;
-        __threadfence();
+        if (live) p.part_lse[half_id * HP + h] = l > 0.f ? m_ref + __log2f(l) : -INFINITY;
       }
-      // The last split to publish (per token and value half) merges them all, in split
-      // order and with the same arithmetic for its own part (from tensor memory) as for
-      // the others (streamed in by warp 0), so the result does not depend on which CTA
-      // finished last; it then resets the counter for the next call.  Both barriers are
-      // passed by warp 0 and warps 8-11 whatever happened before.
-      named_bar_sync(1, kMergeThreads);
-      if (warp == kFinWarp0 && lane == 0) {
-        const uint32_t prev = atomicAdd(p.merge_cnt + tok * 2 + c, 1u);
-        *last_s = prev == (uint32_t)(p.n_splits - 1);
-      }
-      named_bar_sync(1, kMergeThreads);
-      if (*last_s) {
-        __threadfence();
-        const int S = p.n_splits;
-        const int64_t base = (int64_t)tok * S * 2 + c;  // + 2 * s: split s of this half
-        const int hh = live ? h : 0;
-        // split weights 2^(lse_s - max) of this head, kept in the (now idle) exchange
-        // buffer; their sum in split order
-        float* wsm = (float*)xch + hh;
-        float mx = -INFINITY;
-        for (int s2 = 0; s2 < S; ++s2) mx = fmaxf(mx, __ldcg(p.part_lse + (base + 2 * s2) * H + hh));
-        float wsum = 0.f;
-        for (int s2 = 0; s2 < S; ++s2) {
-          const float w = mx != -INFINITY ? exp2f(__ldcg(p.part_lse + (base + 2 * s2) * H + hh) - mx) : 0.f;
-          wsm[s2 * kMaxSfaHeads] = w;
-          wsum += w;
-        }
-        const float winv = wsum > 0.f ? 1.f / wsum : 0.f;
-        const float* ring = (const float*)stages;
-        int q = 0;
-        bool good = ok;
-#pragma unroll 1
-        for (int k = 0; k < 256 / kMergeCols; ++k) {
-          float acc[kMergeCols];
-#pragma unroll
-          for (int j = 0; j < kMergeCols; ++j) acc[j] = 0.f;
-#pragma unroll 1
-          for (int s2 = 0; s2 < S && good; ++s2) {
-            const float w = wsm[s2 * kMaxSfaHeads];
-            if (s2 == split) {
-#pragma unroll
-              for (int u = 0; u < kMergeCols / 32; ++u) {
-                uint32_t v[32];
-                if (n_tiles_run > 0) {
-                  tmem_ld32(tmem + lane_off + kColO + kMergeCols * k + 32 * u, v);
-                  tmem_ld_wait();
-                } else {
-#pragma unroll
-                  for (int j = 0; j < 32; ++j) v[j] = 0u;
-                }
-#pragma unroll
-                for (int j = 0; j < 32; ++j) acc[32 * u + j] += w * (__uint_as_float(v[j]) * inv);
-              }
-            } else {
-              if (lane == 0) good = mbar_wait(&mfull[q & 3], (q >> 2) & 1, abort_flag, p.err);
-              good = __shfl_sync(0xffffffffu, good, 0);
-              __syncwarp();
-              if (good) {
-                const float* b = ring + (q & 3) * (kMergeBuf / 4) + hh;
-#pragma unroll
-                for (int j = 0; j < kMergeCols; ++j) acc[j] += w * b[j * H];
-              }
-              __syncwarp();
-              if (lane == 0) mbar_arrive(&mempty[q & 3]);
-              ++q;
-            }
-          }
-          if (good && live) {
-            uint4* dst = (uint4*)(p.out + ((int64_t)tok * H + h) * kValueDim + 256 * (int)c + kMergeCols * k);
-#pragma unroll
-            for (int j = 0; j < kMergeCols / 8; ++j) {
-              uint4 o;
-              o.x = pack_bf16x2(acc[8 * j] * winv, acc[8 * j + 1] * winv);
-              o.y = pack_bf16x2(acc[8 * j + 2] * winv, acc[8 * j + 3] * winv);
-              o.z = pack_bf16x2(acc[8 * j + 4] * winv, acc[8 * j + 5] * winv);
-              o.w = pack_bf16x2(acc[8 * j + 6] * winv, acc[8 * j + 7] * winv);
-              dst[j] = o;
-            }
-          }
-        }
-        if (warp == kFinWarp0 && lane == 0) p.merge_cnt[tok * 2 + c] = 0u;
-      }
+      // sfa_combine_kernel (the next launch) merges the splits of every (token, half)
     }
     }  // the first finishing warp of each row quarter
   }
@@ -994,7 +900,65 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// Merge of more than two splits: out[tok, h, 256 c + col] = sum_s w_s O_s / l_s with
+// w_s = 2^(lse_s - max) / sum 2^(lse - max), the splits taken in order (the result does
+// not depend on which CTA finished first).  One CTA of 128 threads per (token, value
+// half, 16-column chunk); thread t takes heads 4 (t % 32) .. + 3 and columns
+// 4 (t / 32) .. + 3 of the chunk: 16-byte loads over 4 heads (the partials are
+// column-major, their head stride H rounded up to a multiple of 4), all S x 4 of them in
+// flight together.
+constexpr int kCombineCols = 16;
+constexpr int kCombineThreads = 128;
+
+__global__ void __launch_bounds__(kCombineThreads) sfa_combine_kernel(SfaParams p) {
+  pdl_trigger();
+  pdl_wait();  // the partials of the attention kernel
+  constexpr int kChunks = 256 / kCombineCols;
+  const int tok = blockIdx.y, c = blockIdx.x / kChunks, k = blockIdx.x % kChunks;
+  const int H = p.n_heads, S = p.n_splits, HP = (H + 3) & ~3;  // partials' head stride
+  const int h0 = 4 * (threadIdx.x & 31), col0 = kCombineCols * k + 4 * (threadIdx.x >> 5);
+  if (h0 >= H) return;
+  const int64_t base = (int64_t)tok * S * 2 + c;  // + 2 s: split s of this half
+  float4 mx = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+  for (int s2 = 0; s2 < S; ++s2) {
+    const float4 l = *(const float4*)(p.part_lse + (base + 2 * s2) * HP + h0);
+    mx = make_float4(fmaxf(mx.x, l.x), fmaxf(mx.y, l.y), fmaxf(mx.z, l.z), fmaxf(mx.w, l.w));
+  }
+  float acc[4][4] = {};  // [column][head]
+  float wsum[4] = {0.f, 0.f, 0.f, 0.f};
+  auto wt = [](float l, float m) { return m != -INFINITY ? exp2f(l - m) : 0.f; };
+  for (int s2 = 0; s2 < S; ++s2) {
+    const float4 l = *(const float4*)(p.part_lse + (base + 2 * s2) * HP + h0);
+    const float w[4] = {wt(l.x, mx.x), wt(l.y, mx.y), wt(l.z, mx.z), wt(l.w, mx.w)};
+    const float* po = p.part_o + ((base + 2 * s2) * 256 + col0) * HP + h0;
+    float4 v[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) v[j] = *(const float4*)(po + j * HP);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      acc[j][0] += w[0] * v[j].x;
+      acc[j][1] += w[1] * v[j].y;
+      acc[j][2] += w[2] * v[j].z;
+      acc[j][3] += w[3] * v[j].w;
+    }
+#pragma unroll
+    for (int e = 0; e < 4; ++e) wsum[e] += w[e];
+  }
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    if (h0 + e >= H) break;  // heads past H in the last group of four (padding, never written)
+    const float winv = wsum[e] > 0.f ? 1.f / wsum[e] : 0.f;
+    uint2* dst = (uint2*)(p.out + ((int64_t)tok * H + h0 + e) * kValueDim + 256 * c + col0);
+    *dst = make_uint2(pack_bf16x2(acc[0][e] * winv, acc[1][e] * winv), pack_bf16x2(acc[2][e] * winv, acc[3][e] * winv));
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_sfa_combine(const SfaParams& p, cudaStream_t s) {
+  return launch_pdl(sfa_combine_kernel, dim3(2 * (256 / kCombineCols), p.tv.n_tokens), dim3(kCombineThreads), 0, s,
+                    p);
+}
 
 cudaError_t launch_sfa_tc(const SfaParams& p, cudaStream_t s) {
   // the latent cache as [pages * 64 rows, 576]: one-row boxes of 64 elements (latent

@@ -236,6 +236,15 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
       "l"(src), "r"(bytes), "r"(smem_u32(bar))
       : "memory");
 }
+// 16-byte copy global -> shared on the load/store path (not the TMA unit), cached in L2
+// only; cp_async_arrive_noinc(bar) then arrives on `bar` once every such copy this thread
+// issued so far has landed (the arrival counts against the barrier's expected count).
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];\n" ::"r"(smem_u32(bar)) : "memory");
+}
 // Orders this thread's earlier global-memory accesses (and what it has observed) before
 // its later async-proxy (bulk copy) accesses of global memory.
 __device__ __forceinline__ void fence_proxy_async_global() {
