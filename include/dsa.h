@@ -18,9 +18,10 @@
  * Conventions for every entry point:
  *   - Ownership: the caller allocates and owns every buffer, including the workspace.
  *     The library allocates no memory, keeps no state between calls (apart from
- *     per-device caches of the SM count and of the fixed scratch's address, and the
- *     fixed scratch of dsa_indexer_topk_noalloc itself: see that entry point) and may be
- *     called concurrently on different streams with different workspaces.
+ *     per-device caches of the SM count and of the fixed scratch's address, the fixed
+ *     scratch of dsa_indexer_topk_noalloc itself, and the test hook
+ *     dsa_set_indexer_wait_limit: see those entry points) and may be called concurrently
+ *     on different streams with different workspaces.
  *   - Workspace sizes depend on the arguments and on the current device (the attention
  *     splits its work by the device's SM count): size a workspace with the current
  *     device set to the one it will be used on.
@@ -322,6 +323,19 @@ dsa_status_t dsa_index_cache_append(const void* k_new, const dsa_index_cache_t* 
 dsa_status_t dsa_latent_cache_append(const void* rows_new, const dsa_latent_cache_t* cache,
                                      const dsa_page_table_t* pages, const dsa_tokens_t* tokens,
                                      void* ws, size_t ws_bytes, dsa_stream_t stream);
+
+/* ---- Test hook: the indexer's pipeline wait limit ------------------------------- */
+/* Every wait inside the indexer's tensor-core kernels (a TMA load landing, an MMA
+ * completing, an epilogue freeing an accumulator) gives up after a limit -- about 2 s of
+ * SM clock cycles by default -- and then sets DSA_DEVERR_TIMEOUT in the workspace's error
+ * word, lets its in-flight copies and MMAs finish, frees its tensor memory and returns,
+ * so a lost arrival never hangs the device.  This sets that limit, process-wide, for the
+ * indexer calls launched afterwards (cycles > 0), or restores the default (0); a test
+ * lowers it to a few hundred cycles to make ordinary waits run out.  The attention
+ * kernel keeps its fixed limit (its CTA pairs exchange data through distributed shared
+ * memory, and a CTA must not exit while its peer's copies into it are in flight).
+ * Returns DSA_ERR_INVALID_ARG for cycles < 0. */
+dsa_status_t dsa_set_indexer_wait_limit(int64_t cycles);
 
 /* ---- Errors and introspection --------------------------------------------------- */
 /* Copies the device error word out of ws (synchronises `stream`) into *err. */

@@ -92,6 +92,8 @@ def _load() -> C.CDLL:
     lib.dsa_index_cache_append.restype = C.c_int
     lib.dsa_latent_cache_append.argtypes = [_vp, P(LatentCache), P(PageTable), P(Tokens), _vp, C.c_size_t, _vp]
     lib.dsa_latent_cache_append.restype = C.c_int
+    lib.dsa_set_indexer_wait_limit.argtypes = [C.c_int64]
+    lib.dsa_set_indexer_wait_limit.restype = C.c_int
     lib.dsa_read_device_error.argtypes = [_vp, P(C.c_uint32), _vp]
     lib.dsa_read_device_error.restype = C.c_int
     lib.dsa_clear_device_error.argtypes = [_vp, _vp]

@@ -15,6 +15,10 @@ namespace {
 
 thread_local std::string g_last_error;
 
+// Pipeline wait limit of the indexer's tensor-core kernels (cycles; 0: the default, about
+// 2 s).  Lowered only by tests, through dsa_set_indexer_wait_limit.
+std::atomic<long long> g_indexer_wait_limit{0};
+
 dsa_status_t fail(dsa_status_t st, const char* fmt, ...) {
   char buf[512];
   va_list ap;
@@ -316,6 +320,10 @@ dsa_status_t run_indexer(const dsa_indexer_args_t* a, const dsa_index_cache_t* c
   sp.act = (int)a->act;
   sp.max_page_blocks = (ip.max_visible + kPage - 1) / kPage;
   sp.q_dep = 0;
+  {
+    const long long wl = g_indexer_wait_limit.load(std::memory_order_relaxed);
+    sp.wait_limit = wl > 0 ? wl : sm100_default_wait_limit();
+  }
   tr.begin();
   cudaError_t me = launch_clear(clear, clear_bytes, s);
   tr.end("hist_clear");
@@ -649,6 +657,12 @@ dsa_status_t dsa_latent_cache_append(const void* rows_new, const dsa_latent_cach
   p.err = (uint32_t*)ws;
   cudaError_t e = launch_latent_append(p, fp8, (cudaStream_t)stream);
   if (e != cudaSuccess) return cuda_fail(e, "latent append launch");
+  return DSA_OK;
+}
+
+dsa_status_t dsa_set_indexer_wait_limit(int64_t cycles) {
+  if (cycles < 0) return fail(DSA_ERR_INVALID_ARG, "cycles must be >= 0 (0 restores the default)");
+  g_indexer_wait_limit.store(cycles, std::memory_order_relaxed);
   return DSA_OK;
 }
 

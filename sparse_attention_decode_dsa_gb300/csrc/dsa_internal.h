@@ -22,6 +22,8 @@ constexpr int kMaxDevices = 128;             // device ordinals the per-device c
 // Streaming multiprocessors of the current device (looked up once per device).  Launch
 // plans, and so the attention's workspace size, depend on it.
 int device_sm_count();
+// The pipeline wait limit the tensor-core kernels use by default (cycles, about 2 s).
+long long sm100_default_wait_limit();
 
 // Fixed scratch of dsa_indexer_topk_noalloc (noalloc.cu): its size, and its device
 // address on the current device, looked up once per device.  *ptr stays null (with
@@ -56,6 +58,8 @@ struct ScoreParams {
   const float* qt;         // q~ [T, dim] f32 (the folded-query kernel only)
   int32_t seg_rows;        // row-blocked kernel: rows per segment (consecutive rows of one
                            // sequence; n_tokens is a multiple of it)
+  int64_t wait_limit;      // tensor-core kernel: cycles a pipeline wait may take before it
+                           // gives up (DSA_DEVERR_TIMEOUT); the default unless a test lowers it
 };
 
 struct TopkParams {

@@ -211,6 +211,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       int stage = 0;
       uint32_t phase = 0;
       uint32_t armed = 0, armed_parity = 0;  // stages with a load issued, and its phase parity
+      uint32_t qarmed = 0, qparity = 0;      // the same for the two query slots
       int r = 0, cur_row = -1, qcount = 0;
       for (int it = it_begin; it < it_end; ++it) {
         while (prefix[r + 1] <= it) ++r;
@@ -219,15 +220,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           int ur0 = r, unb = 1;
           if (BLK) block_unit(a, r, &ur0, &unb);
           const int slot = qcount & 1;
-          if (!mbar_wait(&q_empty[slot], ((qcount >> 1) & 1) ^ 1, abort_flag, p.err)) break;
+          if (!mbar_wait(&q_empty[slot], ((qcount >> 1) & 1) ^ 1, abort_flag, p.err, p.wait_limit)) break;
           mbar_arrive_expect_tx(&q_full[slot], C::kRegions * H * 128);
+          qarmed |= 1u << slot;
+          qparity = (qparity & ~(1u << slot)) | ((uint32_t)((qcount >> 1) & 1) << slot);
           const uint32_t qdst = smem_u32(qslots + slot * C::kQSlotBytes);
           for (int g = 0; g < C::kRegions; ++g)
             tma_load_2d(qdst + g * C::kRegionQBytes, &qmap, &q_full[slot], g * C::kBoxInner,
                         BLK ? 3 * (a.row0 + ur0) : (a.row0 + r) * H);
           ++qcount;
         }
-        if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.err)) break;
+        if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.err, p.wait_limit)) break;
         const int tile = it - prefix[r];
         int br = r;
         if (BLK) {
@@ -261,11 +264,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
       }
       if (*abort_flag) {
-        // let every copy still in flight land before the shared memory is released
+        // let every copy still in flight (key tiles and queries) land before the shared
+        // memory is released
         for (int st = 0; st < C::kStages; ++st) {
           if (!(armed >> st & 1)) continue;
           const long long t0 = clock64();
           while (!mbar_try_wait(smem_u32(&full[st]), (armed_parity >> st) & 1) && clock64() - t0 < kWaitLimitCycles) {
+          }
+        }
+        for (int sl = 0; sl < 2; ++sl) {
+          if (!(qarmed >> sl & 1)) continue;
+          const long long t0 = clock64();
+          while (!mbar_try_wait(smem_u32(&q_full[sl]), (qparity >> sl) & 1) && clock64() - t0 < kWaitLimitCycles) {
           }
         }
       }
@@ -282,11 +292,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (r != cur_row) {
           cur_row = r;
           slot = qcount & 1;
-          if (!mbar_wait(&q_full[slot], (qcount >> 1) & 1, abort_flag, p.err)) break;
+          if (!mbar_wait(&q_full[slot], (qcount >> 1) & 1, abort_flag, p.err, p.wait_limit)) break;
           ++qcount;
         }
-        if (!mbar_wait(&full[stage], phase, abort_flag, p.err)) break;
-        if (!mbar_wait(&acc_empty[acc], acc_phase ^ 1, abort_flag, p.err)) break;
+        if (!mbar_wait(&full[stage], phase, abort_flag, p.err, p.wait_limit)) break;
+        if (!mbar_wait(&acc_empty[acc], acc_phase ^ 1, abort_flag, p.err, p.wait_limit)) break;
         tc_fence_after();
         const uint32_t a0 = smem_u32(stages + stage * C::kStageBytes);
         const uint32_t b0 = smem_u32(qslots + slot * C::kQSlotBytes);
@@ -348,7 +358,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const int pg = t < rown[r] ? physical_page(p.tv, rowb[r0], t >> 6, nullptr) : -1;
         const float ksc = (p.k_scale && pg >= 0) ? ((const float*)p.k_scale)[(int64_t)pg * kPage + (t & 63)] : 1.f;
         bool ok = true;
-        if (lane == 0) ok = mbar_wait(&acc_full[acc], acc_phase, abort_flag, p.err);
+        if (lane == 0) ok = mbar_wait(&acc_full[acc], acc_phase, abort_flag, p.err, p.wait_limit);
         if (!__shfl_sync(0xffffffffu, ok, 0)) break;
         __syncwarp();
         tc_fence_after();
@@ -407,7 +417,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           }
         }
         bool ok = true;
-        if (lane == 0) ok = mbar_wait(&full[stage], par, abort_flag, p.err);
+        if (lane == 0) ok = mbar_wait(&full[stage], par, abort_flag, p.err, p.wait_limit);
         if (!__shfl_sync(0xffffffffu, ok, 0)) break;
         __syncwarp();
         const uint8_t* krow_s = stages + stage * C::kStageBytes + i * 128;
@@ -484,7 +494,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
       }
       bool ok = true;
-      if (lane == 0) ok = mbar_wait(&acc_full[acc], acc_phase, abort_flag, p.err);
+      if (lane == 0) ok = mbar_wait(&acc_full[acc], acc_phase, abort_flag, p.err, p.wait_limit);
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
       __syncwarp();
@@ -592,6 +602,8 @@ cudaError_t launch_tc(const ScoreParams& p, cudaStream_t s) {
 }
 
 }  // namespace
+
+long long sm100_default_wait_limit() { return kWaitLimitCycles; }
 
 bool score_tc_supported(dsa_dtype_t dt, int dim, int n_heads) {
   if (n_heads < 1 || n_heads > 64) return false;

@@ -333,6 +333,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t doff = q < 4 ? q * kRegion + g * 512 : 4 * kRegion + g * 256;
       const CUtensorMap* map = q < 4 ? &kvmap : &ropemap;
       const uint32_t my_bytes = __reduce_add_sync(0xffffffffu, mine ? (q < 4 ? 512u : 256u) : 0u);
+      uint32_t armed = 0, armed_parity = 0;  // stages with gathers issued, and their phase parity
       for (int n = 0; n < n_tiles_run; ++n) {
         const int stage = n % kStages;
         bool good = true;
@@ -344,12 +345,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (!__shfl_sync(0xffffffffu, good, 0)) break;
         __syncwarp();
+        armed |= 1u << stage;
+        armed_parity = (armed_parity & ~(1u << stage)) | ((uint32_t)((n / kStages) & 1) << stage);
         if (mine) {
           const int4 v = *(const int4*)(rowid + n * kTok + 4 * g);
           tma_gather4(smem_u32(stages + stage * kStageBytes) + doff, map, &kv_full[stage], x,
                       v.x >= 0 ? v.x : fill, v.y >= 0 ? v.y : fill, v.z >= 0 ? v.z : fill, v.w >= 0 ? v.w : fill);
         }
       }
+      // after an abort, let the gathers still in flight land before the CTA moves on (a
+      // phase another warp never armed completes no more: the wait then ends at its limit)
+      if (*abort_flag && lane == 0) {
+        for (int st = 0; st < kStages; ++st) {
+          if (!(armed >> st & 1)) continue;
+          const long long t0 = clock64();
+          while (!mbar_try_wait(smem_u32(&kv_full[st]), (armed_parity >> st) & 1) && clock64() - t0 < kWaitLimitCycles) {
+          }
+        }
+      }
+      __syncwarp();
     } else if (warp < kGatherWarps) {
       // FP8, issuers (warps 0-2, blocking waits): lane l of warp w takes item i = 3 l + w:
       // gather i (i < 48: pieces q = i % 3 of group i / 3), else the scale copies of rows

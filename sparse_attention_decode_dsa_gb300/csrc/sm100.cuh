@@ -50,17 +50,20 @@ __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
 }
 
 // Waits for the phase with the given parity to complete.  Returns false (after
-// setting the error bit and the abort flag) if it does not within the limit, or if
-// another role of the CTA already aborted.
+// setting the error bit and the abort flag) if it does not within `limit` cycles, or if
+// another role of the CTA already aborted.  A limit below the default is a test
+// setting: the wait then probes without suspending (try_wait may suspend the thread for
+// longer than such a limit), so that it reliably runs out.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                          uint32_t* err) {
+                                          uint32_t* err, long long limit = kWaitLimitCycles) {
   const uint32_t a = smem_u32(bar);
-  if (mbar_try_wait(a, parity)) return true;
+  const bool probe = limit < kWaitLimitCycles;
+  if (probe ? mbar_test(a, parity) : mbar_try_wait(a, parity)) return true;
   const long long t0 = clock64();
   while (true) {
-    if (mbar_try_wait(a, parity)) return true;
+    if (probe ? mbar_test(a, parity) : mbar_try_wait(a, parity)) return true;
     if (*abort_flag) return false;
-    if (clock64() - t0 > kWaitLimitCycles) {
+    if (clock64() - t0 > limit) {
       atomicOr(err, DSA_DEVERR_TIMEOUT);
       *abort_flag = 1;
       return false;

@@ -273,3 +273,28 @@ def test_topk_boundary_bin_near_pool_capacity(dsa):
     wl.idx_q[...] = 0
     wl.idx_q[:, 0, 0] = 0x3F80                     # bf16 1.0 in head 0, dim 0
     _indexer_vs_oracle(dsa, wl, "17 values")
+
+
+def test_indexer_wait_timeout_unwinds_and_the_context_stays_usable(dsa):
+    """Every pipeline wait of the indexer's tensor-core kernels is bounded.  With the
+    limit lowered to 300 cycles the ordinary waits (a TMA load landing, an MMA completing,
+    an accumulator freed) run out: each call must return with DSA_DEVERR_TIMEOUT in the
+    error word, and -- the kernels having let their in-flight copies and MMAs finish and
+    freed their tensor memory -- full parity checks on the same context afterwards must be
+    green.  Covers the per-head, row-blocked, folded FP8 and MX paths."""
+    specs = [W.SMALL_DECODE_BF16, W.SMALL_PREFILL, W.SMALL_DECODE_FP8, W.SMALL_DECODE_MX]
+    assert dsa.lib.dsa_set_indexer_wait_limit(-1) == dsa.DSA_ERR_INVALID_ARG
+    assert dsa.lib.dsa_set_indexer_wait_limit(300) == dsa.DSA_OK
+    try:
+        for spec in specs:
+            wl = W.make(spec, with_latent=False)
+            plan = dsa.Plan(_device(wl))
+            out_idx = torch.empty((wl.n_tokens, spec.topk), dtype=torch.int32, device="cuda")
+            ws = dsa.alloc_workspace(plan.ws_indexer(), poison=True)
+            dsa.indexer_topk(plan, out_idx, ws)
+            torch.cuda.synchronize()
+            assert dsa.read_device_error(ws) & dsa.DSA_DEVERR_TIMEOUT, f"{spec.name}: no wait ran out"
+    finally:
+        assert dsa.lib.dsa_set_indexer_wait_limit(0) == dsa.DSA_OK
+    for spec in specs:
+        _check_config(dsa, spec)
