@@ -468,9 +468,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         for (int h = lane; h < H; h += 32) {
           w_s[h] = p.head_w[(int64_t)grow * H + h];
           if (KIND == 2) {
+            // identity: the head weight joins the query's group scale (a power of two,
+            // so the product is exact)
+            const float wq = p.act == DSA_ACT_IDENTITY ? w_s[h] : 1.f;
             const uint32_t q4 = *(const uint32_t*)((const uint8_t*)p.q_scale + ((int64_t)grow * H + h) * 4);
 #pragma unroll
-            for (int g = 0; g < 4; ++g) qs_s[h * 4 + g] = e8m0_to_f32((q4 >> (8 * g)) & 0xFF);
+            for (int g = 0; g < 4; ++g) qs_s[h * 4 + g] = wq * e8m0_to_f32((q4 >> (8 * g)) & 0xFF);
           }
         }
         qtok = (KIND == 1) ? ((const float*)p.q_scale)[grow] : 1.f;
@@ -527,6 +530,30 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             }
           }
         }
+      } else if (p.act == DSA_ACT_IDENTITY) {
+        // sum_h w_h sum_g (ks_g qs_hg acc_gh) regrouped as sum_g ks_g sum_h (w_h qs_hg) acc_gh:
+        // one FMA per (group, head) and four multiplies per key (exact, like any order)
+#pragma unroll 1
+        for (int hc = 0; hc < 2; ++hc) {
+          if (hc * 32 >= H) break;
+          uint32_t v[C::kGroups][32];
+#pragma unroll
+          for (int g = 0; g < C::kGroups; ++g) tmem_ld32(tbase + g * 64 + hc * 32, v[g]);
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const int h = hc * 32 + j;
+            if (h < H) {
+              const float4 c = *(const float4*)(qs_s + h * 4);
+              part[0] = fmaf(__uint_as_float(v[0][j]), c.x, part[0]);
+              part[1] = fmaf(__uint_as_float(v[1][j]), c.y, part[1]);
+              part[2] = fmaf(__uint_as_float(v[2][j]), c.z, part[2]);
+              part[3] = fmaf(__uint_as_float(v[3][j]), c.w, part[3]);
+            }
+          }
+        }
+#pragma unroll
+        for (int g = 0; g < C::kGroups; ++g) part[g] *= ks[g];
       } else {
 #pragma unroll 1
         for (int hc = 0; hc < 2; ++hc) {

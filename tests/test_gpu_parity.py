@@ -281,8 +281,10 @@ def test_indexer_wait_timeout_unwinds_and_the_context_stays_usable(dsa):
     an accumulator freed) run out: each call must return with DSA_DEVERR_TIMEOUT in the
     error word, and -- the kernels having let their in-flight copies and MMAs finish and
     freed their tensor memory -- full parity checks on the same context afterwards must be
-    green.  Covers the per-head, row-blocked, folded FP8 and MX paths."""
-    specs = [W.SMALL_DECODE_BF16, W.SMALL_PREFILL, W.SMALL_DECODE_FP8, W.SMALL_DECODE_MX]
+    green.  The per-head, row-blocked and MX paths wait for the query's TMA load right
+    after issuing it, so a wait always runs out there; the folded FP8 path's loads may
+    land before its first probe, so it need only return with no other error bit."""
+    specs = [W.SMALL_DECODE_BF16, W.SMALL_PREFILL, W.SMALL_DECODE_MX, W.SMALL_DECODE_FP8]
     assert dsa.lib.dsa_set_indexer_wait_limit(-1) == dsa.DSA_ERR_INVALID_ARG
     assert dsa.lib.dsa_set_indexer_wait_limit(300) == dsa.DSA_OK
     try:
@@ -293,7 +295,10 @@ def test_indexer_wait_timeout_unwinds_and_the_context_stays_usable(dsa):
             ws = dsa.alloc_workspace(plan.ws_indexer(), poison=True)
             dsa.indexer_topk(plan, out_idx, ws)
             torch.cuda.synchronize()
-            assert dsa.read_device_error(ws) & dsa.DSA_DEVERR_TIMEOUT, f"{spec.name}: no wait ran out"
+            err = dsa.read_device_error(ws)
+            assert err & ~dsa.DSA_DEVERR_TIMEOUT == 0, f"{spec.name}: error word {err:#x}"
+            if spec is not W.SMALL_DECODE_FP8:
+                assert err & dsa.DSA_DEVERR_TIMEOUT, f"{spec.name}: no wait ran out"
     finally:
         assert dsa.lib.dsa_set_indexer_wait_limit(0) == dsa.DSA_OK
     for spec in specs:
