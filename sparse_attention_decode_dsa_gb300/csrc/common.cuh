@@ -59,11 +59,11 @@ __device__ __forceinline__ float e4m3_to_f32(uint8_t v) {
   return __half2float(__half(hr));
 }
 
-// E8M0 exponent byte -> 2^(e-127) as f32 (e = 0 gives the subnormal 2^-127).
+// E8M0 exponent byte -> 2^(e-127) as f32 (e = 0 gives the subnormal 2^-127, 0xFF NaN).
+// Branch-free (selects), so that loops over loaded bytes keep their loads in flight.
 __device__ __forceinline__ float e8m0_to_f32(uint8_t e) {
-  if (e == 0xFF) return __uint_as_float(0x7FC00000u);
-  if (e == 0) return __uint_as_float(0x00400000u);
-  return __uint_as_float((uint32_t)e << 23);
+  const uint32_t u = e == 0 ? 0x00400000u : (e == 0xFF ? 0x7FC00000u : (uint32_t)e << 23);
+  return __uint_as_float(u);
 }
 
 // f32 -> bf16 bits, round to nearest even (NaN kept quiet).

@@ -76,20 +76,23 @@ __global__ void __launch_bounds__(kSplitThreads) qsplit_kernel(ScoreParams p, ui
   for (int e = threadIdx.x; e < 4 * D; e += kSplitThreads) {
     const int j = e / D, d = e % D;
     float acc = 0.f;
-    float q[16], w[16];
+    uint32_t qb[16], sb[16];
+    float w[16];
 #pragma unroll
-    for (int u = 0; u < 16; ++u) {
-      const int h = 16 * j + u;
-      const int64_t off = ((int64_t)row * H + (h < H ? h : 0)) * D + d;
-      q[u] = h >= H ? 0.f
-             : KIND == 0 ? bf16_to_f32(__ldg((const uint16_t*)p.q + off))
-                         : e4m3_to_f32(__ldg((const uint8_t*)p.q + off));
-      w[u] = h < H ? __ldg(p.head_w + (int64_t)row * H + h) : 0.f;
-      if (KIND == 2 && h < H)
-        w[u] *= e8m0_to_f32(__ldg((const uint8_t*)p.q_scale + ((int64_t)row * H + h) * (D / 32) + d / 32));
+    for (int u = 0; u < 16; ++u) {  // every load of the 16 heads first, then the arithmetic
+      const int h = min(16 * j + u, H - 1);
+      const int64_t off = ((int64_t)row * H + h) * D + d;
+      qb[u] = KIND == 0 ? __ldg((const uint16_t*)p.q + off) : __ldg((const uint8_t*)p.q + off);
+      w[u] = __ldg(p.head_w + (int64_t)row * H + h);
+      sb[u] = KIND == 2 ? __ldg((const uint8_t*)p.q_scale + ((int64_t)row * H + h) * (D / 32) + d / 32) : 0u;
     }
 #pragma unroll
-    for (int u = 0; u < 16; ++u) acc = fmaf(w[u], q[u], acc);
+    for (int u = 0; u < 16; ++u) {
+      const bool live = 16 * j + u < H;
+      const float q = KIND == 0 ? bf16_to_f32((uint16_t)qb[u]) : e4m3_to_f32((uint8_t)qb[u]);
+      const float wu = KIND == 2 ? w[u] * e8m0_to_f32((uint8_t)sb[u]) : w[u];
+      acc = fmaf(live ? wu : 0.f, q, acc);
+    }
     part[j][d] = acc;
   }
   __syncthreads();

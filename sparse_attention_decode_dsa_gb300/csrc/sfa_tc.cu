@@ -923,6 +923,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 // flight together.
 constexpr int kCombineCols = 16;
 constexpr int kCombineThreads = 128;
+constexpr int kMaxCombineSplits = 16;  // (the planner makes at most 16 splits)
 
 __global__ void __launch_bounds__(kCombineThreads) sfa_combine_kernel(SfaParams p) {
   pdl_trigger();
@@ -933,30 +934,46 @@ __global__ void __launch_bounds__(kCombineThreads) sfa_combine_kernel(SfaParams 
   const int h0 = 4 * (threadIdx.x & 31), col0 = kCombineCols * k + 4 * (threadIdx.x >> 5);
   if (h0 >= H) return;
   const int64_t base = (int64_t)tok * S * 2 + c;  // + 2 s: split s of this half
+  float4 lse[kMaxCombineSplits];
+#pragma unroll
+  for (int s2 = 0; s2 < kMaxCombineSplits; ++s2)
+    if (s2 < S) lse[s2] = *(const float4*)(p.part_lse + (base + 2 * s2) * HP + h0);
   float4 mx = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
-  for (int s2 = 0; s2 < S; ++s2) {
-    const float4 l = *(const float4*)(p.part_lse + (base + 2 * s2) * HP + h0);
-    mx = make_float4(fmaxf(mx.x, l.x), fmaxf(mx.y, l.y), fmaxf(mx.z, l.z), fmaxf(mx.w, l.w));
-  }
+#pragma unroll
+  for (int s2 = 0; s2 < kMaxCombineSplits; ++s2)
+    if (s2 < S)
+      mx = make_float4(fmaxf(mx.x, lse[s2].x), fmaxf(mx.y, lse[s2].y), fmaxf(mx.z, lse[s2].z), fmaxf(mx.w, lse[s2].w));
   float acc[4][4] = {};  // [column][head]
   float wsum[4] = {0.f, 0.f, 0.f, 0.f};
   auto wt = [](float l, float m) { return m != -INFINITY ? exp2f(l - m) : 0.f; };
-  for (int s2 = 0; s2 < S; ++s2) {
-    const float4 l = *(const float4*)(p.part_lse + (base + 2 * s2) * HP + h0);
-    const float w[4] = {wt(l.x, mx.x), wt(l.y, mx.y), wt(l.z, mx.z), wt(l.w, mx.w)};
-    const float* po = p.part_o + ((base + 2 * s2) * 256 + col0) * HP + h0;
-    float4 v[4];
+  // splits in groups of four: the group's 16 loads are in flight together
+#pragma unroll 1
+  for (int s0 = 0; s0 < S; s0 += 4) {
+    float4 v[4][4];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) v[j] = *(const float4*)(po + j * HP);
+    for (int u = 0; u < 4; ++u) {
+      const float* po = p.part_o + ((base + 2 * min(s0 + u, S - 1)) * 256 + col0) * HP + h0;
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      acc[j][0] += w[0] * v[j].x;
-      acc[j][1] += w[1] * v[j].y;
-      acc[j][2] += w[2] * v[j].z;
-      acc[j][3] += w[3] * v[j].w;
+      for (int j = 0; j < 4; ++j) v[u][j] = *(const float4*)(po + j * HP);
     }
 #pragma unroll
-    for (int e = 0; e < 4; ++e) wsum[e] += w[e];
+    for (int u = 0; u < 4; ++u) {
+      if (s0 + u >= S) break;
+      float4 l = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int s2 = 0; s2 < kMaxCombineSplits; ++s2)
+        if (s2 == s0 + u) l = lse[s2];
+      const float w[4] = {wt(l.x, mx.x), wt(l.y, mx.y), wt(l.z, mx.z), wt(l.w, mx.w)};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        acc[j][0] += w[0] * v[u][j].x;
+        acc[j][1] += w[1] * v[u][j].y;
+        acc[j][2] += w[2] * v[u][j].z;
+        acc[j][3] += w[3] * v[u][j].w;
+      }
+#pragma unroll
+      for (int e = 0; e < 4; ++e) wsum[e] += w[e];
+    }
   }
 #pragma unroll
   for (int e = 0; e < 4; ++e) {
