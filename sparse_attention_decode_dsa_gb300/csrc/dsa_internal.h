@@ -4,6 +4,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "../../include/dsa.h"
 
 namespace dsa {
@@ -101,6 +103,20 @@ bool make_tma_2d_sw128(CUtensorMap* m, const void* base, uint64_t rows, int elem
 // promotion); one-row boxes serve to gather 64-byte pieces of scattered rows.
 bool make_tma_2d_sw64_rows(CUtensorMap* m, const void* base, uint64_t rows, int elem, int row_elems,
                            int box_rows = 1);
+
+// cudaFuncSetAttribute(MaxDynamicSharedMemorySize) once per device and kernel (the
+// attribute persists for the context; setting it on every launch costs host time on the
+// launch path).  `done` is the kernel's own per-device flag array.
+template <typename F>
+cudaError_t set_smem_once(F* kernel, int bytes, std::atomic<int> (&done)[kMaxDevices]) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= 0 && dev < kMaxDevices && done[dev].load(std::memory_order_acquire) == bytes) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && dev >= 0 && dev < kMaxDevices) done[dev].store(bytes, std::memory_order_release);
+  return e;
+}
 
 // Launch with programmatic stream serialization: the kernel may start while the previous
 // kernel in the stream is finishing; it calls pdl_wait() before touching what that

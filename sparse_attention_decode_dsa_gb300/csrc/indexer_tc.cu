@@ -603,8 +603,8 @@ cudaError_t launch_tc(const ScoreParams& p, cudaStream_t s) {
   static_assert(C::kSmem <= 232448, "shared memory budget");
   CUtensorMap kmap, qmap;
   if (!make_tma_2d_sw128(&kmap, p.k, (uint64_t)p.tv.num_pages * kPage, C::kElem, D, kPage)) return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(score_tc_kernel<KIND, D, BLK, FOLD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       C::kSmem);
+  static std::atomic<int> smem_set[kMaxDevices];
+  cudaError_t e = set_smem_once(score_tc_kernel<KIND, D, BLK, FOLD>, C::kSmem, smem_set);
   if (e != cudaSuccess) return e;
   const int sms = device_sm_count();
   // the query: [tokens * heads, D], boxes of one token's heads; blocked: [tokens * 3, D],

@@ -1011,7 +1011,8 @@ cudaError_t launch_sfa_tc(const SfaParams& p, cudaStream_t s) {
     return cudaErrorInvalidValue;
   auto kernel = fp8 ? sfa_tc_kernel<true> : sfa_tc_kernel<false>;
   const int smem = fp8 ? kSmemFp8 : kSmem;
-  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  static std::atomic<int> smem_set[2][kMaxDevices];
+  cudaError_t e = set_smem_once(kernel, smem, smem_set[fp8 ? 1 : 0]);
   if (e != cudaSuccess) return e;
   dim3 grid(2 * p.n_splits, p.tv.n_tokens);
   return launch_pdl_cluster(kernel, grid, dim3(kThreads), smem, s, p.sib_merge ? 4u : 2u, kvmap, ropemap, qmap,
