@@ -55,7 +55,7 @@ def _visible(wl):
     return np.minimum(wl.q_pos.astype(np.int64) + 1, lens[wl.q_seq]).clip(min=0)
 
 
-def algorithmic(wl):
+def algorithmic(wl, act="identity"):
     s = wl.spec
     vis = _visible(wl)
     T = wl.n_tokens
@@ -85,7 +85,7 @@ def algorithmic(wl):
     # (21 rows x 3 split terms), K = d MMA.  Its executed tensor work, not the per-head
     # definition's, is what its tensor fraction is measured on.
     blk_flops = 0.0
-    if s.mode in ("prefill", "multi") and s.idx_heads and T >= 2:
+    if s.mode in ("prefill", "multi") and s.idx_heads and T >= 2 and act == "identity":
         seg = T if s.mode == "prefill" else s.tokens_per_seq
         for s0 in range(0, T, seg):
             for r0 in range(s0, s0 + seg, 21):
@@ -255,12 +255,42 @@ def run_prolog(args):
     torch.cuda.synchronize()
     a_us = b.elapsed_time(e) * 1e3 / args.steps
     assert dsa.read_device_error(ws) == 0
+
+    def time_calls(fn):
+        for _ in range(max(3, args.warmup)):
+            fn()
+        torch.cuda.synchronize()
+        b.record(stream)
+        for _ in range(args.steps):
+            fn()
+        e.record(stream)
+        torch.cuda.synchronize()
+        assert dsa.read_device_error(ws) == 0
+        return b.elapsed_time(e) * 1e3 / args.steps
+
+    # the other appends of one decode step (32 new tokens): K-index rows bf16 and e4m3 +
+    # per-token scale, latent rows bf16 and FP8 (tiles of 128)
+    kb = torch.zeros(pool, 64, dim, dtype=torch.bfloat16, device=dev)
+    kf = torch.zeros(pool, 64, dim, dtype=torch.uint8, device=dev)
+    kfs = torch.zeros(pool, 64, dtype=torch.float32, device=dev)
+    lat_new = torch.randn(B, 576, device=dev).to(torch.bfloat16)
+    lb = torch.zeros(pool, 64, 576, dtype=torch.bfloat16, device=dev)
+    lc = torch.zeros(pool, 64, 512, dtype=torch.uint8, device=dev)
+    lsc = torch.zeros(pool, 64, 4, dtype=torch.float32, device=dev)
+    lr = torch.zeros(pool, 64, 64, dtype=torch.bfloat16, device=dev)
+    appends = {
+        "index_bf16_us": time_calls(lambda: dsa.index_cache_append(k_new, kb, None, bt, lens, lens_h, ws)),
+        "index_fp8_per_token_us": time_calls(lambda: dsa.index_cache_append(k_new, kf, kfs, bt, lens, lens_h, ws)),
+        "latent_bf16_us": time_calls(lambda: dsa.latent_cache_append(lat_new, lb, bt, lens, lens_h, ws)),
+        "latent_fp8_us": time_calls(lambda: dsa.latent_cache_append(lat_new, lc, bt, lens, lens_h, ws, cache_scale=lsc,
+                                                                    cache_rope=lr)),
+    }
     peak, _, _, peak_src = _peaks()
     achieved = q_bytes / (q_us * 1e-6) / 1e9
     print(json.dumps({
         "metric": "index prolog: MXFP8 quantisation GB/s (8192 x 64 x 128 bf16 rows)", "value": achieved,
         "unit": "GB/s", "higher_is_better": True, "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
-        "quantize_us": q_us, "append_32_keys_us": a_us, "dtype": "bf16 -> e4m3 + E8M0",
+        "quantize_us": q_us, "append_32_keys_us": a_us, "appends_32_tokens": appends, "dtype": "bf16 -> e4m3 + E8M0",
         "roofline": {"kernel": "mxfp8_quant", "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "algorithmic_bytes": q_bytes,
                      "peak_source": "measured (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured" else "fallback"},
@@ -279,6 +309,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="bf16_decode", choices=sorted(W.ALL))
     ap.add_argument("--batch", type=int, default=0, help="override the batch (smaller capture cases)")
+    ap.add_argument("--act", default="identity", choices=["identity", "relu"],
+                    help="per-head activation of the indexer (relu: the per-head path in every mode)")
     ap.add_argument("--e2e-steps", type=int, default=0)
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -324,13 +356,16 @@ def main():
 
     wl = W.make(spec)
     d = to_device(wl, dev)
+    if args.act == "relu":
+        d.act = dsa.DSA_ACT_RELU
+        config["act"] = "relu"
     plan = dsa.Plan(d)
     T, K, H = wl.n_tokens, spec.topk, spec.sfa_heads
     out_idx = torch.empty((T, K), dtype=torch.int32, device=dev)
     out = torch.empty((T, H, 512), dtype=torch.bfloat16, device=dev)
     ws = dsa.alloc_workspace(plan.ws_fused(), dev)
     stream = torch.cuda.current_stream(dev)
-    work = algorithmic(wl)
+    work = algorithmic(wl, args.act)
     l2_bytes = torch.cuda.get_device_properties(dev).L2_cache_size
     input_bytes = sum(int(t.numel() * t.element_size()) for t in
                       [d.idx_k, d.kv, d.kv_codes, d.kv_scale, d.kv_rope, d.idx_q, d.sfa_q, d.head_w, d.block_table]
@@ -433,7 +468,8 @@ def main():
         a_s = st["avg_us"] * 1e-6
         r = {"algorithmic_bytes": wk["bytes"], "achieved_gbs": wk["bytes"] / a_s / 1e9,
              "frac_hbm": wk["bytes"] / a_s / 1e9 / hbm_gbs}
-        fl = wk.get("executed_flops") or (wk["flops"] if k == "sfa" else 0.0)
+        fl = wk.get("executed_flops") or (wk["flops"] if k == "sfa" or (k == "indexer_score" and spec.mode == "prefill")
+                                          else 0.0)
         if fl:
             r["tensor_tflops"] = fl / a_s / 1e12
             r["frac_tensor"] = fl / a_s / 1e12 / bf16_tf

@@ -154,7 +154,7 @@ def test_multi_token_decode_sampled(dsa):
 
 
 @pytest.mark.parametrize("spec", [W.SMALL_DECODE_BF16, W.SMALL_DECODE_FP8, W.SMALL_DECODE_MX, W.SMALL_FP8_D64,
-                                  W.SMALL_MX_D64, W.SMALL_H8], ids=lambda s: s.name)
+                                  W.SMALL_MX_D64, W.SMALL_H8, W.SMALL_PREFILL, W.SMALL_MULTI], ids=lambda s: s.name)
 def test_relu_activation(dsa, spec):
     """The per-head ReLU variant against the oracle's 'relu' reading, in every key format
     and width (per-head tensor-core kernel for 128-dim keys, the CUDA-core kernel for
