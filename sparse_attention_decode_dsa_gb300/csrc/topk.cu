@@ -9,8 +9,8 @@
 // Scores are compared through an order-preserving 32-bit key (score_key).  The scoring
 // pass already counted, per row, how many keys fall in each of the 4096 bins of their
 // top 12 bits (kept in the workspace).  A cluster of C CTAs (1, 2, 4 or 8: the fewest
-// that keep a CTA's share of the longest row within 4096 keys) shares each row, CTA r
-// owning the r-th C-th of its positions:
+// that keep a CTA's share of the longest row within 4096 keys; 16 for rows beyond 32768)
+// shares each row, CTA r owning the r-th C-th of its positions:
 //   1. every CTA finds, from that histogram, the bin holding the K-th largest key (its
 //      own keys are loading meanwhile);
 //   2. each CTA counts its keys above that bin and gathers the keys in it (the
@@ -29,7 +29,10 @@
 // result.
 #include <cooperative_groups.h>
 
+#include <atomic>
+
 #include "common.cuh"
+#include "dsa_internal.h"
 
 namespace cg = cooperative_groups;
 
@@ -124,9 +127,11 @@ __device__ __forceinline__ void find_bin1024(const uint32_t* hist, uint32_t rema
   }
 }
 
-template <int kCluster>  // CTAs per row
-__global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 3) topk_cluster_kernel(TopkParams p) {
-  constexpr int kSlot = kPoolTotal / kCluster;  // candidates one CTA may put in the pool
+template <int kCluster>  // CTAs per row (the launch's cluster dimension)
+__global__ void __launch_bounds__(kThreads, 3) topk_cluster_kernel(TopkParams p) {
+  // candidates one CTA may put in the pool (clusters of 16 pool twice as many, so that a
+  // CTA keeps 256 slots)
+  constexpr int kSlot = (kCluster >= 16 ? 2 * kPoolTotal : kPoolTotal) / kCluster;
   cg::cluster_group cluster = cg::this_cluster();
   const int rank = (int)cluster.block_rank();
   const int row = blockIdx.y;
@@ -503,13 +508,34 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 3) 
 
 cudaError_t launch_topk(const TopkParams& p, int32_t max_visible, cudaStream_t s) {
   // the fewest CTAs per row that keep each CTA's share of the longest row within one
-  // block of keys held in registers (more for longer rows, at most 8)
-  const int cl = max_visible <= kBlock ? 1 : max_visible <= 2 * kBlock ? 2 : max_visible <= 4 * kBlock ? 4 : 8;
+  // block of keys held in registers (more for longer rows: 16, a non-portable cluster
+  // size, beyond 8 blocks; where a device cannot run clusters of 16, 8)
+  const int cl = max_visible <= kBlock ? 1 : max_visible <= 2 * kBlock ? 2 : max_visible <= 4 * kBlock ? 4
+               : max_visible <= 8 * kBlock ? 8 : 16;
+  const dim3 b(kThreads);
   switch (cl) {
-    case 1: return launch_pdl(topk_cluster_kernel<1>, dim3(1, p.tv.n_tokens), dim3(kThreads), 0, s, p);
-    case 2: return launch_pdl(topk_cluster_kernel<2>, dim3(2, p.tv.n_tokens), dim3(kThreads), 0, s, p);
-    case 4: return launch_pdl(topk_cluster_kernel<4>, dim3(4, p.tv.n_tokens), dim3(kThreads), 0, s, p);
-    default: return launch_pdl(topk_cluster_kernel<8>, dim3(8, p.tv.n_tokens), dim3(kThreads), 0, s, p);
+    case 1: return launch_pdl_cluster(topk_cluster_kernel<1>, dim3(1, p.tv.n_tokens), b, 0, s, 1u, p);
+    case 2: return launch_pdl_cluster(topk_cluster_kernel<2>, dim3(2, p.tv.n_tokens), b, 0, s, 2u, p);
+    case 4: return launch_pdl_cluster(topk_cluster_kernel<4>, dim3(4, p.tv.n_tokens), b, 0, s, 4u, p);
+    case 8: return launch_pdl_cluster(topk_cluster_kernel<8>, dim3(8, p.tv.n_tokens), b, 0, s, 8u, p);
+    default: {
+      static std::atomic<int> allowed[kMaxDevices];  // 1: set, -1: refused on that device
+      int dev = 0;
+      cudaError_t e = cudaGetDevice(&dev);
+      if (e != cudaSuccess) return e;
+      const int idx = dev >= 0 && dev < kMaxDevices ? dev : 0;
+      if (allowed[idx].load(std::memory_order_acquire) == 0) {
+        e = cudaFuncSetAttribute(topk_cluster_kernel<16>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        allowed[idx].store(e == cudaSuccess ? 1 : -1, std::memory_order_release);
+        if (e != cudaSuccess) (void)cudaGetLastError();
+      }
+      if (allowed[idx].load(std::memory_order_acquire) == 1) {
+        e = launch_pdl_cluster(topk_cluster_kernel<16>, dim3(16, p.tv.n_tokens), b, 0, s, 16u, p);
+        if (e == cudaSuccess) return e;
+        (void)cudaGetLastError();  // a device without room for clusters of 16: eight CTAs per row
+      }
+      return launch_pdl_cluster(topk_cluster_kernel<8>, dim3(8, p.tv.n_tokens), b, 0, s, 8u, p);
+    }
   }
 }
 
