@@ -25,8 +25,8 @@
 // Keys are read from the score row (in L2) in blocks of 4096 positions held in
 // registers, all loads of a block in flight together.  If a CTA has more candidates
 // than its pool slot (a row with very many equal top bits), steps 3-4 fall back to a
-// radix select that rescans the whole row and exchanges the counts, with the same
-// result.
+// radix select over each CTA's own keys whose histograms and counts the cluster sums
+// through distributed shared memory, with the same result.
 #include <cooperative_groups.h>
 
 #include <atomic>
@@ -386,25 +386,42 @@ __global__ void __launch_bounds__(kThreads, 3) topk_cluster_kernel(TopkParams p)
     taken0 = s_taken_before;
     ties0 = s_eq_before;
   } else {
-    // fallback: radix select rescanning the whole row, counts exchanged in the cluster
+    // fallback: an MSB-first radix select over the remaining 20 bits (8 + 8 + 4): each
+    // CTA counts its own keys (the row's r-th C-th, from registers) into a 256-bin
+    // histogram, and the cluster sums the CTAs' histograms through distributed shared
+    // memory (one barrier once all are counted, one once all are read, since the next
+    // pass recounts into the same bins); counts are exchanged the same way below
 #pragma unroll 1
     for (int pass = 0; pass < 3; ++pass) {
       const int shift = pass == 0 ? 12 : (pass == 1 ? 4 : 0);
       const uint32_t dmask = pass == 2 ? 0xFu : 0xFFu;
       hist[tid] = 0;
       __syncthreads();
-      for (int base = 0; base < n; base += kThreads) {
-        const int i = base + tid;
-        const uint32_t k = i < n ? score_key(__ldg(srow + i)) : 0u;
-        const bool in = i < n && (k & mask) == prefix;
-        const unsigned act = __ballot_sync(0xffffffffu, in);
-        if (in) {
-          const unsigned peers = __match_any_sync(act, (k >> shift) & dmask);
-          if (lane == __ffs(peers) - 1) atomicAdd(&hist[(k >> shift) & dmask], (uint32_t)__popc(peers));
+      for (int blk = 0; blk < nblocks; ++blk) {
+        if (loaded != blk) {
+          load_block(blk);
+          loaded = blk;
+        }
+        const int base = lo + blk * kBlock + warp * (kChunks * 32) + lane;
+#pragma unroll
+        for (int c = 0; c < kChunks; ++c) {
+          const uint32_t k = kr[c];
+          const bool in = base + c * 32 < hi && (k & mask) == prefix;
+          const unsigned act = __ballot_sync(0xffffffffu, in);
+          if (in) {
+            const unsigned peers = __match_any_sync(act, (k >> shift) & dmask);
+            if (lane == __ffs(peers) - 1) atomicAdd(&hist[(k >> shift) & dmask], (uint32_t)__popc(peers));
+          }
         }
       }
       __syncthreads();
-      if (warp == 0) find_bin256(hist, remaining, &s_digit, &s_above);
+      cluster.sync();  // every CTA's counts are in its hist[0, 256)
+      uint32_t tot = 0;
+      for (int r = 0; r < kCluster; ++r) tot += *cluster.map_shared_rank(&hist[tid], r);
+      cluster.sync();  // every CTA has read them (the next pass recounts into them)
+      hist[256 + tid] = tot;
+      __syncthreads();
+      if (warp == 0) find_bin256(hist + 256, remaining, &s_digit, &s_above);
       __syncthreads();
       prefix |= s_digit << shift;
       mask |= dmask << shift;
