@@ -214,6 +214,11 @@ SMALL_H5 = Spec(
     idx_heads=4, idx_dim=64, head_w_exps=(-3, 0), topk=512, sfa_heads=5, seed=7019,
     description="5 SFA heads, 512 selected rows per token in eight splits")
 
+# an MXFP8 indexer with 40 heads: the MMA's N = 48 columns, heads 32-39 in the second
+# column of the query's scale factors, columns 40-47 computed and ignored
+SMALL_MX_H40 = replace(SMALL_DECODE_MX, name="small_mx_h40", idx_heads=40, seed=7020,
+                       description="as small_decode_mx with 40 indexer heads")
+
 # long rows whose selection runs in clusters of eight CTAs (more than 16384 positions);
 # the tests give them degenerate queries (all scores equal, or 17 distinct values) so
 # that a CTA's boundary bin overflows its share of the candidate pool
@@ -224,7 +229,8 @@ LONG_ROWS = Spec(
 
 SMALL = [SMALL_DECODE_BF16, SMALL_DECODE_FP8, SMALL_DECODE_MX, SMALL_TIES, SMALL_PREFILL,
          SMALL_H8, EMPTY_AND_SHORT, SMALL_MID, SMALL_SIB, SMALL_MULTI, SMALL_FP8_D64, SMALL_MX_D64,
-         SMALL_PREFILL_FP8, SMALL_PREFILL_MX, SMALL_MULTI25, SMALL_MULTI_FP8, SMALL_FP8_KV, SMALL_H5]
+         SMALL_PREFILL_FP8, SMALL_PREFILL_MX, SMALL_MULTI25, SMALL_MULTI_FP8, SMALL_FP8_KV, SMALL_H5,
+         SMALL_MX_H40]
 
 ALL = {s.name: s for s in HEADLINE + EXTRA + SMALL + [LONG_ROWS]}
 

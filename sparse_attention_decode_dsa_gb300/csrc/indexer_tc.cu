@@ -11,18 +11,21 @@
 // tile) items.  Warp roles:
 //   warp 0     TMA producer: two 64-token pages of the K-index cache per tile (each a
 //              64 x 128 B box with 128-byte swizzle) into a ring of shared-memory
-//              stages; the row's query [H x d] into one of two query slots;
+//              stages (for MXFP8 also the pages' key scales, 256 B each); the row's
+//              query [H x d] into one of two query slots;
 //   warp 1     one thread issues tcgen05.mma: D[128 tokens x N heads] (f32, TMEM) =
-//              K_tile[128 x d] . q[N x d]^T, N = H rounded up to 16; MXFP8 keeps one
-//              accumulator per 32-wide group so the group scales apply exactly;
+//              K_tile[128 x d] . q[N x d]^T, N = H rounded up to 16; for MXFP8 the
+//              block-scaled form applies both sides' group scales in the tensor core;
 //   warps 2-9  epilogue, two groups of four warps taking alternate tiles: TMEM lane
 //              i = token i; each thread reads its token's head scores with
 //              tcgen05.ld, applies scales, activation and head weights, sums over
 //              heads, stores one f32 score and counts it in the row's histogram of
-//              key top-12-bit bins (what the Top-K pass starts from).
-// Four TMEM accumulators (two for MXFP8, whose four groups need four times the
-// columns) let the MMA run ahead of both epilogue groups.  Every wait is bounded (see
-// sm100::mbar_wait).
+//              key top-12-bit bins (what the Top-K pass starts from);
+//   warps 10-13  MXFP8 only: one warp per TMEM lane quarter copies each tile's key
+//              scales (and, per row, the query's) from shared into tensor memory,
+//              where the block-scaled MMA reads them.
+// Four TMEM accumulators let the MMA run ahead of both epilogue groups.  Every wait is
+// bounded (see sm100::mbar_wait).
 #include "sm100.cuh"
 
 namespace dsa {
@@ -32,7 +35,10 @@ namespace {
 using namespace sm100;
 
 constexpr int kEpiGroups = 2;                    // epilogue groups, alternating tiles
-constexpr int kTcThreads = 64 + kEpiGroups * 128; // producer warp, MMA warp, 4 warps per group
+// producer warp, MMA warp, 4 warps per epilogue group; MXFP8 MMAs: 4 scale-factor warps
+__host__ __device__ constexpr int tc_threads(int kind, bool fold) {
+  return 64 + kEpiGroups * 128 + (kind == 2 && !fold ? 128 : 0);
+}
 constexpr int kTileTok = 128;
 constexpr int kMaxRowsPerLaunch = 1024;
 static_assert(kBlockedMaxSeg == kMaxRowsPerLaunch, "a segment of several sequences' rows fits in one launch");
@@ -43,16 +49,27 @@ struct Cfg {
   static constexpr int kRowBytes = D * kElem;              // bytes of one key / query row
   static constexpr int kRegions = kRowBytes / 128;         // 128-byte swizzle columns per row
   static constexpr int kBoxInner = 128 / kElem;            // elements in one 128-byte piece
-  static constexpr int kStageBytes = kTileTok * kRowBytes;
+  static constexpr int kTileBytes = kTileTok * kRowBytes;  // the keys of a tile
+  // MXFP8: the tile's key scales (128 words of four E8M0 bytes) follow its keys
+  static constexpr int kStageBytes = kTileBytes + (KIND == 2 ? 1024 : 0);
+  // The folded path's epilogue groups wait on the stages themselves: group g takes the
+  // tiles n = g mod G and stage n mod S, so with S a multiple of G each group sees every
+  // phase of the stages it reads and no parity wait can match a phase two back.
   static constexpr int kStages = KIND == 0 ? 4 : 10;
+  static_assert(kStages % kEpiGroups == 0, "stages a multiple of the epilogue groups");
   static constexpr int kRegionStageBytes = kTileTok * 128;  // 16 KB
   static constexpr int kRegionQBytes = 64 * 128;           // 8 KB (up to 64 heads)
   static constexpr int kQSlotBytes = kRegions * kRegionQBytes;
   static constexpr int kKSteps = kRowBytes / 32;           // one MMA consumes 32 bytes of K
-  static constexpr int kGroups = KIND == 2 ? D / 32 : 1;
-  static constexpr int kAccCols = 64 * kGroups;
-  static constexpr int kNumAcc = KIND == 2 ? 2 : 4;        // TMEM accumulator buffers
-  static constexpr int kTmemCols = kNumAcc * kAccCols;
+  static constexpr int kGroups = KIND == 2 ? D / 32 : 1;   // scale groups per key
+  static constexpr int kAccCols = 64;                      // one accumulator: up to 64 heads
+  static constexpr int kNumAcc = 4;                        // TMEM accumulator buffers
+  // MXFP8: the MMA's scale factors follow the accumulators in tensor memory, 32-column
+  // aligned: the keys' for each accumulator in flight, the query's for each query slot
+  static constexpr int kSfaCol = kNumAcc * kAccCols;
+  static constexpr int kSfbCol = kSfaCol + 32 * kNumAcc;
+  static constexpr int kTmemCols = KIND == 2 ? 512 : kNumAcc * kAccCols;
+  static_assert(kSfbCol + 64 <= kTmemCols || KIND != 2, "tensor memory budget");
   static constexpr uint32_t kFmt = KIND == 0 ? 1u : 0u;    // bf16 / e4m3
   static constexpr int kSmem = 1024 /*align*/ + kStages * kStageBytes + 2 * kQSlotBytes + 4096 /*bars*/ +
                                4 * (kMaxRowsPerLaunch + 1) * 4 + 4 * kEpiGroups * (64 + 64 * 4 + 4) * 4;
@@ -101,10 +118,12 @@ __device__ __forceinline__ void e4m3x16_to_f32(const uint4& raw, float* out) {
 // FOLD: e4m3 keys, identity activation: no tensor cores; the epilogue warps take each
 // key's dot product with the folded query q~ (p.qt) straight from the staged tile.
 template <int KIND, int D, bool BLK, bool FOLD = false>
-__global__ void __launch_bounds__(kTcThreads, 1)
+__global__ void __launch_bounds__(tc_threads(KIND, FOLD), 1)
     score_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap qmap,
                     const TcArgs a) {
   using C = Cfg<KIND, D>;
+  constexpr bool BS = KIND == 2 && !FOLD;  // block-scaled MMAs, scale-factor warps
+  constexpr int kThreads = tc_threads(KIND, FOLD);
   const ScoreParams& p = a.p;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   pdl_trigger();  // the next kernel may start its set-up; it waits for this one to finish
@@ -123,7 +142,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   uint64_t* acc_empty = acc_full + C::kNumAcc;
   uint64_t* q_full = acc_empty + C::kNumAcc;
   uint64_t* q_empty = q_full + 2;
-  uint64_t* drain = q_empty + 2;
+  uint64_t* sf_ready = q_empty + 2;  // MXFP8: a tile's scale factors are in TMEM
+  uint64_t* drain = sf_ready + C::kStages;
   uint32_t* tmem_base_s = (uint32_t*)(drain + 1);
   volatile int* abort_flag = (volatile int*)(tmem_base_s + 1);
   int* prefix = (int*)(bars + 512);                 // [units + 1] item prefix (unit: a row, or a block)
@@ -146,6 +166,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       mbar_init(&q_full[i], 1);
       mbar_init(&q_empty[i], 1);
     }
+    for (int s = 0; s < C::kStages; ++s) mbar_init(&sf_ready[s], 4);  // the four scale warps
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -158,7 +179,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   }
   // visible counts and tiles of every row, then an exclusive scan (one warp)
   const int nunits = BLK ? a.nrows / a.seg * ((a.seg + kBlockRows - 1) / kBlockRows) : a.nrows;
-  for (int r = tid; r < a.nrows; r += kTcThreads) {
+  for (int r = tid; r < a.nrows; r += kThreads) {
     int b, n;
     resolve_token(p.tv, a.row0 + r, &b, &n, p.err);
     rowb[r] = b;
@@ -170,7 +191,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   }
   if (BLK) {
     __syncthreads();
-    for (int u = tid; u < nunits; u += kTcThreads) {  // a block sees its rows' widest window
+    for (int u = tid; u < nunits; u += kThreads) {  // a block sees its rows' widest window
       int r0, nb, m = 0;
       block_unit(a, u, &r0, &nb);
       for (int r = r0; r < r0 + nb; ++r) m = max(m, rn[r]);
@@ -207,76 +228,98 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // When the query is written by the preceding kernel the producer waits for it (the
     // K-index loads share its in-order issue); a caller-supplied query is read at once.
     if (p.q_dep) pdl_wait();
-    if (lane == 0) {
-      int stage = 0;
-      uint32_t phase = 0;
-      uint32_t armed = 0, armed_parity = 0;  // stages with a load issued, and its phase parity
-      uint32_t qarmed = 0, qparity = 0;      // the same for the two query slots
-      int r = 0, cur_row = -1, qcount = 0;
-      for (int it = it_begin; it < it_end; ++it) {
-        while (prefix[r + 1] <= it) ++r;
-        if (!FOLD && r != cur_row) {
-          cur_row = r;
-          int ur0 = r, unb = 1;
-          if (BLK) block_unit(a, r, &ur0, &unb);
-          const int slot = qcount & 1;
-          if (!mbar_wait(&q_empty[slot], ((qcount >> 1) & 1) ^ 1, abort_flag, p.err, p.wait_limit)) break;
-          mbar_arrive_expect_tx(&q_full[slot], C::kRegions * H * 128);
-          qarmed |= 1u << slot;
-          qparity = (qparity & ~(1u << slot)) | ((uint32_t)((qcount >> 1) & 1) << slot);
-          const uint32_t qdst = smem_u32(qslots + slot * C::kQSlotBytes);
-          for (int g = 0; g < C::kRegions; ++g)
-            tma_load_2d(qdst + g * C::kRegionQBytes, &qmap, &q_full[slot], g * C::kBoxInner,
-                        BLK ? 3 * (a.row0 + ur0) : (a.row0 + r) * H);
-          ++qcount;
-        }
-        if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.err, p.wait_limit)) break;
-        const int tile = it - prefix[r];
-        int br = r;
+    // The page ids of the next 32 items are resolved by the warp's lanes at once, one item
+    // each (a page-table read costs several hundred cycles: one at a time they would
+    // bound the stream); lane 0 then arms and issues the loads in order.
+    int stage = 0;
+    uint32_t phase = 0;
+    uint32_t armed = 0, armed_parity = 0;  // stages with a load issued, and its phase parity
+    uint32_t qarmed = 0, qparity = 0;      // the same for the two query slots
+    int r = 0, cur_row = -1, qcount = 0;
+    bool stop = false;
+    for (int it0 = it_begin; it0 < it_end && !stop; it0 += 32) {
+      const int mine = it0 + lane;
+      int lr = r, lpg0 = -1, lpg1 = -1;
+      if (mine < it_end) {
+        while (prefix[lr + 1] <= mine) ++lr;
+        const int tile = mine - prefix[lr];
+        int br = lr;
         if (BLK) {
           int unb;
-          block_unit(a, r, &br, &unb);
+          block_unit(a, lr, &br, &unb);
         }
-        const int b = rowb[br];
-        const int npages = (rown[r] + kPage - 1) / kPage;
-        int pg[2] = {-1, -1};
-        uint32_t bytes = 0;
-        for (int u = 0; u < 2; ++u) {
-          const int j = 2 * tile + u;
-          if (j < npages) {
-            pg[u] = physical_page(p.tv, b, j, p.err);
-            if (pg[u] >= 0) bytes += kPage * C::kRowBytes;
+        const int npages = (rown[lr] + kPage - 1) / kPage;
+        if (2 * tile < npages) lpg0 = physical_page(p.tv, rowb[br], 2 * tile, p.err);
+        if (2 * tile + 1 < npages) lpg1 = physical_page(p.tv, rowb[br], 2 * tile + 1, p.err);
+      }
+      const int nb = min(32, it_end - it0);
+      for (int k = 0; k < nb; ++k) {
+        const int pg[2] = {__shfl_sync(0xffffffffu, lpg0, k), __shfl_sync(0xffffffffu, lpg1, k)};
+        int ok = 1;
+        if (lane == 0) {
+          const int it = it0 + k;
+          while (prefix[r + 1] <= it) ++r;
+          if (!FOLD && r != cur_row) {
+            cur_row = r;
+            int ur0 = r, unb = 1;
+            if (BLK) block_unit(a, r, &ur0, &unb);
+            const int slot = qcount & 1;
+            ok = mbar_wait(&q_empty[slot], ((qcount >> 1) & 1) ^ 1, abort_flag, p.err, p.wait_limit);
+            if (ok) {
+              mbar_arrive_expect_tx(&q_full[slot], C::kRegions * H * 128);
+              qarmed |= 1u << slot;
+              qparity = (qparity & ~(1u << slot)) | ((uint32_t)((qcount >> 1) & 1) << slot);
+              const uint32_t qdst = smem_u32(qslots + slot * C::kQSlotBytes);
+              for (int g = 0; g < C::kRegions; ++g)
+                tma_load_2d(qdst + g * C::kRegionQBytes, &qmap, &q_full[slot], g * C::kBoxInner,
+                            BLK ? 3 * (a.row0 + ur0) : (a.row0 + r) * H);
+              ++qcount;
+            }
+          }
+          if (ok) ok = mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.err, p.wait_limit);
+          if (ok) {
+            uint32_t bytes = 0;
+            for (int u = 0; u < 2; ++u)
+              if (pg[u] >= 0) bytes += kPage * C::kRowBytes + (BS ? kPage * 4 : 0);
+            mbar_arrive_expect_tx(&full[stage], bytes);
+            armed |= 1u << stage;
+            armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
+            const uint32_t sdst = smem_u32(stages + stage * C::kStageBytes);
+            for (int u = 0; u < 2; ++u) {
+              if (pg[u] < 0) continue;
+              for (int g = 0; g < C::kRegions; ++g)
+                tma_load_2d(sdst + g * C::kRegionStageBytes + u * (kPage * 128), &kmap, &full[stage],
+                            g * C::kBoxInner, pg[u] * kPage);
+              if (BS)  // the page's 64 key scale words (a 16-byte aligned 256-byte run)
+                bulk_load(sdst + C::kTileBytes + u * (kPage * 4), (const uint8_t*)p.k_scale + (int64_t)pg[u] * kPage * 4,
+                          kPage * 4, &full[stage]);
+            }
+            if (++stage == C::kStages) {
+              stage = 0;
+              phase ^= 1;
+            }
           }
         }
-        mbar_arrive_expect_tx(&full[stage], bytes);
-        armed |= 1u << stage;
-        armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
-        const uint32_t sdst = smem_u32(stages + stage * C::kStageBytes);
-        for (int u = 0; u < 2; ++u) {
-          if (pg[u] < 0) continue;
-          for (int g = 0; g < C::kRegions; ++g)
-            tma_load_2d(sdst + g * C::kRegionStageBytes + u * (kPage * 128), &kmap, &full[stage],
-                        g * C::kBoxInner, pg[u] * kPage);
-        }
-        if (++stage == C::kStages) {
-          stage = 0;
-          phase ^= 1;
+        if (!__shfl_sync(0xffffffffu, ok, 0)) {
+          stop = true;
+          break;
         }
       }
-      if (*abort_flag) {
-        // let every copy still in flight (key tiles and queries) land before the shared
-        // memory is released
-        for (int st = 0; st < C::kStages; ++st) {
-          if (!(armed >> st & 1)) continue;
-          const long long t0 = clock64();
-          while (!mbar_try_wait(smem_u32(&full[st]), (armed_parity >> st) & 1) && clock64() - t0 < kWaitLimitCycles) {
-          }
+      r = __shfl_sync(0xffffffffu, r, 0);
+    }
+    if (lane == 0 && *abort_flag) {
+      // let every copy still in flight (key tiles and queries) land before the shared
+      // memory is released
+      for (int st = 0; st < C::kStages; ++st) {
+        if (!(armed >> st & 1)) continue;
+        const long long t0 = clock64();
+        while (!mbar_try_wait(smem_u32(&full[st]), (armed_parity >> st) & 1) && clock64() - t0 < kWaitLimitCycles) {
         }
-        for (int sl = 0; sl < 2; ++sl) {
-          if (!(qarmed >> sl & 1)) continue;
-          const long long t0 = clock64();
-          while (!mbar_try_wait(smem_u32(&q_full[sl]), (qparity >> sl) & 1) && clock64() - t0 < kWaitLimitCycles) {
-          }
+      }
+      for (int sl = 0; sl < 2; ++sl) {
+        if (!(qarmed >> sl & 1)) continue;
+        const long long t0 = clock64();
+        while (!mbar_try_wait(smem_u32(&q_full[sl]), (qparity >> sl) & 1) && clock64() - t0 < kWaitLimitCycles) {
         }
       }
     }
@@ -296,6 +339,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           ++qcount;
         }
         if (!mbar_wait(&full[stage], phase, abort_flag, p.err, p.wait_limit)) break;
+        if (BS && !mbar_wait(&sf_ready[stage], phase, abort_flag, p.err, p.wait_limit)) break;
         if (!mbar_wait(&acc_empty[acc], acc_phase ^ 1, abort_flag, p.err, p.wait_limit)) break;
         tc_fence_after();
         const uint32_t a0 = smem_u32(stages + stage * C::kStageBytes);
@@ -310,8 +354,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             mma_f16(d0, ad, bd, idesc_v, k > 0);
           } else if (KIND == 1) {
             mma_f8(d0, ad, bd, idesc_v, k > 0);
-          } else {
-            mma_f8(d0 + k * 64, ad, bd, idesc_v, 0);  // one accumulator per 32-wide group
+          } else {  // K block k: byte k of each scale word
+            mma_mxf8(d0, ad, bd, idesc_mx(128, N, k, k), tmem_base + C::kSfaCol + 32 * acc,
+                     tmem_base + C::kSfbCol + 32 * slot, k > 0);
           }
         }
         tc_commit(&empty[stage]);
@@ -330,6 +375,51 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       tc_commit(drain);
       const long long t0 = clock64();
       while (!mbar_try_wait(smem_u32(drain), 0) && clock64() - t0 < kWaitLimitCycles) {
+      }
+    }
+  } else if (BS && warp >= 2 + 4 * kEpiGroups) {
+    // ============================ scale factors (MXFP8) ===========================
+    // Each lane quarter of the tensor core reads the scale factors from its own 32
+    // TMEM lanes, so each of the four warps writes the same words into its quarter:
+    // row j of the MMA (key j of the tile, head j of the query) at lane j % 32, column
+    // j / 32, one byte per 32-element group.  A tile's key scales go to the columns of
+    // its accumulator once that accumulator is free (its previous MMAs are done); the
+    // query's go to its slot's columns with the row's first tile, which the producer
+    // loads only after the slot's previous row has finished.
+    const uint32_t lq = tmem_base + ((uint32_t)((warp & 3) * 32) << 16);
+    int stage = 0, acc = 0, r = 0, cur_row = -1, qcount = 0;
+    uint32_t phase = 0, acc_phase = 0;
+    for (int it = it_begin; it < it_end; ++it) {
+      while (prefix[r + 1] <= it) ++r;
+      bool ok = true;
+      if (lane == 0) {
+        ok = mbar_wait(&full[stage], phase, abort_flag, p.err, p.wait_limit) &&
+             mbar_wait(&acc_empty[acc], acc_phase ^ 1, abort_flag, p.err, p.wait_limit);
+      }
+      if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+      __syncwarp();
+      tc_fence_after();
+      if (r != cur_row) {
+        cur_row = r;
+        const int slot = qcount++ & 1;
+        const int64_t qrow = (int64_t)(a.row0 + r) * H;
+        const uint32_t* qs = (const uint32_t*)p.q_scale;
+        tmem_st2(lq + C::kSfbCol + 32 * slot, lane < H ? qs[qrow + lane] : 0x7F7F7F7Fu,
+                 32 + lane < H ? qs[qrow + 32 + lane] : 0x7F7F7F7Fu);
+      }
+      const uint32_t* ks = (const uint32_t*)(stages + stage * C::kStageBytes + C::kTileBytes);
+      tmem_st4(lq + C::kSfaCol + 32 * acc, ks[lane], ks[32 + lane], ks[64 + lane], ks[96 + lane]);
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sf_ready[stage]);
+      if (++stage == C::kStages) {
+        stage = 0;
+        phase ^= 1;
+      }
+      if (++acc == C::kNumAcc) {
+        acc = 0;
+        acc_phase ^= 1;
       }
     }
   } else {
@@ -451,8 +541,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
       }
     } else {
+    // (MXFP8 accumulators arrive with both sides' scales applied by the MMA)
     float* w_s = epi + (warp - 2) * (64 + 64 * 4 + 4);
-    float* qs_s = w_s + 64;             // [h][g] query group scales (MX)
     int r = 0, cur_row = -1;
     float qtok = 1.f;
     for (int it = it_begin; it < it_end; ++it) {
@@ -465,17 +555,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       if (r != cur_row) {
         cur_row = r;
         __syncwarp();
-        for (int h = lane; h < H; h += 32) {
-          w_s[h] = p.head_w[(int64_t)grow * H + h];
-          if (KIND == 2) {
-            // identity: the head weight joins the query's group scale (a power of two,
-            // so the product is exact)
-            const float wq = p.act == DSA_ACT_IDENTITY ? w_s[h] : 1.f;
-            const uint32_t q4 = *(const uint32_t*)((const uint8_t*)p.q_scale + ((int64_t)grow * H + h) * 4);
-#pragma unroll
-            for (int g = 0; g < 4; ++g) qs_s[h * 4 + g] = wq * e8m0_to_f32((q4 >> (8 * g)) & 0xFF);
-          }
-        }
+        for (int h = lane; h < H; h += 32) w_s[h] = p.head_w[(int64_t)grow * H + h];
         qtok = (KIND == 1) ? ((const float*)p.q_scale)[grow] : 1.f;
         __syncwarp();
       }
@@ -484,18 +564,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const bool valid = t < rown[r];
       int pg = -1;
       if (valid) pg = physical_page(p.tv, rowb[r], t >> 6, nullptr);
-      float ks[C::kGroups];
-#pragma unroll
-      for (int g = 0; g < C::kGroups; ++g) ks[g] = 1.f;
-      if (pg >= 0) {
-        const int64_t krow = (int64_t)pg * kPage + (t & 63);
-        if (KIND == 1) ks[0] = ((const float*)p.k_scale)[krow];
-        if (KIND == 2) {
-          const uint32_t k4 = *(const uint32_t*)((const uint8_t*)p.k_scale + krow * 4);
-#pragma unroll
-          for (int g = 0; g < C::kGroups; ++g) ks[g] = e8m0_to_f32((k4 >> (8 * g)) & 0xFF);
-        }
-      }
+      const float ks = (KIND == 1 && pg >= 0) ? ((const float*)p.k_scale)[(int64_t)pg * kPage + (t & 63)] : 1.f;
       bool ok = true;
       if (lane == 0) ok = mbar_wait(&acc_full[acc], acc_phase, abort_flag, p.err, p.wait_limit);
       ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -504,12 +573,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       tc_fence_after();
       const uint32_t tbase = tmem_base + ((uint32_t)(quarter * 32) << 16) + acc * C::kAccCols;
       float part[4] = {0.f, 0.f, 0.f, 0.f};  // four independent sums over heads
-      if (KIND != 2) {
+      {
         uint32_t v0[32], v1[32];
         tmem_ld32(tbase, v0);
         if (H > 32) tmem_ld32(tbase + 32, v1);
         tmem_ld_wait();
-        const float sc = (KIND == 1) ? qtok * ks[0] : 1.f;
+        const float sc = (KIND == 1) ? qtok * ks : 1.f;
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
           if (j < H) {
@@ -527,50 +596,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
               if (KIND == 1) x *= sc;
               if (p.act == DSA_ACT_RELU) x = fmaxf(x, 0.f);
               part[j & 3] += x * w_s[32 + j];
-            }
-          }
-        }
-      } else if (p.act == DSA_ACT_IDENTITY) {
-        // sum_h w_h sum_g (ks_g qs_hg acc_gh) regrouped as sum_g ks_g sum_h (w_h qs_hg) acc_gh:
-        // one FMA per (group, head) and four multiplies per key (exact, like any order)
-#pragma unroll 1
-        for (int hc = 0; hc < 2; ++hc) {
-          if (hc * 32 >= H) break;
-          uint32_t v[C::kGroups][32];
-#pragma unroll
-          for (int g = 0; g < C::kGroups; ++g) tmem_ld32(tbase + g * 64 + hc * 32, v[g]);
-          tmem_ld_wait();
-#pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const int h = hc * 32 + j;
-            if (h < H) {
-              const float4 c = *(const float4*)(qs_s + h * 4);
-              part[0] = fmaf(__uint_as_float(v[0][j]), c.x, part[0]);
-              part[1] = fmaf(__uint_as_float(v[1][j]), c.y, part[1]);
-              part[2] = fmaf(__uint_as_float(v[2][j]), c.z, part[2]);
-              part[3] = fmaf(__uint_as_float(v[3][j]), c.w, part[3]);
-            }
-          }
-        }
-#pragma unroll
-        for (int g = 0; g < C::kGroups; ++g) part[g] *= ks[g];
-      } else {
-#pragma unroll 1
-        for (int hc = 0; hc < 2; ++hc) {
-          if (hc * 32 >= H) break;
-          uint32_t v[C::kGroups][32];
-#pragma unroll
-          for (int g = 0; g < C::kGroups; ++g) tmem_ld32(tbase + g * 64 + hc * 32, v[g]);
-          tmem_ld_wait();
-#pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const int h = hc * 32 + j;
-            if (h < H) {
-              float x = 0.f;
-#pragma unroll
-              for (int g = 0; g < C::kGroups; ++g) x += __uint_as_float(v[g][j]) * (ks[g] * qs_s[h * 4 + g]);
-              if (p.act == DSA_ACT_RELU) x = fmaxf(x, 0.f);
-              part[j & 3] += x * w_s[h];
             }
           }
         }
@@ -622,7 +647,7 @@ cudaError_t launch_tc(const ScoreParams& p, cudaStream_t s) {
     a.row0 = row0;
     a.nrows = p.tv.n_tokens - row0 < per_launch ? p.tv.n_tokens - row0 : per_launch;
     a.seg = seg < a.nrows ? seg : a.nrows;
-    e = launch_pdl(score_tc_kernel<KIND, D, BLK, FOLD>, dim3(sms), dim3(kTcThreads), C::kSmem, s, kmap, qmap, a);
+    e = launch_pdl(score_tc_kernel<KIND, D, BLK, FOLD>, dim3(sms), dim3(tc_threads(KIND, FOLD)), C::kSmem, s, kmap, qmap, a);
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;

@@ -152,6 +152,20 @@ __device__ __forceinline__ void mma_f8(uint32_t d_tmem, uint64_t adesc, uint64_t
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate));
 }
 
+// Same with block scaling (MXFP8: e4m3 inputs, one E8M0 scale per 32 elements along K
+// for every row of A and of B, applied by the tensor core).  One instruction covers one
+// 32-wide K block; its scales are read from tensor memory at sfa / sfb (column addresses
+// 32-column aligned): row j's scale in lane j % 32 of every lane quarter, column j / 32,
+// the byte selected by the descriptor's scale ids (idesc_mx).
+__device__ __forceinline__ void mma_mxf8(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                         uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %6, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n}\n" ::"r"(
+          d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate));
+}
+
 // D[tmem] (+)= A[tmem] * B[smem]^T, bf16/f16 inputs: A (M x K) lives in tensor memory,
 // lane = row, each 32-bit column two consecutive K elements (lower half = lower K).
 __device__ __forceinline__ void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
@@ -173,6 +187,14 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
       "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31]));
 }
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory"); }
+// Stores 4 (2) consecutive 32-bit columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_st4(uint32_t taddr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};\n" ::"r"(taddr), "r"(a), "r"(b), "r"(c),
+               "r"(d));
+}
+__device__ __forceinline__ void tmem_st2(uint32_t taddr, uint32_t a, uint32_t b) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x2.b32 [%0], {%1, %2};\n" ::"r"(taddr), "r"(a), "r"(b));
+}
 
 // ---- thread-block clusters ----------------------------------------------------------
 __device__ __forceinline__ uint32_t cluster_rank() {
@@ -383,6 +405,11 @@ __device__ __forceinline__ uint64_t desc_sw128_mn(uint32_t saddr, uint32_t lbo, 
 // a_fmt/b_fmt: kind::f16 -> 0 f16, 1 bf16; kind::f8f6f4 -> 0 e4m3, 1 e5m2.
 __host__ __device__ constexpr uint32_t idesc(int M, int N, uint32_t a_fmt, uint32_t b_fmt) {
   return (1u << 4) | (a_fmt << 7) | (b_fmt << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+// Block-scaled (kind::mxf8f6f4) instruction descriptor: e4m3 A and B, K-major, E8M0
+// scales; a_sf / b_sf pick the byte (0-3) of each scale word that this K block uses.
+__host__ __device__ constexpr uint32_t idesc_mx(int M, int N, uint32_t a_sf, uint32_t b_sf) {
+  return (b_sf << 4) | ((uint32_t)(N >> 3) << 17) | (1u << 23) | ((uint32_t)(M >> 4) << 24) | (a_sf << 29);
 }
 // Same with B read MN-major (bit 16).
 __host__ __device__ constexpr uint32_t idesc_bmn(int M, int N, uint32_t a_fmt, uint32_t b_fmt) {
