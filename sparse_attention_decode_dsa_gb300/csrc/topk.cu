@@ -99,32 +99,31 @@ __device__ __forceinline__ void find_bin256(const uint32_t* hist, uint32_t remai
   }
 }
 
-// Same over a 1024-bin histogram: lane l owns bins 1023 - 32 l .. 992 - 32 l.
-__device__ __forceinline__ void find_bin1024(const uint32_t* hist, uint32_t remaining, uint32_t* s_digit,
-                                             uint32_t* s_above) {
-  const int lane = threadIdx.x & 31;
-  uint32_t loc = 0;
-#pragma unroll
-  for (int u = 0; u < 32; ++u) loc += hist[1023 - 32 * lane - ((u + lane) & 31)];  // rotated: no bank conflicts
-  uint32_t incl = loc;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const uint32_t v = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += v;
-  }
-  const uint32_t ex = incl - loc;
-  if (ex < remaining && remaining <= incl) {
+// Same over a 1024-bin histogram, by the whole CTA: thread t owns bins 1023 - 4t ..
+// 1020 - 4t (one 16-byte load); a block scan places them.  Every thread calls it; it
+// ends with a barrier after which s_digit / s_above hold the result.
+__device__ __forceinline__ void find_bin1024(const uint32_t* hist, uint32_t remaining, int* buf,
+                                             uint32_t* s_digit, uint32_t* s_above) {
+  static_assert(kThreads * 4 == 1024, "four bins per thread");
+  const int tid = threadIdx.x;
+  const uint4 q = *(const uint4*)(hist + 1020 - 4 * tid);
+  const uint32_t h[4] = {q.w, q.z, q.y, q.x};  // bins 1023 - 4t - u, high to low
+  const uint32_t loc = h[0] + h[1] + h[2] + h[3];
+  int tot;
+  const uint32_t ex = (uint32_t)block_excl_sum((int)loc, buf, &tot);
+  if (ex < remaining && remaining <= ex + loc) {
     uint32_t cum = ex;
-    for (int u = 0; u < 32; ++u) {
-      const int bin = 1023 - 32 * lane - u;
-      if (cum + hist[bin] >= remaining) {
-        *s_digit = (uint32_t)bin;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      if (cum + h[u] >= remaining) {
+        *s_digit = (uint32_t)(1023 - 4 * tid - u);
         *s_above = cum;
         break;
       }
-      cum += hist[bin];
+      cum += h[u];
     }
   }
+  __syncthreads();
 }
 
 template <int kCluster>  // CTAs per row (the launch's cluster dimension)
@@ -138,10 +137,10 @@ __global__ void __launch_bounds__(kThreads, 3) topk_cluster_kernel(TopkParams p)
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int K = p.top_k;
   pdl_trigger();
+  int b, n;  // (token metadata are inputs: read before the dependency wait)
+  resolve_token(p.tv, row, &b, &n, nullptr);  // the score pass reports bad metadata
   pdl_wait();  // scores and histograms of the score kernel
 
-  int b, n;
-  resolve_token(p.tv, row, &b, &n, nullptr);  // the score pass reports bad metadata
   int32_t* out = p.out_idx + (int64_t)row * K;
   float* outs = p.out_score ? p.out_score + (int64_t)row * K : nullptr;
   const float* srow = p.scores + (int64_t)row * p.score_stride;
@@ -157,7 +156,7 @@ __global__ void __launch_bounds__(kThreads, 3) topk_cluster_kernel(TopkParams p)
   __shared__ uint32_t cand_local[kLocalCap];
   __shared__ uint32_t pool[kCluster][kSlot];  // every CTA's candidates
   __shared__ int pool_n[kCluster], pool_above[kCluster];
-  __shared__ uint32_t hist[1024];
+  __shared__ __align__(16) uint32_t hist[1024];
   __shared__ int wcnt[kWarpsPerCta];                 // candidates each warp gathered
   __shared__ int2 wstat[2][kWarpsPerCta];            // output: each warp's #{> T}, #{== T}
   __shared__ int red[kWarpsPerCta][2 * kCluster];    // per warp: #{> T}, #{== T} of each CTA's pool
@@ -323,8 +322,7 @@ __global__ void __launch_bounds__(kThreads, 3) topk_cluster_kernel(TopkParams p)
           }
       }
       __syncthreads();
-      if (warp == 0) find_bin1024(hist, remaining, &s_digit, &s_above);
-      __syncthreads();
+      find_bin1024(hist, remaining, buf, &s_digit, &s_above);
       prefix |= s_digit << shift;
       mask |= dmask << shift;
       remaining -= s_above;
