@@ -237,6 +237,9 @@ __global__ void __launch_bounds__(tc_threads(KIND, FOLD), 1)
     uint32_t qarmed = 0, qparity = 0;      // the same for the two query slots
     int r = 0, cur_row = -1, qcount = 0;
     bool stop = false;
+    // (streamed keys leave L2 first: the scores and histograms written meanwhile stay
+    // there for the selection pass)
+    const uint64_t l2_evict_first = l2_policy_evict_first();
     for (int it0 = it_begin; it0 < it_end && !stop; it0 += 32) {
       const int mine = it0 + lane;
       int lr = r, lpg0 = -1, lpg1 = -1;
@@ -287,9 +290,9 @@ __global__ void __launch_bounds__(tc_threads(KIND, FOLD), 1)
             const uint32_t sdst = smem_u32(stages + stage * C::kStageBytes);
             for (int u = 0; u < 2; ++u) {
               if (pg[u] < 0) continue;
-              for (int g = 0; g < C::kRegions; ++g)
-                tma_load_2d(sdst + g * C::kRegionStageBytes + u * (kPage * 128), &kmap, &full[stage],
-                            g * C::kBoxInner, pg[u] * kPage);
+              for (int g = 0; g < C::kRegions; ++g)  // keys are read once: evict them first
+                tma_load_2d_hint(sdst + g * C::kRegionStageBytes + u * (kPage * 128), &kmap, &full[stage],
+                                 g * C::kBoxInner, pg[u] * kPage, l2_evict_first);
               if (BS)  // the page's 64 key scale words (a 16-byte aligned 256-byte run)
                 bulk_load(sdst + C::kTileBytes + u * (kPage * 4), (const uint8_t*)p.k_scale + (int64_t)pg[u] * kPage * 4,
                           kPage * 4, &full[stage]);

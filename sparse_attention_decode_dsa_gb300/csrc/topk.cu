@@ -180,30 +180,32 @@ __global__ void __launch_bounds__(kThreads, 3) topk_cluster_kernel(TopkParams p)
       kr[c] = i < hi ? score_key(__ldg(srow + i)) : 0u;
     }
   };
-  int loaded = -1;
-  if (nblocks > 0) {
-    load_block(0);  // in flight while the histogram is scanned
-    loaded = 0;
-  }
-
   // ---- 1. bin of the K-th largest key among the 4096 top-12-bit bins (all CTAs alike)
-  // thread t owns bins 4095-16t .. 4080-16t (high to low)
+  // thread t owns bins 4095-16t .. 4080-16t (high to low); its loads go out first, the
+  // CTA's first block of keys right behind them (in flight while the bins are scanned)
   const uint32_t* h12 = p.hist + (int64_t)row * kTopkBins;
   uint32_t hb[16];
   uint32_t local = 0;
   {
     const uint4* hp = (const uint4*)(h12 + kTopkBins - 16 * (tid + 1));  // this thread's 16 bins, low to high
+    uint4 x[4];
+#pragma unroll
+    for (int v = 0; v < 4; ++v) x[v] = __ldg(hp + v);
 #pragma unroll
     for (int v = 0; v < 4; ++v) {
-      const uint4 x = __ldg(hp + v);
-      hb[15 - 4 * v] = x.x;
-      hb[14 - 4 * v] = x.y;
-      hb[13 - 4 * v] = x.z;
-      hb[12 - 4 * v] = x.w;
+      hb[15 - 4 * v] = x[v].x;
+      hb[14 - 4 * v] = x[v].y;
+      hb[13 - 4 * v] = x[v].z;
+      hb[12 - 4 * v] = x[v].w;
     }
-#pragma unroll
-    for (int u = 0; u < 16; ++u) local += hb[u];
   }
+  int loaded = -1;
+  if (nblocks > 0) {
+    load_block(0);
+    loaded = 0;
+  }
+#pragma unroll
+  for (int u = 0; u < 16; ++u) local += hb[u];
   if (tid == 0) {
     s_nlocal = 0;
     s_above_local = 0;
