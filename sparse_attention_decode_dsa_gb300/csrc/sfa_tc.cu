@@ -917,12 +917,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 // Merge of more than two splits: out[tok, h, 256 c + col] = sum_s w_s O_s / l_s with
 // w_s = 2^(lse_s - max) / sum 2^(lse - max), the splits taken in order (the result does
 // not depend on which CTA finished first).  One CTA of 128 threads per (token, value
-// half, 16-column chunk); thread t takes heads 4 (t % 32) .. + 3 and columns
-// 4 (t / 32) .. + 3 of the chunk: 16-byte loads over 4 heads (the partials are
-// column-major, their head stride H rounded up to a multiple of 4), all S x 4 of them in
-// flight together.
-constexpr int kCombineCols = 16;
+// half, 8-column chunk); thread t takes heads 4 (t % 32) .. + 3 and columns 2 (t / 32)
+// .. + 1 of the chunk: 16-byte loads over 4 heads (the partials are column-major, their
+// head stride H rounded up to a multiple of 4).  Every split's log2-sum-exp and the
+// values of up to eight splits are in flight together: a merge of eight splits waits
+// for one round of loads.
+constexpr int kCombineCols = 8;
 constexpr int kCombineThreads = 128;
+constexpr int kCombineGroup = 8;       // splits whose value loads are in flight together
 constexpr int kMaxCombineSplits = 16;  // (the planner makes at most 16 splits)
 
 __global__ void __launch_bounds__(kCombineThreads) sfa_combine_kernel(SfaParams p) {
@@ -931,33 +933,35 @@ __global__ void __launch_bounds__(kCombineThreads) sfa_combine_kernel(SfaParams 
   constexpr int kChunks = 256 / kCombineCols;
   const int tok = blockIdx.y, c = blockIdx.x / kChunks, k = blockIdx.x % kChunks;
   const int H = p.n_heads, S = p.n_splits, HP = (H + 3) & ~3;  // partials' head stride
-  const int h0 = 4 * (threadIdx.x & 31), col0 = kCombineCols * k + 4 * (threadIdx.x >> 5);
+  const int h0 = 4 * (threadIdx.x & 31), col0 = kCombineCols * k + 2 * (threadIdx.x >> 5);
   if (h0 >= H) return;
   const int64_t base = (int64_t)tok * S * 2 + c;  // + 2 s: split s of this half
   float4 lse[kMaxCombineSplits];
 #pragma unroll
   for (int s2 = 0; s2 < kMaxCombineSplits; ++s2)
     if (s2 < S) lse[s2] = *(const float4*)(p.part_lse + (base + 2 * s2) * HP + h0);
-  float4 mx = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
-#pragma unroll
-  for (int s2 = 0; s2 < kMaxCombineSplits; ++s2)
-    if (s2 < S)
-      mx = make_float4(fmaxf(mx.x, lse[s2].x), fmaxf(mx.y, lse[s2].y), fmaxf(mx.z, lse[s2].z), fmaxf(mx.w, lse[s2].w));
-  float acc[4][4] = {};  // [column][head]
+  float acc[2][4] = {};  // [column][head]
   float wsum[4] = {0.f, 0.f, 0.f, 0.f};
+  float4 mx = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
   auto wt = [](float l, float m) { return m != -INFINITY ? exp2f(l - m) : 0.f; };
-  // splits in groups of four: the group's 16 loads are in flight together
 #pragma unroll 1
-  for (int s0 = 0; s0 < S; s0 += 4) {
-    float4 v[4][4];
+  for (int s0 = 0; s0 < S; s0 += kCombineGroup) {
+    float4 v[kCombineGroup][2];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
+    for (int u = 0; u < kCombineGroup; ++u) {
       const float* po = p.part_o + ((base + 2 * min(s0 + u, S - 1)) * 256 + col0) * HP + h0;
+      v[u][0] = *(const float4*)po;
+      v[u][1] = *(const float4*)(po + HP);
+    }
+    if (s0 == 0) {  // (the first group's values are in flight meanwhile)
 #pragma unroll
-      for (int j = 0; j < 4; ++j) v[u][j] = *(const float4*)(po + j * HP);
+      for (int s2 = 0; s2 < kMaxCombineSplits; ++s2)
+        if (s2 < S)
+          mx = make_float4(fmaxf(mx.x, lse[s2].x), fmaxf(mx.y, lse[s2].y), fmaxf(mx.z, lse[s2].z),
+                           fmaxf(mx.w, lse[s2].w));
     }
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
+    for (int u = 0; u < kCombineGroup; ++u) {
       if (s0 + u >= S) break;
       float4 l = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
@@ -965,7 +969,7 @@ __global__ void __launch_bounds__(kCombineThreads) sfa_combine_kernel(SfaParams 
         if (s2 == s0 + u) l = lse[s2];
       const float w[4] = {wt(l.x, mx.x), wt(l.y, mx.y), wt(l.z, mx.z), wt(l.w, mx.w)};
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
+      for (int j = 0; j < 2; ++j) {
         acc[j][0] += w[0] * v[u][j].x;
         acc[j][1] += w[1] * v[u][j].y;
         acc[j][2] += w[2] * v[u][j].z;
@@ -979,8 +983,8 @@ __global__ void __launch_bounds__(kCombineThreads) sfa_combine_kernel(SfaParams 
   for (int e = 0; e < 4; ++e) {
     if (h0 + e >= H) break;  // heads past H in the last group of four (padding, never written)
     const float winv = wsum[e] > 0.f ? 1.f / wsum[e] : 0.f;
-    uint2* dst = (uint2*)(p.out + ((int64_t)tok * H + h0 + e) * kValueDim + 256 * c + col0);
-    *dst = make_uint2(pack_bf16x2(acc[0][e] * winv, acc[1][e] * winv), pack_bf16x2(acc[2][e] * winv, acc[3][e] * winv));
+    uint32_t* dst = (uint32_t*)(p.out + ((int64_t)tok * H + h0 + e) * kValueDim + 256 * c + col0);
+    *dst = pack_bf16x2(acc[0][e] * winv, acc[1][e] * winv);
   }
 }
 
