@@ -23,34 +23,46 @@ namespace dsa {
 
 namespace {
 
-constexpr int kQtThreads = 128;
+constexpr int kQtThreads = 512;
 
 // q~[row][d] = (per-token query scale) * sum_h w_h * (query group scale of h, MX) * q[h][d].
+// 512 threads per query token: thread (quarter j, dim d) sums 16 heads, all their loads
+// in flight together; the four quarter sums are added in order.  The query, weights and
+// scales are inputs, so all of it runs before the dependency wait; only the store of q~
+// (workspace the previous pass may still use) waits.
 template <int D, int KIND>  // KIND 0: bf16; 1: e4m3 + per-token f32; 2: e4m3 + E8M0/32
 __global__ void __launch_bounds__(kQtThreads) qtilde_kernel(ScoreParams p, float* qt) {
   pdl_trigger();
-  pdl_wait();  // q~ lives in workspace that the previous pass may still use
   const int row = blockIdx.x;
   const int H = p.n_heads;
-  for (int d = threadIdx.x; d < D; d += kQtThreads) {
-    float acc = 0.f;
-    for (int h0 = 0; h0 < H; h0 += 16) {  // fixed order; 16 heads' loads in flight
-      float q[16], w[16];
+  __shared__ float part[4][D];
+  for (int e = threadIdx.x; e < 4 * D; e += kQtThreads) {
+    const int j = e / D, d = e % D;
+    uint32_t qb[16], sb[16];
+    float w[16];
 #pragma unroll
-      for (int u = 0; u < 16; ++u) {
-        const int h = h0 + u;
-        const int64_t off = ((int64_t)row * H + (h < H ? h : 0)) * D + d;
-        q[u] = KIND == 0 ? bf16_to_f32(__ldg((const uint16_t*)p.q + off)) : e4m3_to_f32(__ldg((const uint8_t*)p.q + off));
-        w[u] = h < H ? __ldg(p.head_w + (int64_t)row * H + h) : 0.f;
-        if (KIND == 2 && h < H)
-          w[u] *= e8m0_to_f32(__ldg((const uint8_t*)p.q_scale + ((int64_t)row * H + h) * (D / 32) + d / 32));
-      }
-#pragma unroll
-      for (int u = 0; u < 16; ++u) acc = fmaf(w[u], q[u], acc);
+    for (int u = 0; u < 16; ++u) {  // every load of the 16 heads first, then the arithmetic
+      const int h = min(16 * j + u, H - 1);
+      const int64_t off = ((int64_t)row * H + h) * D + d;
+      qb[u] = KIND == 0 ? __ldg((const uint16_t*)p.q + off) : __ldg((const uint8_t*)p.q + off);
+      w[u] = __ldg(p.head_w + (int64_t)row * H + h);
+      sb[u] = KIND == 2 ? __ldg((const uint8_t*)p.q_scale + ((int64_t)row * H + h) * (D / 32) + d / 32) : 0u;
     }
-    if (KIND == 1) acc *= ((const float*)p.q_scale)[row];
-    qt[(int64_t)row * D + d] = acc;
+    float acc = 0.f;
+#pragma unroll
+    for (int u = 0; u < 16; ++u) {
+      const bool live = 16 * j + u < H;
+      const float q = KIND == 0 ? bf16_to_f32((uint16_t)qb[u]) : e4m3_to_f32((uint8_t)qb[u]);
+      const float wu = KIND == 2 ? w[u] * e8m0_to_f32((uint8_t)sb[u]) : w[u];
+      acc = fmaf(live ? wu : 0.f, q, acc);
+    }
+    part[j][d] = acc;
   }
+  const float qtok = KIND == 1 ? __ldg((const float*)p.q_scale + row) : 1.f;
+  __syncthreads();
+  pdl_wait();  // q~ lives in workspace that the previous pass may still use
+  for (int d = threadIdx.x; d < D; d += kQtThreads)
+    qt[(int64_t)row * D + d] = (((part[0][d] + part[1][d]) + part[2][d]) + part[3][d]) * qtok;
 }
 
 // bf16 keys on the tensor cores: q~ split exactly into three bf16 terms
@@ -69,7 +81,6 @@ constexpr int kSplitThreads = 512;
 template <int D, int KIND>
 __global__ void __launch_bounds__(kSplitThreads) qsplit_kernel(ScoreParams p, uint16_t* qs, float* ws, int stride) {
   pdl_trigger();
-  pdl_wait();  // the split query lives in workspace that the previous pass may still use
   const int row = blockIdx.x;
   const int H = p.n_heads;
   __shared__ float part[4][D];
@@ -97,6 +108,9 @@ __global__ void __launch_bounds__(kSplitThreads) qsplit_kernel(ScoreParams p, ui
   }
   __syncthreads();
   const float qtok = KIND == 1 ? __ldg((const float*)p.q_scale + row) : 1.f;
+  // (the sums above read inputs only; the split query lives in workspace that the
+  // previous pass may still use)
+  pdl_wait();
   for (int d = threadIdx.x; d < D; d += kSplitThreads) {
     const float qt = (((part[0][d] + part[1][d]) + part[2][d]) + part[3][d]) * qtok;
     const uint16_t hi = f32_to_bf16_rne(qt);
