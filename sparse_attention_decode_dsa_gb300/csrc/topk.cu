@@ -260,6 +260,10 @@ __global__ void __launch_bounds__(kThreads, 3) topk_cluster_kernel(TopkParams p)
       atomicAdd(&s_nlocal, nw);
     }
   }
+  if (loaded > 0) {  // the output (or the fallback) starts over at block 0: its loads now
+    load_block(0);   // overlap the pool exchange and the select
+    loaded = 0;
+  }
   __syncthreads();
 
   // ---- 3. pool (every CTA writes its part into every CTA), then one cluster barrier --
