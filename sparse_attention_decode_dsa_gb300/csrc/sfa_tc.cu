@@ -229,6 +229,41 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   __syncwarp();
   cluster_arrive();  // this CTA's barriers exist (the wait comes before any remote traffic)
+  if (warp >= kSendWarp0 && warp < kFinWarp0) {
+    // each sending thread moves its head row h of the latent part into tensor memory
+    // (packed bf16 pairs); rows past the head count are zero, in the rope operand too.
+    // Q is an input: this runs before the dependency wait, off the gathers' path
+    const int quarter = warp & 3;
+    const int h = quarter * 32 + lane;  // head row == TMEM lane
+    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    const bool live = h < H;
+    bool good = true;
+    if (lane == 0) good = mbar_wait(q_tma, 0, abort_flag, p.err);
+    good = __shfl_sync(0xffffffffu, good, 0);
+#pragma unroll 1
+    for (int q = 0; q < 4; ++q) {
+      uint32_t w[32];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const uint4 x = (live && good) ? *(const uint4*)(qstage + q * kQRegion + h * 128 + ((u ^ (h & 7)) << 4))
+                                       : make_uint4(0, 0, 0, 0);
+        w[4 * u] = x.x;
+        w[4 * u + 1] = x.y;
+        w[4 * u + 2] = x.z;
+        w[4 * u + 3] = x.w;
+      }
+      tmem_st32(tmem + lane_off + kColQl + 32 * q, w);
+    }
+    if (!live) {
+#pragma unroll
+      for (int v = 0; v < 4; ++v) *(uint4*)(qrope + h * 64 + (v << 4)) = make_uint4(0, 0, 0, 0);
+    }
+    fence_proxy_async_smem();  // visible to the MMA (async proxy)
+    tmem_st_wait();
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(q_ready);
+  }
   pdl_wait();        // the selected positions come from the previous kernel
   // Cache row of every selected position of this split (-1: padding or invalid), while
   // Q is in flight; all index loads of a thread are in flight together, then all
@@ -267,40 +302,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       rowid[j] = rid;
     }
     if (mylast >= 0) atomicMax(last_valid_s, mylast);
-  }
-  if (warp >= kSendWarp0 && warp < kFinWarp0) {
-    // each sending thread moves its head row h of the latent part into tensor memory
-    // (packed bf16 pairs); rows past the head count are zero, in the rope operand too
-    const int quarter = warp & 3;
-    const int h = quarter * 32 + lane;  // head row == TMEM lane
-    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-    const bool live = h < H;
-    bool good = true;
-    if (lane == 0) good = mbar_wait(q_tma, 0, abort_flag, p.err);
-    good = __shfl_sync(0xffffffffu, good, 0);
-#pragma unroll 1
-    for (int q = 0; q < 4; ++q) {
-      uint32_t w[32];
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const uint4 x = (live && good) ? *(const uint4*)(qstage + q * kQRegion + h * 128 + ((u ^ (h & 7)) << 4))
-                                       : make_uint4(0, 0, 0, 0);
-        w[4 * u] = x.x;
-        w[4 * u + 1] = x.y;
-        w[4 * u + 2] = x.z;
-        w[4 * u + 3] = x.w;
-      }
-      tmem_st32(tmem + lane_off + kColQl + 32 * q, w);
-    }
-    if (!live) {
-#pragma unroll
-      for (int v = 0; v < 4; ++v) *(uint4*)(qrope + h * 64 + (v << 4)) = make_uint4(0, 0, 0, 0);
-    }
-    fence_proxy_async_smem();  // visible to the MMA (async proxy)
-    tmem_st_wait();
-    tc_fence_before();
-    __syncwarp();
-    if (lane == 0) mbar_arrive(q_ready);
   }
   tc_fence_before();
   __syncthreads();
