@@ -127,8 +127,9 @@ __device__ __forceinline__ void find_bin1024(const uint32_t* hist, uint32_t rema
 }
 
 // kCluster: CTAs per row (the launch's cluster dimension).  kPerSm: CTAs the register
-// budget lets one SM hold -- 4 for launches of many short rows (a prefill), where the
-// rows' latency chains overlap across CTAs, else 3 (fewer registers spill nothing).
+// budget lets one SM hold -- 5 (48 registers) for launches of many short rows (a
+// prefill), where the rows' latency chains overlap across CTAs, else 3 (80 registers:
+// the lowest latency per row).  (Six per SM spills.)
 template <int kCluster, int kPerSm = 3>
 __global__ void __launch_bounds__(kThreads, kPerSm) topk_cluster_kernel(TopkParams p) {
   // candidates one CTA may put in the pool (clusters of 16 pool twice as many, so that a
@@ -537,14 +538,14 @@ cudaError_t launch_topk(const TopkParams& p, int32_t max_visible, cudaStream_t s
   const int cl = max_visible <= kBlock ? 1 : max_visible <= 2 * kBlock ? 2 : max_visible <= 4 * kBlock ? 4
                : max_visible <= 8 * kBlock ? 8 : 16;
   const dim3 b(kThreads);
-  // more rows than three CTAs per SM hold at once: the four-per-SM variant
+  // more rows than three CTAs per SM hold at once: the five-per-SM variant
   const bool many = (int64_t)p.tv.n_tokens * cl > 3 * (int64_t)device_sm_count();
   switch (cl) {
     case 1:
-      return many ? launch_pdl_cluster(topk_cluster_kernel<1, 4>, dim3(1, p.tv.n_tokens), b, 0, s, 1u, p)
+      return many ? launch_pdl_cluster(topk_cluster_kernel<1, 5>, dim3(1, p.tv.n_tokens), b, 0, s, 1u, p)
                   : launch_pdl_cluster(topk_cluster_kernel<1>, dim3(1, p.tv.n_tokens), b, 0, s, 1u, p);
     case 2:
-      return many ? launch_pdl_cluster(topk_cluster_kernel<2, 4>, dim3(2, p.tv.n_tokens), b, 0, s, 2u, p)
+      return many ? launch_pdl_cluster(topk_cluster_kernel<2, 5>, dim3(2, p.tv.n_tokens), b, 0, s, 2u, p)
                   : launch_pdl_cluster(topk_cluster_kernel<2>, dim3(2, p.tv.n_tokens), b, 0, s, 2u, p);
     case 4: return launch_pdl_cluster(topk_cluster_kernel<4>, dim3(4, p.tv.n_tokens), b, 0, s, 4u, p);
     case 8: return launch_pdl_cluster(topk_cluster_kernel<8>, dim3(8, p.tv.n_tokens), b, 0, s, 8u, p);
