@@ -127,9 +127,9 @@ __device__ __forceinline__ void find_bin1024(const uint32_t* hist, uint32_t rema
 }
 
 // kCluster: CTAs per row (the launch's cluster dimension).  kPerSm: CTAs the register
-// budget lets one SM hold -- 5 (48 registers) for launches of many short rows (a
-// prefill), where the rows' latency chains overlap across CTAs, else 3 (80 registers:
-// the lowest latency per row).  (Six per SM spills.)
+// budget lets one SM hold -- 5 (48 registers) for launches with more CTAs than three
+// per SM hold (a prefill, a multi-token decode), so that more rows' latency chains
+// overlap, else 3 (up to 80 registers: the lowest latency per row).  (Six per SM spills.)
 template <int kCluster, int kPerSm = 3>
 __global__ void __launch_bounds__(kThreads, kPerSm) topk_cluster_kernel(TopkParams p) {
   // candidates one CTA may put in the pool (clusters of 16 pool twice as many, so that a
@@ -547,8 +547,12 @@ cudaError_t launch_topk(const TopkParams& p, int32_t max_visible, cudaStream_t s
     case 2:
       return many ? launch_pdl_cluster(topk_cluster_kernel<2, 5>, dim3(2, p.tv.n_tokens), b, 0, s, 2u, p)
                   : launch_pdl_cluster(topk_cluster_kernel<2>, dim3(2, p.tv.n_tokens), b, 0, s, 2u, p);
-    case 4: return launch_pdl_cluster(topk_cluster_kernel<4>, dim3(4, p.tv.n_tokens), b, 0, s, 4u, p);
-    case 8: return launch_pdl_cluster(topk_cluster_kernel<8>, dim3(8, p.tv.n_tokens), b, 0, s, 8u, p);
+    case 4:
+      return many ? launch_pdl_cluster(topk_cluster_kernel<4, 5>, dim3(4, p.tv.n_tokens), b, 0, s, 4u, p)
+                  : launch_pdl_cluster(topk_cluster_kernel<4>, dim3(4, p.tv.n_tokens), b, 0, s, 4u, p);
+    case 8:
+      return many ? launch_pdl_cluster(topk_cluster_kernel<8, 5>, dim3(8, p.tv.n_tokens), b, 0, s, 8u, p)
+                  : launch_pdl_cluster(topk_cluster_kernel<8>, dim3(8, p.tv.n_tokens), b, 0, s, 8u, p);
     default: {
       static std::atomic<int> allowed[kMaxDevices];  // 1: set, -1: refused on that device
       int dev = 0;
