@@ -172,3 +172,26 @@ def test_workspace_holds_dequantised_keys_for_quantised_prefill():
     args.act = 1  # ReLU: per-head scoring, never row-blocked
     n_relu = dsa.lib.dsa_indexer_workspace_size(C.byref(args), C.byref(cache), C.byref(pages), C.byref(toks))
     assert n_relu == base
+
+
+@pytest.mark.parametrize("T,heads", [(32, 128), (8, 128), (8, 5), (2, 16), (200, 128)])
+def test_attention_workspace_holds_split_partials_only_beyond_two_splits(T, heads):
+    """The attention splits each token's K selected rows over s = min(SMs / (2 T), ceil(K/64),
+    16) CTA pairs (at least 1), in whole 64-row tiles; one or two splits need no workspace
+    beyond the 256-byte header (two merge inside their cluster), more keep f32 partials
+    [T, S, 2, 256, HP] and log2-sum-exps [T, S, 2, HP] (HP = heads rounded up to 4, each
+    part 256-byte aligned).  S is recomputed from the split length, so no split is empty."""
+    lens = (4000,) * T
+    pages, toks, cache, args, keep = _structs(B=T, maxp=64, lens=lens)
+    sargs = dsa.SfaArgs(FAKE, heads, 0.04)
+    K = 2048
+    n = dsa.lib.dsa_sparse_attn_workspace_size(C.byref(sargs), C.byref(pages), C.byref(toks), K)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count if torch.cuda.is_available() else 148
+    tiles = (K + 63) // 64
+    s = max(1, min(sms // (2 * T), tiles, 16))
+    split_len = -(-tiles // s) * 64
+    S = -(-(tiles * 64) // split_len)
+    a256 = lambda x: (x + 255) // 256 * 256
+    hp = (heads + 3) // 4 * 4
+    want = 256 if S <= 2 else 256 + a256(T * S * hp * 512 * 4) + a256(T * S * 2 * hp * 4)
+    assert n == want
